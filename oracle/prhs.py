@@ -1,0 +1,219 @@
+"""fp64 restatement of the PrHS decode path (test infrastructure only).
+
+Source throughout: "Near-Oracle KV Selection via Pre-hoc Sparsity for
+Long-Context Inference" (arXiv 2602.08329), abstract, Table I (notation),
+Fig. 2, Fig. 4, Fig. 8, Fig. 9, Table VIII. The pages print no formula; each
+function states the plain definition it takes and the reading behind it.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------- #
+# input decoding
+# --------------------------------------------------------------------------- #
+def widen(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Stored float32 values or bfloat16 bit patterns -> exact float64."""
+    if dtype == "f32":
+        return np.asarray(a, dtype=np.float32).astype(np.float64)
+    bits = np.asarray(a, dtype=np.uint16).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------- #
+# attention weights (Table I: A(.), K, q, d)
+# --------------------------------------------------------------------------- #
+def scores(q: np.ndarray, K: np.ndarray, scale: float) -> np.ndarray:
+    """Attention logits s_i = scale * <q, k_i> for every cached key i.
+
+    Table I names the attention weight A(.) over the KV cache; the scaled dot
+    product with scale = 1/sqrt(d) is the standard transformer logit (reading:
+    no positional rotation is applied, the synthetic keys are post-position).
+    """
+    return scale * (np.asarray(K, np.float64) @ np.asarray(q, np.float64))
+
+
+def softmax(s: np.ndarray) -> np.ndarray:
+    """A_i = exp(s_i - m) / sum_j exp(s_j - m), m = max_j s_j (Table I, A(.))."""
+    s = np.asarray(s, np.float64)
+    e = np.exp(s - s.max())
+    return e / e.sum()
+
+
+def logsumexp(s: np.ndarray) -> float:
+    """Natural-log partition function: m + log sum_i exp(s_i - m)."""
+    s = np.asarray(s, np.float64)
+    m = s.max()
+    return float(m + np.log(np.exp(s - m).sum()))
+
+
+# --------------------------------------------------------------------------- #
+# top-N oracle selector and dropped mass (abstract; Table I S, S_t, N, tau, delta)
+# --------------------------------------------------------------------------- #
+def top_n(s: np.ndarray, N: int) -> np.ndarray:
+    """Index set S_t of the N largest logits, returned in ascending order.
+
+    The abstract's "top-k oracle" keeps the N (Table I: KV budget N) keys with
+    the largest attention weights; ranking by the logit gives the same order
+    as ranking by A_i. Reading: ties go to the lowest index; N >= t keeps all.
+    """
+    s = np.asarray(s, np.float64)
+    t = s.shape[0]
+    if N >= t:
+        return np.arange(t, dtype=np.int64)
+    order = np.argsort(-s, kind="stable")     # stable: equal logits keep index order
+    return np.sort(order[:N])
+
+
+def dropped_mass(s: np.ndarray, S: np.ndarray) -> float:
+    """delta(S) = sum of the attention weights A_i of the keys i not in S.
+
+    Abstract: "the attention mass of discarded entries"; Table I: tau(.) the
+    retained mass and delta(.) = 1 - tau(.) the dropped mass. Summed over
+    the complement directly (not as 1 - tau) so small masses keep precision.
+    """
+    A = softmax(s)
+    keep = np.zeros(A.shape[0], bool)
+    keep[np.asarray(S, np.int64)] = True
+    return float(A[~keep].sum())
+
+
+# --------------------------------------------------------------------------- #
+# critical-index-set reuse (Fig. 2, Fig. 4, Fig. 8, Table VIII)
+# --------------------------------------------------------------------------- #
+def cosine(q: np.ndarray, qa: np.ndarray) -> float | None:
+    """Cosine similarity <q, qa> / (|q| |qa|); None when either norm is 0."""
+    q = np.asarray(q, np.float64)
+    qa = np.asarray(qa, np.float64)
+    den = np.sqrt(q @ q) * np.sqrt(qa @ qa)
+    if den == 0.0:
+        return None
+    return float((q @ qa) / den)
+
+
+def cis_gate(q: np.ndarray, qa: np.ndarray, tau: float) -> tuple[float | None, bool]:
+    """Share the anchor's critical-index set iff sim(q, q_a) >= tau.
+
+    Fig. 8 defines triggering as sim(q, q') >= tau; Fig. 2 and Table VIII use
+    tau = 0.8. Reading: a zero-norm query never shares.
+    """
+    c = cosine(q, qa)
+    return c, (c is not None and c >= tau)
+
+
+def dilate(S: np.ndarray, w: int, t: int) -> np.ndarray:
+    """Dilated set: union over i in S of [i - w, i + w], clipped to [0, t).
+
+    Fig. 4 ("Critical-index set (CIS) dilation") widens the shared set around
+    its indices so that neighbouring keys of a cluster are covered for later
+    queries; Table VIII's radius r (r = 2 raises the average processed tokens
+    from 131 to 167) is read as this +/- w. Result sorted, without repeats,
+    not truncated back to N.
+    """
+    mask = np.zeros(t, bool)
+    for i in np.asarray(S, np.int64):
+        mask[max(0, i - w):min(t, i + w + 1)] = True
+    return np.nonzero(mask)[0].astype(np.int64)
+
+
+# --------------------------------------------------------------------------- #
+# attention over a selected set (abstract; Table V caption, sparse kernel)
+# --------------------------------------------------------------------------- #
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, S: np.ndarray,
+              scale: float) -> tuple[np.ndarray, float]:
+    """Exact softmax attention restricted to the keys in S.
+
+    out = sum_{i in S} p_i v_i with p_i = exp(s_i - lse_S) and
+    lse_S = log sum_{i in S} exp(s_i) (weights renormalised over S).
+    """
+    S = np.asarray(S, np.int64)
+    s = scale * (np.asarray(K, np.float64)[S] @ np.asarray(q, np.float64))
+    m = s.max()
+    p = np.exp(s - m)
+    l = p.sum()
+    out = (p @ np.asarray(V, np.float64)[S]) / l
+    return out, float(m + np.log(l))
+
+
+def dense_attention(q, K, V, scale):
+    """Attention over every cached key (the dense baseline of Table IV)."""
+    return attention(q, K, V, np.arange(np.asarray(K).shape[0]), scale)
+
+
+# --------------------------------------------------------------------------- #
+# multi-step decode with CIS reuse
+# --------------------------------------------------------------------------- #
+@dataclass
+class HeadStep:
+    reuse: bool                 # this step shared the anchor's set
+    cos: float | None           # sim(q_s, q_anchor); None on step 0 / zero norm
+    S: np.ndarray               # index set attended at this step (ascending)
+    anchor_S: np.ndarray        # anchor's undilated top-N set after this step
+    delta: float | None         # dropped mass of the fresh top-N set (fresh steps)
+    delta_used: float           # dropped mass of S under the current query
+    s_nth: float | None         # N-th largest logit (fresh steps, N < t)
+    out: np.ndarray             # attention output over S
+    lse: float
+    scores: np.ndarray | None = None
+
+
+def decode_head(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, N: int, w: int,
+                tau: float, scale: float, keep_scores: bool = False) -> list[HeadStep]:
+    """One head through a sequence of decode queries with CIS reuse.
+
+    Reading of Fig. 4 ("critical tokens from query 405 are shared to queries
+    406 and 407") and Fig. 8 (pairs (q, q') for which sharing triggers): the
+    first query retrieves; a later query whose similarity to the last
+    retrieving query (the anchor) is >= tau attends the anchor's top-N set
+    dilated by +/- w; otherwise it retrieves and becomes the new anchor.
+    Dilation is applied to the anchor set once, never compounded.
+    """
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    t = K.shape[0]
+    anchor_S = None
+    anchor_q = None
+    rec = []
+    for q in np.asarray(q_steps, np.float64):
+        c, reuse = (None, False) if anchor_S is None else cis_gate(q, anchor_q, tau)
+        s = scores(q, K, scale)
+        delta = s_nth = None
+        if reuse:
+            S = dilate(anchor_S, w, t)
+        else:
+            S = top_n(s, N)
+            delta = dropped_mass(s, S)
+            if N < t:
+                s_nth = float(np.sort(s)[::-1][N - 1])
+            anchor_S, anchor_q = S, q
+        out, lse = attention(q, K, V, S, scale)
+        rec.append(HeadStep(reuse=reuse, cos=c, S=S, anchor_S=anchor_S, delta=delta,
+                            delta_used=dropped_mass(s, S), s_nth=s_nth, out=out, lse=lse,
+                            scores=s if keep_scores else None))
+    return rec
+
+
+def decode_workload(wl, heads=None, steps=None, keep_scores=False):
+    """Run decode_head over (b, query head) pairs of a ``workloads.Workload``.
+
+    Query head hq reads KV head hq // (Hq / Hkv) (consecutive grouping, the
+    usual grouped-query layout). Returns {(b, hq): [HeadStep, ...]}.
+    """
+    G = wl.Hq // wl.Hkv
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.Hq)] if heads is None else heads
+    nsteps = wl.steps if steps is None else steps
+    res = {}
+    cache = {}
+    for b, hq in heads:
+        kvh = hq // G
+        if (b, kvh) not in cache:
+            cache = {(b, kvh): (widen(wl.logical_rows("K", b, kvh), wl.dtype),
+                                widen(wl.logical_rows("V", b, kvh), wl.dtype))}
+        K, V = cache[(b, kvh)]
+        qs = widen(wl.q[:nsteps, b, hq], wl.dtype)
+        res[(b, hq)] = decode_head(qs, K, V, int(wl.budget[b]), wl.w, wl.tau, wl.scale,
+                                   keep_scores=keep_scores)
+    return res

@@ -1,0 +1,373 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each ``check_*`` helper reads the oracle functions through the module object
+at call time, so the mutation tests at the bottom can plant a plausible
+mistake in the oracle and confirm that some pin catches it.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle.prhs as P
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *rest = line.split()
+            vals[key] = [float(x) for x in rest]
+    return vals
+
+
+# --------------------------------------------------------------------------- #
+# pin helpers
+# --------------------------------------------------------------------------- #
+def check_softmax_hand():
+    g = _read_golden("softmax_hand.txt")
+    s = np.log(np.array(g["logits_exp"]))
+    assert np.allclose(P.softmax(s), g["weights"], rtol=0, atol=1e-15)
+    assert abs(P.logsumexp(s) - math.log(g["lse_exp"][0])) < 1e-14
+    S = P.top_n(s, int(g["N"][0]))
+    assert S.tolist() == [int(x) for x in g["topN"]]
+    assert abs(P.dropped_mass(s, S) - g["delta"][0]) < 1e-15
+
+
+def check_softmax_invariants(rng):
+    s = rng.normal(size=257) * 5
+    A = P.softmax(s)
+    assert abs(A.sum() - 1.0) < 1e-12 and (A >= 0).all()
+    assert np.allclose(P.softmax(s + 123.0), A, rtol=1e-12, atol=0)   # shift invariance
+    # the largest logit gets the largest weight
+    assert A.argmax() == s.argmax()
+
+
+def check_topn_bruteforce(rng):
+    """delta(top-N) is the minimum over every size-N subset (t <= 12)."""
+    for t in (1, 5, 9, 12):
+        for trial in range(4):
+            s = rng.normal(size=t) * 2
+            if trial == 3:
+                s = np.round(s)                  # force ties
+            for N in range(1, t + 1):
+                S = P.top_n(s, N)
+                assert len(S) == N and np.all(np.diff(S) > 0)
+                d = P.dropped_mass(s, S)
+                best = min(P.dropped_mass(s, np.array(c)) for c in
+                           itertools.combinations(range(t), N))
+                assert d <= best + 1e-15
+                # ties go to the lowest index: among the optimal subsets it is the
+                # lexicographically smallest one once sorted by descending logit
+                optimal = [c for c in itertools.combinations(range(t), N)
+                           if P.dropped_mass(s, np.array(c)) <= best + 1e-15]
+                if trial == 3:
+                    thr = np.sort(s)[::-1][N - 1]
+                    above = set(np.nonzero(s > thr)[0])
+                    ties = sorted(np.nonzero(s == thr)[0])
+                    expect = sorted(above | set(ties[:N - len(above)]))
+                    assert S.tolist() == expect
+                    assert tuple(expect) in optimal
+
+
+def check_topn_ties():
+    s = np.array([1.0, 3.0, 3.0, 2.0, 3.0])
+    assert P.top_n(s, 2).tolist() == [1, 2]
+    assert P.top_n(s, 4).tolist() == [1, 2, 3, 4]
+    assert P.top_n(np.zeros(7), 3).tolist() == [0, 1, 2]
+    assert P.top_n(np.array([0.0, -0.0, 0.0]), 1).tolist() == [0]
+    assert P.top_n(s, 5).tolist() == [0, 1, 2, 3, 4]
+    assert P.top_n(s, 9).tolist() == [0, 1, 2, 3, 4]
+
+
+def check_delta_properties(rng):
+    s = rng.normal(size=300) * 3
+    t = s.size
+    assert P.dropped_mass(s, np.arange(t)) == 0.0
+    assert abs(P.dropped_mass(s, np.array([], np.int64)) - 1.0) < 1e-12
+    prev = 1.0
+    for N in (1, 10, 50, 150, 299, 300):
+        d = P.dropped_mass(s, P.top_n(s, N))
+        assert 0.0 <= d <= 1.0 and d <= prev + 1e-15
+        prev = d
+    # delta = 1 - exp(lse_S - lse_full), with lse_S from the attention routine
+    K = rng.normal(size=(t, 16))
+    V = rng.normal(size=(t, 16))
+    q = rng.normal(size=16)
+    sc = P.scores(q, K, 0.25)
+    S = P.top_n(sc, 40)
+    _, lse_S = P.attention(q, K, V, S, 0.25)
+    _, lse_F = P.dense_attention(q, K, V, 0.25)
+    assert abs(P.dropped_mass(sc, S) - (1.0 - math.exp(lse_S - lse_F))) < 1e-12
+
+
+def check_attention_identities(rng):
+    t, d = 200, 32
+    K = rng.normal(size=(t, d))
+    V = rng.normal(size=(t, d))
+    q = rng.normal(size=d)
+    scale = 1 / math.sqrt(d)
+    o_all, l_all = P.attention(q, K, V, np.arange(t), scale)
+    o_d, l_d = P.dense_attention(q, K, V, scale)
+    assert np.allclose(o_all, o_d, atol=1e-14) and abs(l_all - l_d) < 1e-14
+    # convex split: o_full = (1 - delta) o_S + delta o_Sc; lse_full = logaddexp
+    sc = P.scores(q, K, scale)
+    S = P.top_n(sc, 37)
+    Sc = np.setdiff1d(np.arange(t), S)
+    oS, lS = P.attention(q, K, V, S, scale)
+    oC, lC = P.attention(q, K, V, Sc, scale)
+    delta = P.dropped_mass(sc, S)
+    assert np.allclose(o_d, (1 - delta) * oS + delta * oC, atol=1e-13)
+    assert abs(l_d - np.logaddexp(lS, lC)) < 1e-13
+    # equal keys -> uniform weights -> mean of V; lse = s + log t
+    Ke = np.tile(rng.normal(size=d), (t, 1))
+    oe, le = P.dense_attention(q, Ke, V, scale)
+    assert np.allclose(oe, V.mean(0), atol=1e-13)
+    assert abs(le - (scale * Ke[0] @ q + math.log(t))) < 1e-12
+    # one dominant key -> its value row
+    Kd = K.copy()
+    Kd[17] = 200.0 * q / np.linalg.norm(q)
+    od, _ = P.dense_attention(q, Kd, V, scale)
+    assert np.allclose(od, V[17], atol=1e-9)
+
+
+def check_attention_vs_torch_sdpa(rng):
+    torch = pytest.importorskip("torch")
+    B, H, t, d = 2, 3, 97, 64
+    q = rng.normal(size=(B, H, 1, d))
+    K = rng.normal(size=(B, H, t, d))
+    V = rng.normal(size=(B, H, t, d))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(K), torch.from_numpy(V)).numpy()
+    for b in range(B):
+        for h in range(H):
+            o, _ = P.dense_attention(q[b, h, 0], K[b, h], V[b, h], 1 / math.sqrt(d))
+            assert np.allclose(o, ref[b, h, 0], atol=1e-12)
+    # restricted to a subset = SDPA with a boolean mask
+    S = np.array([3, 4, 5, 40, 41, 90])
+    mask = np.zeros((1, 1, 1, t), bool)
+    mask[..., S] = True
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(K), torch.from_numpy(V),
+        attn_mask=torch.from_numpy(mask)).numpy()
+    o, _ = P.attention(q[1, 2, 0], K[1, 2], V[1, 2], S, 1 / math.sqrt(d))
+    assert np.allclose(o, ref[1, 2, 0], atol=1e-12)
+
+
+def check_dilation_golden():
+    g = _read_golden("fig4_dilation.txt")
+    out = P.dilate(np.array(g["input"], np.int64), int(g["w"][0]), int(g["t"][0]))
+    assert out.tolist() == [int(x) for x in g["expected"]]
+
+
+def check_dilation_bruteforce(rng):
+    for trial in range(60):
+        t = int(rng.integers(1, 80))
+        n = int(rng.integers(0, t + 1))
+        w = int(rng.integers(0, 6))
+        S = np.sort(rng.choice(t, size=n, replace=False))
+        out = P.dilate(S, w, t)
+        ref = sorted({j for i in S for j in range(i - w, i + w + 1) if 0 <= j < t})
+        assert out.tolist() == ref
+        assert set(S.tolist()) <= set(out.tolist())
+        assert len(out) <= min(t, n * (2 * w + 1))
+        if w == 0:
+            assert out.tolist() == S.tolist()
+    # a contiguous run [a, b] -> [max(0, a - w), min(t - 1, b + w)]
+    assert P.dilate(np.arange(1, 4), 3, 10).tolist() == list(range(0, 7))
+    assert P.dilate(np.arange(7, 10), 2, 10).tolist() == list(range(5, 10))
+
+
+def check_cosine_gate(rng):
+    scipy_dist = pytest.importorskip("scipy.spatial.distance")
+    for _ in range(20):
+        a, b = rng.normal(size=64), rng.normal(size=64)
+        assert abs(P.cosine(a, b) - (1 - scipy_dist.cosine(a, b))) < 1e-13
+    q = rng.normal(size=32)
+    assert P.cis_gate(q, q, 0.8)[1] and abs(P.cosine(q, q) - 1) < 1e-15
+    c, r = P.cis_gate(q, -q, 0.8)
+    assert not r and abs(c + 1) < 1e-15
+    assert P.cis_gate(np.zeros(4), np.ones(4), -2.0) == (None, False)
+    # boundary: cosine exactly equal to tau triggers sharing (">=")
+    assert P.cis_gate(np.array([1.0, 0.0]), np.array([0.8, 0.6]), 0.8)[1]
+    assert not P.cis_gate(np.array([1.0, 0.0]), np.array([0.6, 0.8]), 0.8)[1]
+
+
+def check_decode_schedule(rng):
+    t, d, N, w = 120, 16, 10, 1
+    K = rng.normal(size=(t, d))
+    V = rng.normal(size=(t, d))
+    qs = rng.normal(size=(6, d))
+    sc = 1 / math.sqrt(d)
+    # tau above 1: every step retrieves its own top-N
+    rec = P.decode_head(qs, K, V, N, w, 1.5, sc)
+    for q, r in zip(qs, rec):
+        assert not r.reuse
+        assert r.S.tolist() == P.top_n(P.scores(q, K, sc), N).tolist()
+        assert abs(r.delta - r.delta_used) < 1e-15
+    # tau below -1: step 0 retrieves, later steps share its dilated set
+    rec = P.decode_head(qs, K, V, N, w, -1.5, sc)
+    S0 = P.top_n(P.scores(qs[0], K, sc), N)
+    assert not rec[0].reuse and rec[0].S.tolist() == S0.tolist()
+    for r in rec[1:]:
+        assert r.reuse and r.S.tolist() == P.dilate(S0, w, t).tolist()
+        assert r.anchor_S.tolist() == S0.tolist()
+    # attended output of each step equals attention over the attended set
+    for q, r in zip(qs, rec):
+        o, l = P.attention(q, K, V, r.S, sc)
+        assert np.allclose(o, r.out) and abs(l - r.lse) < 1e-14
+
+
+def check_widen():
+    bits = np.array([0x3F80, 0xC020, 0x0000, 0x8000, 0x7F7F], np.uint16)
+    v = P.widen(bits, "bf16")
+    assert v[0] == 1.0 and v[1] == -2.5 and v[2] == 0.0 and v[4] == 3.3895313892515355e38
+    assert P.widen(np.array([0.1], np.float32), "f32")[0] == float(np.float32(0.1))
+
+
+# --------------------------------------------------------------------------- #
+# tests
+# --------------------------------------------------------------------------- #
+@pytest.fixture
+def rng():
+    return np.random.default_rng(1234)
+
+
+def test_softmax_hand():
+    check_softmax_hand()
+
+
+def test_softmax_invariants(rng):
+    check_softmax_invariants(rng)
+
+
+def test_topn_bruteforce(rng):
+    check_topn_bruteforce(rng)
+
+
+def test_topn_ties():
+    check_topn_ties()
+
+
+def test_delta_properties(rng):
+    check_delta_properties(rng)
+
+
+def test_attention_identities(rng):
+    check_attention_identities(rng)
+
+
+def test_attention_vs_torch_sdpa(rng):
+    check_attention_vs_torch_sdpa(rng)
+
+
+def test_dilation_golden():
+    check_dilation_golden()
+
+
+def test_dilation_bruteforce(rng):
+    check_dilation_bruteforce(rng)
+
+
+def test_cosine_gate(rng):
+    check_cosine_gate(rng)
+
+
+def test_decode_schedule(rng):
+    check_decode_schedule(rng)
+
+
+def test_widen():
+    check_widen()
+
+
+# --------------------------------------------------------------------------- #
+# planted mistakes: each must be caught by at least one pin
+# --------------------------------------------------------------------------- #
+def _caught(fn, *args):
+    try:
+        fn(*args)
+    except AssertionError:
+        return True
+    return False
+
+
+def test_mutation_topn_highest_index_ties(monkeypatch, rng):
+    def bad(s, N):
+        s = np.asarray(s, np.float64)
+        if N >= s.size:
+            return np.arange(s.size)
+        order = np.argsort(-s[::-1], kind="stable")
+        return np.sort(s.size - 1 - order[:N])
+    monkeypatch.setattr(P, "top_n", bad)
+    assert _caught(check_topn_ties)
+
+
+def test_mutation_topn_off_by_one(monkeypatch, rng):
+    good = P.top_n
+    monkeypatch.setattr(P, "top_n", lambda s, N: good(s, max(N - 1, 0)) if N < len(s) else good(s, N))
+    assert _caught(check_softmax_hand) and _caught(check_topn_bruteforce, rng)
+
+
+def test_mutation_delta_retained(monkeypatch):
+    good = P.dropped_mass
+    monkeypatch.setattr(P, "dropped_mass", lambda s, S: 1.0 - good(s, S))
+    assert _caught(check_softmax_hand)
+
+
+def test_mutation_scores_missing_scale(monkeypatch, rng):
+    monkeypatch.setattr(P, "scores", lambda q, K, scale: np.asarray(K) @ np.asarray(q))
+    assert _caught(check_delta_properties, rng)
+
+
+def test_mutation_attention_unnormalised(monkeypatch, rng):
+    good = P.attention
+
+    def bad(q, K, V, S, scale):
+        o, l = good(q, K, V, S, scale)
+        return o * len(S), l
+    monkeypatch.setattr(P, "attention", bad)
+    assert _caught(check_attention_identities, rng)
+
+
+def test_mutation_attention_transposed_value(monkeypatch, rng):
+    """Weights applied to K instead of V must fail the SDPA pin."""
+    good = P.attention
+    monkeypatch.setattr(P, "attention", lambda q, K, V, S, scale: good(q, K, K, S, scale))
+    assert _caught(check_attention_vs_torch_sdpa, rng)
+
+
+def test_mutation_dilation_radius(monkeypatch):
+    good = P.dilate
+    monkeypatch.setattr(P, "dilate", lambda S, w, t: good(S, max(w - 1, 0), t))
+    assert _caught(check_dilation_golden)
+
+
+def test_mutation_dilation_no_clip(monkeypatch, rng):
+    def bad(S, w, t):
+        return np.array(sorted({j for i in S for j in range(i - w, i + w + 1) if j >= 0}))
+    monkeypatch.setattr(P, "dilate", bad)
+    assert _caught(check_dilation_bruteforce, rng)
+
+
+def test_mutation_gate_strict(monkeypatch):
+    good = P.cosine
+
+    def bad(q, qa, tau):
+        c = good(q, qa)
+        return c, (c is not None and c > tau)
+    monkeypatch.setattr(P, "cis_gate", bad)
+    assert _caught(check_cosine_gate, np.random.default_rng(0))
+
+
+def test_mutation_gate_sign(monkeypatch):
+    good = P.cosine
+    monkeypatch.setattr(P, "cosine", lambda q, qa: None if good(q, qa) is None else -good(q, qa))
+    assert _caught(check_cosine_gate, np.random.default_rng(0))

@@ -1,0 +1,441 @@
+"""Benchmark of the PrHS sparse decode path on one GB300 (or N replicas).
+
+One bench step = one full decode sequence of the workload through the C ABI:
+for every decode query, CIS gate + dilation, scoring and top-N selection for
+the heads that retrieve, and sparse attention for every head (all kernels of
+the hot path). The per-query launches are captured once in a CUDA graph and
+replayed; inputs are resident in HBM. Between consecutive decode queries the
+KV cache alternates over enough identical copies that the copies together
+exceed twice the L2, so no query finds the cache it reads in L2.
+
+Prints one JSON line (metric: query-heads per second). ``--impl reference``
+times the fp64 CPU oracle instead, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle must run on a known number of cores: one BLAS thread
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import math
+import signal
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode attn: query-heads/s and achieved HBM GB/s vs 8 TB/s at N/t"
+UNIT = "query-heads/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="llama2_7b_mha",
+                   help="workload preset (tiny, llama2_7b_mha, mistral_7b_gqa, paged_serving, long_context)")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="host time budget of the CPU-oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def workload_label(wl) -> str:
+    t = (f"t={int(wl.seq_lens[0])}" if len(set(wl.seq_lens.tolist())) == 1
+         else f"t~U[{int(wl.seq_lens.min())},{int(wl.seq_lens.max())}]")
+    N = (f"N={int(wl.budget[0])}" if len(set(wl.budget.tolist())) == 1 else "N=t_b/16")
+    paged = f" paged{wl.block_size}" if wl.paged else ""
+    return (f"{wl.name}: B{wl.B} Hq{wl.Hq} Hkv{wl.Hkv} d{wl.d} {wl.dtype} {t}{paged}, "
+            f"{wl.steps} decode queries, {N}, w={wl.w}, tau={wl.tau}")
+
+
+# --------------------------------------------------------------------------- #
+# CPU oracle timing (baseline / reference arm)
+# --------------------------------------------------------------------------- #
+def oracle_sample(wl, seconds: float, start_head: int = 0):
+    """Decode heads with the fp64 oracle until `seconds` of host time pass.
+    Returns (query-heads done, elapsed s, heads used)."""
+    import oracle.prhs as P
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.Hq)]
+    done, used = 0, 0
+    t0 = time.perf_counter()
+    i = start_head
+    while True:
+        b, h = heads[i % len(heads)]
+        P.decode_workload(wl, heads=[(b, h)])
+        done += wl.steps
+        used += 1
+        i += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return done, time.perf_counter() - t0, used
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from workloads import preset
+    wl = preset(args.config, seed=0)
+    per_step = max(1.0, min(6.0, 120.0 / max(1, args.steps + args.warmup)))
+    for w in range(args.warmup):
+        oracle_sample(wl, per_step, start_head=w)
+    done_tot, el_tot, heads_tot = 0, 0.0, 0
+    for k in range(args.steps):
+        d, el, used = oracle_sample(wl, per_step, start_head=k)
+        done_tot += d
+        el_tot += el
+        heads_tot += used
+    value = done_tot / el_tot
+    sample = (f"{heads_tot} (sequence, head) decode runs of {wl.steps} queries each, "
+              f"~{per_step:.1f} s per step, fp64 numpy, 1 thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el_tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator, workloads/)",
+            "config": {"workload": workload_label(wl)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- #
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.send_signal(signal.SIGTERM)
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() == "active"})
+        load = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": float(np.median(load)) if load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Largest value of x over all ranks (the slowest replica sets the time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peak_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of each kernel from the committed ncu summary."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    try:
+        with open(path) as f:
+            for line in f:
+                line = line.split("#", 1)[0].strip()
+                if "=" in line:
+                    k, v = line.split("=", 1)
+                    out[k.strip()] = float(v)
+    except OSError:
+        pass
+    return out
+
+
+# --------------------------------------------------------------------------- #
+# our arm
+# --------------------------------------------------------------------------- #
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    import __graft_entry__ as entry
+    entry.build()
+    import sparse_kv_selection_gb300 as S
+    from workloads import preset
+    from workloads.torch_io import upload
+
+    wl = preset(args.config, seed=rank)
+    dev = upload(wl)
+    Sq, B, Hq, d = wl.steps, wl.B, wl.Hq, wl.d
+    kv_bytes = wl.kv_bytes()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    R = max(1, math.ceil(2 * l2 / kv_bytes))
+    kvs = []
+    for r in range(R):
+        k = dev["k"] if r == 0 else dev["k"].clone()
+        v = dev["v"] if r == 0 else dev["v"].clone()
+        kvs.append(S.KVCache(k, v, dev["seq_lens"], Hq, block_table=dev["block_table"]))
+    varied = len(set(wl.budget.tolist())) > 1
+    N = 0 if varied else int(wl.budget[0])
+    nb = dev["budget"] if varied else None
+    nmax = int(wl.budget.max())
+    acap = max(1, min(nmax, kvs[0].t_max))
+    cap = max(1, min(kvs[0].t_max, acap * (2 * wl.w + 1)))
+    i32 = dict(device="cuda", dtype=torch.int32)
+    anchor_idx = torch.zeros(B, Hq, acap, **i32)
+    anchor_n = torch.zeros(B, Hq, **i32)
+    q_anchor = torch.zeros_like(dev["q"][0])
+    idx = torch.zeros(B, Hq, cap, **i32)
+    n_sel = torch.zeros(Sq, B, Hq, **i32)
+    reuse = torch.zeros(Sq, B, Hq, device="cuda", dtype=torch.uint8)
+    delta = torch.full((Sq, B, Hq), float("nan"), device="cuda")
+    out = torch.zeros(Sq, B, Hq, d, device="cuda")
+    lse = torch.zeros(Sq, B, Hq, device="cuda")
+    ws = S.make_workspace(kvs[0], cap)
+    q = dev["q"]
+    scale = wl.scale
+
+    def enqueue(ev=None):
+        anchor_n.zero_()
+        for s in range(Sq):
+            kv = kvs[s % R]
+            if ev is not None:
+                ev[s][0].record()
+            S.cis_dilate(kv, anchor_idx, anchor_n, q[s], q_anchor, wl.w, wl.tau, idx, n_sel[s],
+                         reuse[s])
+            if ev is not None:
+                ev[s][1].record()
+            S.binding.score(kv, q[s], scale, ws, head_skip=reuse[s])
+            if ev is not None:
+                ev[s][2].record()
+            S.binding.select(kv, q[s], N, idx, n_sel[s], delta[s], ws, n_budget=nb,
+                             head_skip=reuse[s], anchor_idx=anchor_idx, anchor_n=anchor_n,
+                             q_anchor=q_anchor)
+            if ev is not None:
+                ev[s][3].record()
+            S.sparse_attn(kv, q[s], scale, idx, n_sel[s], out[s], lse[s], ws)
+            if ev is not None:
+                ev[s][4].record()
+
+    launches_per_step = 4 * Sq
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        enqueue()                    # eager warm-up: resolves per-device state
+    torch.cuda.synchronize()
+    assert S.last_error() == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        enqueue()
+
+    # instrumented copy: timing events between the kernels of every query
+    try:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+               for _ in range(Sq)]
+        graph_i = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_i, stream=stream):
+            enqueue(evs)
+    except TypeError:
+        graph_i = None
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---------------- timed region: K decode sequences ----------------
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            t0.record()
+            for _ in range(args.steps):
+                graph.replay()
+            t1.record()
+        torch.cuda.synchronize()
+        barrier()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, "cuda")
+    assert S.last_error() == 0
+    units = B * Hq * Sq * args.steps * world
+    value = units / (elapsed_ms / 1e3)
+
+    # ---------------- per-kernel durations over the same steps ----------------
+    names = ["cis", "score", "select", "sparse_attn"]
+    ktime = {n: 0.0 for n in names}
+    if graph_i is not None:
+        for _ in range(args.steps):
+            graph_i.replay()
+            torch.cuda.synchronize()
+            for s in range(Sq):
+                for i, n in enumerate(names):
+                    ktime[n] += evs[s][i].elapsed_time(evs[s][i + 1])
+    launches = {n: Sq * args.steps for n in names}
+
+    # algorithmic bytes per launch, from the flags and set sizes the run produced
+    r_h = reuse.cpu().numpy().astype(bool)
+    n_h = n_sel.cpu().numpy().astype(np.int64)
+    es = 2 if wl.dtype == "bf16" else 4
+    G = wl.G
+    tlen = wl.seq_lens.astype(np.int64)
+    score_bytes = 0.0
+    for s in range(Sq):
+        fresh_groups = (~r_h[s]).reshape(B, wl.Hkv, G).any(-1)       # [B][Hkv]
+        score_bytes += float((fresh_groups * tlen[:, None]).sum() * d * es)
+        score_bytes += float((~r_h[s]).sum() * d * es)                # q rows
+    score_bytes /= Sq
+    attn_bytes = float((n_h * (2 * d * es + 4)).sum() + Sq * B * Hq * (d * es + 4 * d + 4)) / Sq
+    kb = {"score": score_bytes, "sparse_attn": attn_bytes}
+    peak, peak_kind = measured_peak_gbs()
+    traffic = profiled_traffic()
+    kern = {}
+    for n in names:
+        avg_ms = ktime[n] / launches[n] if launches[n] else None
+        e = {"avg_us": None if not avg_ms else 1e3 * avg_ms,
+             "share": ktime[n] / max(1e-9, sum(ktime.values()))}
+        if n in kb and avg_ms:
+            gbs = kb[n] / (avg_ms / 1e3) / 1e9
+            e.update({"alg_bytes_per_launch": kb[n], "achieved_gbs": gbs,
+                      "frac_of_measured": gbs / peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS})
+        kern[n] = e
+    dom = max(["score", "sparse_attn"], key=lambda n: ktime[n])
+    roof = None
+    if kern[dom]["avg_us"]:
+        ach = kern[dom]["achieved_gbs"]
+        tr = traffic.get(f"{args.config}.{dom}")
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "peak_kind": peak_kind,
+                "frac_of_8tbs": ach / NOMINAL_HBM_GBS,
+                "traffic": tr, "alg_bytes_per_launch": kb[dom]}
+
+    # ---------------- end to end: pinned host queries -> host results ----------------
+    q_host = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    q_host.copy_(q.cpu())
+    outs_dev = (out, lse, delta, reuse, n_sel)
+    outs_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs_dev]
+    h2d = q_host.numel() * q_host.element_size()
+    d2h = sum(x.numel() * x.element_size() for x in outs_host)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            q.copy_(q_host, non_blocking=True)
+            graph.replay()
+            for h, dv in zip(outs_host, outs_dev):
+                h.copy_(dv, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    te0, te1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        te0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        te1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(te0.elapsed_time(te1), world, "cuda")
+    e2e_value = units / (e2e_ms / 1e3)
+
+    # ---------------- CPU oracle on a bounded sample ----------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        done, el, used = oracle_sample(wl, args.cpu_seconds)
+        cpu = {"value": done / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{used} (sequence, head) decode runs x {wl.steps} queries of this "
+                         f"workload in {el:.1f} s, fp64 numpy, 1 thread"}
+
+    if rank == 0:
+        fresh_frac = float((~r_h).mean())
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if wl.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded clustered-key generator, AR(1) correlated queries)",
+            "config": {"workload": workload_label(wl),
+                       "step": f"one decode sequence of {Sq} queries x {B * Hq} heads",
+                       "l2": f"{R} rotating identical KV copies ({R * kv_bytes / 2**20:.0f} MiB >= 2x L2)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "cuda_graph": True, "fresh_retrieval_fraction": fresh_frac,
+                       "mean_n_sel": float(n_h.mean())},
+            "roofline": roof,
+            "kernels": kern,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * prhs.h - C ABI of the GB300 (sm_103a) Pre-hoc Sparsity decode path.
+ *
+ * Source of the operations: "Near-Oracle KV Selection via Pre-hoc Sparsity
+ * for Long-Context Inference" (arXiv 2602.08329): the abstract (top-k oracle
+ * selection before attention, dropped mass delta), Table I (notation: K, V,
+ * t, N, S_t, tau(.), delta(.)), Fig. 2 / Fig. 8 (sharing between queries
+ * whose similarity is >= tau = 0.8), Fig. 4 and Table VIII (critical-index
+ * set dilation, radius r) and the Table V caption (a fused sparse-attention
+ * kernel over the selected KV entries).
+ *
+ * Conventions shared by every call:
+ *  - All array pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no device memory. Scratch comes from a caller workspace sized
+ *    by prhs_workspace_size() and zero-filled once by prhs_workspace_init().
+ *  - Calls are asynchronous on the given stream. Arguments are checked on
+ *    the host before any launch; a bad argument returns PRHS_EINVAL (or
+ *    PRHS_EUNSUPPORTED for a valid but unbuilt shape) and launches nothing.
+ *    prhs_last_message() then describes the failure.
+ *  - Errors found by kernels (an index outside [0, t_b), a page number
+ *    outside the pool, a wait that timed out, a set larger than its row
+ *    capacity) set bits in a device error word; the offending element is
+ *    skipped, nothing faults. prhs_last_error() synchronises the device,
+ *    reads and clears that word.
+ *  - Layouts (row-major, innermost last):
+ *      q, q_anchor   [B][Hq][d]      same element type as the cache
+ *      K, V          contiguous [B][Hkv][t_max][d]
+ *                    or paged   [num_blocks][Hkv][block_size][d]
+ *      idx           [B][Hq][cap]    int32, ascending, n_sel valid entries
+ *      n_sel, n_budget, anchor_n     int32 [B][Hq] (n_budget: [B])
+ *      reuse         uint8 [B][Hq];  delta, lse float [B][Hq]; out float [B][Hq][d]
+ *    Query head h reads KV head h / (Hq / Hkv).
+ *  - Inputs must be finite; NaN or Inf in q, K or V gives undefined results.
+ *  - No call is thread-safe against another call using the same workspace.
+ */
+#ifndef PRHS_H
+#define PRHS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PRHS_OK = 0,
+  PRHS_EINVAL = 1,        /* bad argument (null pointer, size, alignment, capacity) */
+  PRHS_EUNSUPPORTED = 2,  /* head dim / dtype / group size not built */
+  PRHS_EWORKSPACE = 3,    /* workspace null or smaller than prhs_workspace_size() */
+  PRHS_ECUDA = 4,         /* a CUDA runtime call failed (launch, attribute, encode) */
+  PRHS_EDEVICE = 5        /* a kernel reported a data error (see prhs_device_error_bits) */
+} prhs_status;
+
+typedef enum { PRHS_F32 = 0, PRHS_BF16 = 1 } prhs_dtype;
+
+/* device error word bits (prhs_device_error_bits) */
+#define PRHS_DEV_TIMEOUT   1u   /* a bounded barrier wait gave up */
+#define PRHS_DEV_BAD_INDEX 2u   /* idx / anchor entry outside [0, t_b) or not ascending */
+#define PRHS_DEV_BAD_LEN   4u   /* seq_lens[b] outside [0, t_max] */
+#define PRHS_DEV_BAD_BLOCK 8u   /* block_table entry outside [0, num_blocks) */
+#define PRHS_DEV_CAPACITY  16u  /* a result set did not fit its row capacity */
+
+/* KV cache descriptor (Table I: K, V, t; H heads of dimension d).
+ * Host struct; its pointers are device pointers, borrowed for the call only. */
+typedef struct prhs_kv {
+  prhs_dtype dtype;            /* element type of K, V and q */
+  int B;                       /* sequences in the batch */
+  int Hq;                      /* query heads per sequence */
+  int Hkv;                     /* KV heads per sequence; Hq % Hkv == 0, Hq/Hkv in {1,2,4,8} */
+  int d;                       /* head dimension: 64 or 128 */
+  const void* k;               /* K rows, 16-byte aligned */
+  const void* v;               /* V rows, same layout as K */
+  int t_max;                   /* contiguous: keys per (b, kv head) row stride.
+                                  paged: ignored (max_blocks * block_size is used) */
+  const int32_t* seq_lens;     /* [B] cache length t_b of each sequence, 0 <= t_b <= t_max */
+  const int32_t* block_table;  /* NULL: contiguous. else [B][max_blocks] physical page ids */
+  int block_size;              /* paged: keys per page, a positive multiple of 16 */
+  int max_blocks;              /* paged: columns of block_table */
+  int num_blocks;              /* paged: pages in the pool (bounds check) */
+} prhs_kv;
+
+/* Bytes of workspace that every call below needs for this cache and a
+ * per-head set capacity `cap` (scores [B][Hq][t_max] f32 plus split-K
+ * partials and counters). Returns 0 for an invalid descriptor. */
+size_t prhs_workspace_size(const prhs_kv* kv, int cap);
+
+/* Zero-fill the workspace's completion counters (required once after the
+ * workspace is allocated; every later call leaves them zero again). */
+prhs_status prhs_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Top-N oracle selector (abstract: "near-oracle top-k KV selection"; Table I:
+ * S_t, N, delta). For every query head not flagged in head_skip:
+ *   s_i = scale * <q, k_i>, i < t_b;  A = softmax(s);
+ *   S = the N largest s_i (ties -> lowest index), written ascending to idx;
+ *   delta = sum_{i not in S} A_i.
+ * N is `N`, or n_budget[b] when n_budget != NULL. When N >= t_b the set is
+ * all of [0, t_b) and delta = 0. cap >= max budget is required.
+ * head_skip [B][Hq] uint8 (nullable): heads with a nonzero flag are left
+ * untouched (their idx, n_sel and delta rows are not written).
+ * anchor_idx / anchor_n / q_anchor (all nullable together): also copy each
+ * written set, its size and the query into these anchor buffers (the CIS
+ * anchor, row capacity anchor_cap). */
+prhs_status prhs_score_select(const prhs_kv* kv, const void* q, float scale, int N,
+                              const int32_t* n_budget, const uint8_t* head_skip,
+                              int32_t* idx, int32_t* n_sel, int cap, float* delta,
+                              int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
+                              void* q_anchor, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The two halves of prhs_score_select, for callers that time or reuse them
+ * separately. prhs_score writes the logits s_i = scale * <q, k_i> of every
+ * query head not flagged in head_skip into the workspace; prhs_select then
+ * selects from the logits the last prhs_score call on the same workspace left
+ * there (same q, kv and head_skip), with the arguments and results of
+ * prhs_score_select. */
+prhs_status prhs_score(const prhs_kv* kv, const void* q, float scale, const uint8_t* head_skip,
+                       void* ws, size_t ws_bytes, cudaStream_t stream);
+prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* n_budget,
+                        const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
+                        float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
+                        void* q_anchor, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Critical-index-set reuse with dilation (Fig. 2, Fig. 4, Fig. 8, Table VIII).
+ * Per query head: c = <q, q_anchor> / (|q| |q_anchor|) evaluated in float64;
+ * reuse = anchor_n > 0 and |q| |q_anchor| > 0 and c >= tau.
+ * When reuse: idx = union over anchor entries a of [a - w, a + w] clipped to
+ * [0, t_b), ascending without repeats, n_sel its size (<= cap required).
+ * When not: idx and n_sel rows are left untouched. reuse [B][Hq] is always
+ * written. anchor_idx rows must be ascending and inside [0, t_b). */
+prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx,
+                            const int32_t* anchor_n, int anchor_cap, const void* q,
+                            const void* q_anchor, int w, double tau, int32_t* idx,
+                            int32_t* n_sel, int cap, uint8_t* reuse, cudaStream_t stream);
+
+/* Sparse attention over the selected rows (Table V caption: sparse-attention
+ * kernel over the selected KV): per query head with n = n_sel entries of idx,
+ *   lse = log sum_{i in S} exp(s_i),  out = sum_{i in S} exp(s_i - lse) v_i,
+ * s_i = scale * <q, k_i>; natural log; fp32 accumulation. n = 0 gives
+ * out = 0, lse = -inf. Entries outside [0, t_b) are skipped and flagged. */
+prhs_status prhs_sparse_attn(const prhs_kv* kv, const void* q, float scale,
+                             const int32_t* idx, const int32_t* n_sel, int cap,
+                             float* out, float* lse, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/* Dense attention over all t_b keys (the dense baseline of Table IV). The
+ * Hq/Hkv query heads of one KV head share each K/V row read. */
+prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float* out,
+                            float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* One decode step with CIS reuse, stream-ordered, no host round trip:
+ *   prhs_cis_dilate(anchor -> idx, reuse);
+ *   prhs_score_select(head_skip = reuse, anchor outputs = the anchor buffers);
+ *   prhs_sparse_attn(idx).
+ * Heads that reuse attend the dilated anchor set; the others retrieve a fresh
+ * top-N set, attend it and make it (with q) the new anchor. delta is written
+ * for retrieving heads only. Start a sequence with anchor_n all zero. */
+prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int N,
+                             const int32_t* n_budget, int w, double tau,
+                             int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
+                             void* q_anchor, int32_t* idx, int32_t* n_sel, int cap,
+                             uint8_t* reuse, float* delta, float* out, float* lse,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronise the current device, read and clear the device error word.
+ * PRHS_OK when it was zero, PRHS_EDEVICE otherwise, PRHS_ECUDA when the
+ * synchronisation itself failed. */
+prhs_status prhs_last_error(void);
+
+/* Bits of the device error word seen by the last prhs_last_error(). */
+unsigned prhs_device_error_bits(void);
+
+/* Text of a status code; text of the calling thread's last host-side failure. */
+const char* prhs_status_str(prhs_status s);
+const char* prhs_last_message(void);
+
+/* Launch geometry the library picks for this device (for benchmarks and
+ * tests): SM count and split-K factors of the attention kernels. */
+int prhs_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PRHS_H */

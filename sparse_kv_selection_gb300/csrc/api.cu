@@ -1,0 +1,537 @@
+// C ABI of the PrHS decode path: argument checks, workspace layout, TMA
+// descriptor encoding and kernel launches. Declarations and the contract of
+// every entry point are in include/prhs.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kernels.h"
+
+namespace prhs {
+
+__device__ unsigned int g_error_word = 0;
+
+namespace {
+
+thread_local std::string t_message;
+unsigned g_last_bits = 0;
+
+prhs_status fail(prhs_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+prhs_status fail(prhs_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_message = buf;
+  return s;
+}
+
+prhs_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PRHS_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int MAX_DEVICES = 64;
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  unsigned* err = nullptr;
+};
+DeviceInfo g_dev[MAX_DEVICES];
+std::mutex g_dev_mu;
+
+// Per-device facts resolved once, with that device current.
+prhs_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= MAX_DEVICES) return fail(PRHS_ECUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    di.err = static_cast<unsigned*>(p);
+    di.ready = true;
+  }
+  *out = &di;
+  return PRHS_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// ---------------------------------------------------------------------------
+// descriptor checks
+// ---------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int t_max_of(const prhs_kv& kv) {
+  return kv.block_table != nullptr ? kv.max_blocks * kv.block_size : kv.t_max;
+}
+
+prhs_status check_kv(const prhs_kv* kv) {
+  if (kv == nullptr) return fail(PRHS_EINVAL, "kv descriptor is null");
+  if (kv->dtype != PRHS_F32 && kv->dtype != PRHS_BF16)
+    return fail(PRHS_EINVAL, "unknown dtype %d", (int)kv->dtype);
+  if (kv->B <= 0 || kv->Hq <= 0 || kv->Hkv <= 0)
+    return fail(PRHS_EINVAL, "B, Hq, Hkv must be positive (got %d, %d, %d)", kv->B, kv->Hq, kv->Hkv);
+  if (kv->Hq % kv->Hkv != 0) return fail(PRHS_EINVAL, "Hq %% Hkv != 0");
+  const int G = kv->Hq / kv->Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(PRHS_EUNSUPPORTED, "query group Hq/Hkv = %d not built (1, 2, 4, 8)", G);
+  if (kv->d != 64 && kv->d != 128) return fail(PRHS_EUNSUPPORTED, "head dim %d not built (64, 128)", kv->d);
+  if (kv->k == nullptr || kv->v == nullptr || kv->seq_lens == nullptr)
+    return fail(PRHS_EINVAL, "k, v and seq_lens must be non-null");
+  if (!aligned16(kv->k) || !aligned16(kv->v)) return fail(PRHS_EINVAL, "k and v must be 16-byte aligned");
+  if (kv->block_table != nullptr) {
+    if (kv->block_size <= 0 || kv->block_size % 16 != 0)
+      return fail(PRHS_EINVAL, "block_size must be a positive multiple of 16 (got %d)", kv->block_size);
+    if (kv->max_blocks <= 0 || kv->num_blocks <= 0)
+      return fail(PRHS_EINVAL, "max_blocks and num_blocks must be positive");
+    const long long rows = (long long)kv->num_blocks * kv->Hkv * kv->block_size;
+    if (rows >= (1ll << 31)) return fail(PRHS_EINVAL, "paged pool too large (%lld rows)", rows);
+    if ((long long)kv->max_blocks * kv->block_size >= (1ll << 30))
+      return fail(PRHS_EINVAL, "max_blocks * block_size too large");
+  } else {
+    if (kv->t_max <= 0) return fail(PRHS_EINVAL, "t_max must be positive (got %d)", kv->t_max);
+    const long long rows = (long long)kv->B * kv->Hkv * kv->t_max;
+    if (rows >= (1ll << 31)) return fail(PRHS_EINVAL, "cache too large (%lld rows)", rows);
+  }
+  return PRHS_OK;
+}
+
+KVView view_of(const prhs_kv& kv, unsigned* err) {
+  KVView v;
+  v.dtype = kv.dtype;
+  v.k = kv.k;
+  v.v = kv.v;
+  v.seq_lens = kv.seq_lens;
+  v.block_table = kv.block_table;
+  v.B = kv.B;
+  v.Hq = kv.Hq;
+  v.Hkv = kv.Hkv;
+  v.d = kv.d;
+  v.t_max = t_max_of(kv);
+  v.block_size = kv.block_table ? kv.block_size : 1;
+  v.max_blocks = kv.block_table ? kv.max_blocks : 0;
+  v.num_blocks = kv.block_table ? kv.num_blocks : 0;
+  v.err = err;
+  return v;
+}
+
+size_t elem_size(prhs_dtype dt) { return dt == PRHS_BF16 ? 2 : 4; }
+
+// ---------------------------------------------------------------------------
+// launch geometry and workspace layout
+// ---------------------------------------------------------------------------
+constexpr int ATTN_CTAS_PER_SM = 4;
+constexpr int MAX_SPLITS = 256;
+
+int sparse_splits(const prhs_kv& kv, int sms) {
+  const int units = kv.B * kv.Hq;
+  int s = (ATTN_CTAS_PER_SM * sms + units - 1) / units;
+  return s < 1 ? 1 : (s > MAX_SPLITS ? MAX_SPLITS : s);
+}
+
+int dense_splits(const prhs_kv& kv, int sms) {
+  const int units = kv.B * kv.Hkv;
+  int s = (ATTN_CTAS_PER_SM * sms + units - 1) / units;
+  const int by_len = (t_max_of(kv) + 63) / 64;
+  if (s > by_len) s = by_len;
+  return s < 1 ? 1 : (s > MAX_SPLITS ? MAX_SPLITS : s);
+}
+
+struct Layout {
+  size_t counters, partials, scores, total;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+Layout layout_of(const prhs_kv& kv, int sms) {
+  Layout L;
+  const int G = kv.Hq / kv.Hkv;
+  const size_t units = (size_t)kv.B * kv.Hq;  // >= B * Hkv
+  const size_t ps = (size_t)kv.B * kv.Hq * sparse_splits(kv, sms);
+  const size_t pd = (size_t)kv.B * kv.Hkv * G * dense_splits(kv, sms);
+  const size_t prec = (size_t)(kv.d + 2) * sizeof(float);
+  L.counters = 0;
+  L.partials = round_up(units * sizeof(unsigned), 256);
+  L.scores = round_up(L.partials + (ps > pd ? ps : pd) * prec, 256);
+  L.total = round_up(L.scores + (size_t)kv.B * kv.Hq * t_max_of(kv) * sizeof(float), 256);
+  return L;
+}
+
+prhs_status check_ws(const prhs_kv& kv, int sms, void* ws, size_t ws_bytes, Layout* L) {
+  *L = layout_of(kv, sms);
+  if (ws == nullptr) return fail(PRHS_EWORKSPACE, "workspace is null");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(PRHS_EWORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < L->total)
+    return fail(PRHS_EWORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, L->total);
+  return PRHS_OK;
+}
+
+// TMA descriptor over K viewed as [rows][d*esize/128][128 bytes] with the
+// 128-byte swizzle; boxes of `box_rows` rows.
+prhs_status make_tmap(const prhs_kv& kv, int box_rows, CUtensorMap* map) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return fail(PRHS_ECUDA, "cuTensorMapEncodeTiled unavailable");
+  const size_t es = elem_size(kv.dtype);
+  const cuuint64_t inner = 128 / es;
+  const cuuint64_t segs = kv.d * es / 128;
+  const cuuint64_t rows = kv.block_table != nullptr
+                              ? (cuuint64_t)kv.num_blocks * kv.Hkv * kv.block_size
+                              : (cuuint64_t)kv.B * kv.Hkv * kv.t_max;
+  const cuuint64_t dims[3] = {inner, segs, rows};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)kv.d * es};  // bytes, dims 1 and 2
+  const cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)segs, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, kv.dtype == PRHS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   3, const_cast<void*>(kv.k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PRHS_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PRHS_OK;
+}
+
+// Keys per scoring CTA: fill every SM (two resident CTAs each) in one wave
+// when the cache is small, bounded chunks when it is large.
+void score_geometry(const prhs_kv& kv, int sms, int* chunk_keys, int* nchunks) {
+  const int tmax = t_max_of(kv);
+  const int tiles = (tmax + SCORE_TILE - 1) / SCORE_TILE;
+  const int units = kv.B * kv.Hkv;
+  const int slots = 2 * sms;
+  int per;
+  if (units <= slots) {
+    int nc = slots / units;
+    if (nc < 1) nc = 1;
+    per = (tiles + nc - 1) / nc;
+  } else {
+    per = tiles < 16 ? tiles : 16;
+  }
+  if (per < 1) per = 1;
+  *chunk_keys = per * SCORE_TILE;
+  *nchunks = (tiles + per - 1) / per;
+}
+
+prhs_status launch_result(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return PRHS_OK;
+  if (e == cudaErrorNotSupported) return fail(PRHS_EUNSUPPORTED, "%s: shape not built", what);
+  return cuda_fail(e, what);
+}
+
+prhs_status do_score(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws, const void* q,
+                     float scale, const uint8_t* head_skip, cudaStream_t st) {
+  CUtensorMap map;
+  const bool paged = kv.block_table != nullptr;
+  prhs_status s = make_tmap(kv, paged ? PAGED_BOX_ROWS : SCORE_TILE, &map);
+  if (s != PRHS_OK) return s;
+  ScoreLaunch sl;
+  sl.kv = view_of(kv, di->err);
+  sl.q = q;
+  sl.scale = scale;
+  sl.head_skip = head_skip;
+  sl.scores = reinterpret_cast<float*>(static_cast<char*>(ws) + L.scores);
+  sl.paged = paged;
+  score_geometry(kv, di->sms, &sl.chunk_keys, &sl.nchunks);
+  return launch_result(launch_score(sl, &map, st), "score kernel");
+}
+
+prhs_status do_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws,
+                      const void* q, int N, const int32_t* n_budget, const uint8_t* head_skip,
+                      int32_t* idx, int32_t* n_sel, int cap, float* delta, int32_t* anchor_idx,
+                      int32_t* anchor_n, int anchor_cap, void* q_anchor, cudaStream_t st) {
+  SelectLaunch se;
+  se.kv = view_of(kv, di->err);
+  se.scores = reinterpret_cast<float*>(static_cast<char*>(ws) + L.scores);
+  se.N = N;
+  se.n_budget = n_budget;
+  se.head_skip = head_skip;
+  se.idx = idx;
+  se.n_sel = n_sel;
+  se.cap = cap;
+  se.delta = delta;
+  se.anchor_idx = anchor_idx;
+  se.anchor_n = anchor_n;
+  se.anchor_cap = anchor_cap;
+  se.q = q;
+  se.q_anchor = q_anchor;
+  return launch_result(launch_select(se, st), "select kernel");
+}
+
+prhs_status do_score_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws,
+                            const void* q, float scale, int N, const int32_t* n_budget,
+                            const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
+                            float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
+                            void* q_anchor, cudaStream_t st) {
+  prhs_status s = do_score(kv, di, L, ws, q, scale, head_skip, st);
+  if (s != PRHS_OK) return s;
+  return do_select(kv, di, L, ws, q, N, n_budget, head_skip, idx, n_sel, cap, delta, anchor_idx,
+                   anchor_n, anchor_cap, q_anchor, st);
+}
+
+// Host checks shared by the selection entry points.
+prhs_status check_select_args(const prhs_kv& kv, const void* q, int N, const int32_t* n_budget,
+                              int32_t* idx, int32_t* n_sel, int cap, float* delta,
+                              int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
+                              void* q_anchor) {
+  if (q == nullptr || idx == nullptr || n_sel == nullptr || delta == nullptr)
+    return fail(PRHS_EINVAL, "q, idx, n_sel and delta must be non-null");
+  if (n_budget == nullptr && N <= 0) return fail(PRHS_EINVAL, "N must be positive (got %d)", N);
+  if (cap <= 0) return fail(PRHS_EINVAL, "cap must be positive");
+  const int tmax = t_max_of(kv);
+  if (n_budget == nullptr && cap < (N < tmax ? N : tmax))
+    return fail(PRHS_EINVAL, "cap %d < budget %d", cap, N < tmax ? N : tmax);
+  const bool any_anchor = anchor_idx || anchor_n || q_anchor;
+  if (any_anchor && !(anchor_idx && anchor_n && q_anchor))
+    return fail(PRHS_EINVAL, "anchor_idx, anchor_n and q_anchor must be all set or all null");
+  if (any_anchor && n_budget == nullptr && anchor_cap < (N < tmax ? N : tmax))
+    return fail(PRHS_EINVAL, "anchor_cap %d < budget", anchor_cap);
+  return PRHS_OK;
+}
+
+prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws, const void* q,
+                    float scale, const int32_t* idx, const int32_t* n_sel, int cap, float* out,
+                    float* lse, bool sparse, cudaStream_t st) {
+  AttnLaunch a;
+  a.kv = view_of(kv, di->err);
+  a.q = q;
+  a.scale = scale;
+  a.idx = idx;
+  a.n_sel = n_sel;
+  a.cap = cap;
+  a.out = out;
+  a.lse = lse;
+  a.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partials);
+  a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.counters);
+  a.splits = sparse ? sparse_splits(kv, di->sms) : dense_splits(kv, di->sms);
+  return launch_result(launch_attn(a, sparse, st), sparse ? "sparse attention" : "dense attention");
+}
+
+prhs_status do_cis(const prhs_kv& kv, DeviceInfo* di, const int32_t* anchor_idx,
+                   const int32_t* anchor_n, int anchor_cap, const void* q, const void* q_anchor,
+                   int w, double tau, int32_t* idx, int32_t* n_sel, int cap, uint8_t* reuse,
+                   cudaStream_t st) {
+  CisLaunch c;
+  c.kv = view_of(kv, di->err);
+  c.anchor_idx = anchor_idx;
+  c.anchor_n = anchor_n;
+  c.anchor_cap = anchor_cap;
+  c.q = q;
+  c.q_anchor = q_anchor;
+  c.w = w;
+  c.tau = tau;
+  c.idx = idx;
+  c.n_sel = n_sel;
+  c.cap = cap;
+  c.reuse = reuse;
+  return launch_result(launch_cis(c, st), "cis kernel");
+}
+
+bool dilated_fits(long long anchor_cap, int w, int tmax, int cap) {
+  long long need = anchor_cap * (2ll * w + 1);
+  if (need > tmax) need = tmax;
+  return need <= cap;
+}
+
+}  // namespace
+}  // namespace prhs
+
+using namespace prhs;
+
+extern "C" {
+
+size_t prhs_workspace_size(const prhs_kv* kv, int cap) {
+  (void)cap;
+  if (check_kv(kv) != PRHS_OK) return 0;
+  DeviceInfo* di = nullptr;
+  if (device_info(&di) != PRHS_OK) return 0;
+  return layout_of(*kv, di->sms).total;
+}
+
+prhs_status prhs_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (ws == nullptr || ws_bytes == 0) return fail(PRHS_EWORKSPACE, "workspace is null or empty");
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, stream);
+  return e == cudaSuccess ? PRHS_OK : cuda_fail(e, "cudaMemsetAsync");
+}
+
+prhs_status prhs_score_select(const prhs_kv* kv, const void* q, float scale, int N,
+                              const int32_t* n_budget, const uint8_t* head_skip, int32_t* idx,
+                              int32_t* n_sel, int cap, float* delta, int32_t* anchor_idx,
+                              int32_t* anchor_n, int anchor_cap, void* q_anchor, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if ((s = check_select_args(*kv, q, N, n_budget, idx, n_sel, cap, delta, anchor_idx, anchor_n,
+                             anchor_cap, q_anchor)) != PRHS_OK)
+    return s;
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  Layout L;
+  if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
+  return do_score_select(*kv, di, L, ws, q, scale, N, n_budget, head_skip, idx, n_sel, cap, delta,
+                         anchor_idx, anchor_n, anchor_cap, q_anchor, stream);
+}
+
+prhs_status prhs_score(const prhs_kv* kv, const void* q, float scale, const uint8_t* head_skip,
+                       void* ws, size_t ws_bytes, cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if (q == nullptr) return fail(PRHS_EINVAL, "q must be non-null");
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  Layout L;
+  if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
+  return do_score(*kv, di, L, ws, q, scale, head_skip, stream);
+}
+
+prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* n_budget,
+                        const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
+                        float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
+                        void* q_anchor, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if ((s = check_select_args(*kv, q, N, n_budget, idx, n_sel, cap, delta, anchor_idx, anchor_n,
+                             anchor_cap, q_anchor)) != PRHS_OK)
+    return s;
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  Layout L;
+  if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
+  return do_select(*kv, di, L, ws, q, N, n_budget, head_skip, idx, n_sel, cap, delta, anchor_idx,
+                   anchor_n, anchor_cap, q_anchor, stream);
+}
+
+prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx, const int32_t* anchor_n,
+                            int anchor_cap, const void* q, const void* q_anchor, int w, double tau,
+                            int32_t* idx, int32_t* n_sel, int cap, uint8_t* reuse,
+                            cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if (!anchor_idx || !anchor_n || !q || !q_anchor || !idx || !n_sel || !reuse)
+    return fail(PRHS_EINVAL, "cis: null pointer argument");
+  if (w < 0) return fail(PRHS_EINVAL, "w must be >= 0 (got %d)", w);
+  if (anchor_cap <= 0 || cap <= 0) return fail(PRHS_EINVAL, "capacities must be positive");
+  if (!dilated_fits(anchor_cap, w, t_max_of(*kv), cap))
+    return fail(PRHS_EINVAL, "cap %d < min(t_max, anchor_cap * (2w + 1))", cap);
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  return do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, tau, idx, n_sel, cap,
+                reuse, stream);
+}
+
+prhs_status prhs_sparse_attn(const prhs_kv* kv, const void* q, float scale, const int32_t* idx,
+                             const int32_t* n_sel, int cap, float* out, float* lse, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if (!q || !idx || !n_sel || !out || !lse) return fail(PRHS_EINVAL, "sparse: null pointer argument");
+  if (cap <= 0) return fail(PRHS_EINVAL, "cap must be positive");
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  Layout L;
+  if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
+  return do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, stream);
+}
+
+prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float* out, float* lse,
+                            void* ws, size_t ws_bytes, cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if (!q || !out || !lse) return fail(PRHS_EINVAL, "dense: null pointer argument");
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  Layout L;
+  if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
+  return do_attn(*kv, di, L, ws, q, scale, nullptr, nullptr, 0, out, lse, false, stream);
+}
+
+prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int N,
+                             const int32_t* n_budget, int w, double tau, int32_t* anchor_idx,
+                             int32_t* anchor_n, int anchor_cap, void* q_anchor, int32_t* idx,
+                             int32_t* n_sel, int cap, uint8_t* reuse, float* delta, float* out,
+                             float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if (!q || !anchor_idx || !anchor_n || !q_anchor || !idx || !n_sel || !reuse || !delta || !out || !lse)
+    return fail(PRHS_EINVAL, "decode: null pointer argument");
+  if (n_budget == nullptr && N <= 0) return fail(PRHS_EINVAL, "N must be positive (got %d)", N);
+  if (w < 0) return fail(PRHS_EINVAL, "w must be >= 0 (got %d)", w);
+  const int tmax = t_max_of(*kv);
+  if (anchor_cap <= 0 || cap <= 0) return fail(PRHS_EINVAL, "capacities must be positive");
+  if (n_budget == nullptr && anchor_cap < (N < tmax ? N : tmax))
+    return fail(PRHS_EINVAL, "anchor_cap %d < budget", anchor_cap);
+  if (!dilated_fits(anchor_cap, w, tmax, cap))
+    return fail(PRHS_EINVAL, "cap %d < min(t_max, anchor_cap * (2w + 1))", cap);
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  Layout L;
+  if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
+  if ((s = do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, tau, idx, n_sel, cap,
+                  reuse, stream)) != PRHS_OK)
+    return s;
+  if ((s = do_score_select(*kv, di, L, ws, q, scale, N, n_budget, reuse, idx, n_sel, cap, delta,
+                           anchor_idx, anchor_n, anchor_cap, q_anchor, stream)) != PRHS_OK)
+    return s;
+  return do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, stream);
+}
+
+prhs_status prhs_last_error(void) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  unsigned bits = 0;
+  e = cudaMemcpyFromSymbol(&bits, g_error_word, sizeof(bits));
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  const unsigned zero = 0;
+  e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  g_last_bits = bits;
+  if (bits != 0) return fail(PRHS_EDEVICE, "device error bits 0x%x", bits);
+  return PRHS_OK;
+}
+
+unsigned prhs_device_error_bits(void) { return g_last_bits; }
+
+const char* prhs_status_str(prhs_status s) {
+  switch (s) {
+    case PRHS_OK: return "ok";
+    case PRHS_EINVAL: return "invalid argument";
+    case PRHS_EUNSUPPORTED: return "unsupported shape";
+    case PRHS_EWORKSPACE: return "workspace missing or too small";
+    case PRHS_ECUDA: return "CUDA runtime error";
+    case PRHS_EDEVICE: return "device-side data error";
+  }
+  return "unknown status";
+}
+
+const char* prhs_last_message(void) { return t_message.c_str(); }
+
+int prhs_num_sms(void) {
+  DeviceInfo* di = nullptr;
+  if (device_info(&di) != PRHS_OK) return 0;
+  return di->sms;
+}
+
+}  // extern "C"

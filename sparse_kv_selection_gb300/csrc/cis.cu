@@ -1,0 +1,134 @@
+// Critical-index-set (CIS) reuse with dilation.
+// "Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference":
+// Fig. 2 (adjacent queries with cosine similarity above 0.8 share critical
+// indices), Fig. 8 (sharing triggers when sim(q, q') >= tau), Fig. 4 and
+// Table VIII (the shared set is dilated; radius r).
+//
+// One CTA per query head. The gate is evaluated in float64 so that it takes
+// the same decision as a float64 reference. The dilated set
+//   union_{a in anchor} [a - w, a + w] clipped to [0, t_b)
+// is produced without sorting: the anchor row is ascending, so interval j
+// contributes the positions after max(lo_j, hi_{j-1} + 1); a block-wide
+// exclusive scan of those counts gives every write position directly and the
+// output comes out ascending and free of repeats.
+#include "kernels.h"
+
+namespace prhs {
+
+constexpr int CIS_THREADS = 256;
+
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  return v;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
+  __shared__ double red[3][CIS_THREADS / 32];
+  __shared__ int sh_reuse;
+  __shared__ int warp_tot[CIS_THREADS / 32];
+  const KVView& kv = a.kv;
+  const int qh = blockIdx.x;
+  const int b = qh / kv.Hq;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int d = kv.d;
+
+  double dot = 0.0, nq = 0.0, na = 0.0;
+  for (int i = tid; i < d; i += CIS_THREADS) {
+    const double x = (double)Elem<T>::load1(a.q, (long long)qh * d + i);
+    const double y = (double)Elem<T>::load1(a.q_anchor, (long long)qh * d + i);
+    dot = fma(x, y, dot);
+    nq = fma(x, x, nq);
+    na = fma(y, y, na);
+  }
+  dot = warp_sum_f64(dot);
+  nq = warp_sum_f64(nq);
+  na = warp_sum_f64(na);
+  if (lane == 0) {
+    red[0][warp] = dot;
+    red[1][warp] = nq;
+    red[2][warp] = na;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double D = 0, Q = 0, A = 0;
+    for (int w = 0; w < CIS_THREADS / 32; w++) {
+      D += red[0][w];
+      Q += red[1][w];
+      A += red[2][w];
+    }
+    const double den = sqrt(Q) * sqrt(A);
+    const int n_anchor = a.anchor_n[qh];
+    const int reuse = n_anchor > 0 && den > 0.0 && (D / den) >= a.tau;
+    sh_reuse = reuse;
+    a.reuse[qh] = (uint8_t)reuse;
+  }
+  __syncthreads();
+  if (!sh_reuse) return;
+
+  // ---- dilation of the anchor set ----
+  const int t = seq_len(kv, b);
+  int n = a.anchor_n[qh];
+  if (n > a.anchor_cap) {
+    if (tid == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
+    n = a.anchor_cap;
+  }
+  const int32_t* anc = a.anchor_idx + (long long)qh * a.anchor_cap;
+  int32_t* out = a.idx + (long long)qh * a.cap;
+  const int w = a.w;
+  int carry = 0;
+  for (int base = 0; base < n; base += CIS_THREADS) {
+    const int jdx = base + tid;
+    int start = 0, cnt = 0;
+    if (jdx < n) {
+      const int x = anc[jdx];
+      const int prev = jdx > 0 ? anc[jdx - 1] : -1;
+      if (x < 0 || x >= t || x <= prev) {
+        raise_error(kv.err, PRHS_DEV_BAD_INDEX);
+      } else {
+        const int lo = max(0, x - w);
+        const int hi = min(t - 1, x + w);
+        const int prev_hi = jdx > 0 ? min(t - 1, prev + w) : -1;
+        start = max(lo, prev_hi + 1);
+        cnt = max(0, hi - start + 1);
+      }
+    }
+    // block exclusive scan of cnt
+    int v = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w2 = 0; w2 < CIS_THREADS / 32; w2++) {
+      if (w2 < warp) before += warp_tot[w2];
+      total += warp_tot[w2];
+    }
+    const int pos = carry + before + v - cnt;
+    for (int e = 0; e < cnt; e++) {
+      if (pos + e < a.cap) {
+        out[pos + e] = start + e;
+      } else {
+        raise_error(kv.err, PRHS_DEV_CAPACITY);
+        break;
+      }
+    }
+    carry += total;
+    __syncthreads();  // warp_tot reused by the next chunk
+  }
+  if (tid == 0) a.n_sel[qh] = min(carry, a.cap);
+}
+
+cudaError_t launch_cis(const CisLaunch& a, cudaStream_t st) {
+  if (a.kv.dtype == PRHS_BF16)
+    cis_kernel<__nv_bfloat16><<<a.kv.B * a.kv.Hq, CIS_THREADS, 0, st>>>(a);
+  else
+    cis_kernel<float><<<a.kv.B * a.kv.Hq, CIS_THREADS, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace prhs

@@ -1,0 +1,86 @@
+// Internal launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace prhs {
+
+// Keys per TMA stage of the scoring kernel, and rows per TMA box when the
+// cache is paged (one box never crosses a page: block_size % 16 == 0).
+constexpr int SCORE_TILE = 128;
+constexpr int PAGED_BOX_ROWS = 16;
+
+// Scores cached in shared memory by the selection kernel (floats).
+constexpr int SELECT_CACHE_FLOATS = 48 * 1024;
+constexpr int SELECT_THREADS = 1024;
+
+struct ScoreLaunch {
+  KVView kv;
+  const void* q;
+  float scale;
+  const uint8_t* head_skip;  // [B][Hq] or null
+  float* scores;             // [B][Hq][t_max]
+  int chunk_keys;            // keys per CTA (multiple of SCORE_TILE)
+  int nchunks;               // CTAs per (b, kv head)
+  bool paged;
+};
+
+struct SelectLaunch {
+  KVView kv;
+  const float* scores;
+  int N;
+  const int32_t* n_budget;
+  const uint8_t* head_skip;
+  int32_t* idx;
+  int32_t* n_sel;
+  int cap;
+  float* delta;
+  int32_t* anchor_idx;  // all three null or all three set
+  int32_t* anchor_n;
+  int anchor_cap;
+  const void* q;
+  void* q_anchor;
+};
+
+struct CisLaunch {
+  KVView kv;
+  const int32_t* anchor_idx;
+  const int32_t* anchor_n;
+  int anchor_cap;
+  const void* q;
+  const void* q_anchor;
+  int w;
+  double tau;
+  int32_t* idx;
+  int32_t* n_sel;
+  int cap;
+  uint8_t* reuse;
+};
+
+struct AttnLaunch {
+  KVView kv;
+  const void* q;
+  float scale;
+  const int32_t* idx;    // sparse: [B][Hq][cap]; dense: null
+  const int32_t* n_sel;  // sparse: [B][Hq]
+  int cap;
+  float* out;
+  float* lse;
+  float* partials;       // [units][G][splits][d + 2]
+  unsigned* counters;    // [units], zero on entry, left zero
+  int splits;
+};
+
+cudaError_t launch_score(const ScoreLaunch& a, const CUtensorMap* tmap, cudaStream_t s);
+cudaError_t launch_select(const SelectLaunch& a, cudaStream_t s);
+cudaError_t launch_cis(const CisLaunch& a, cudaStream_t s);
+cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t s);
+
+// Bytes of dynamic shared memory the scoring kernel needs for this shape.
+size_t score_smem_bytes(prhs_dtype dt, int d);
+
+}  // namespace prhs

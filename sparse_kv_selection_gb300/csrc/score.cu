@@ -1,0 +1,476 @@
+// Top-N oracle selector: logits s_i = scale * <q, k_i> over the whole cache,
+// then the N largest (lowest index on ties) and the dropped mass
+//   delta = sum_{i not in S} softmax(s)_i.
+// "Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference",
+// abstract (top-k oracle selection before attention scoring, dropped mass)
+// and Table I (S_t, N, tau(.), delta(.)).
+//
+// Two kernels:
+//  * score_kernel  streams K once per KV head through a TMA -> shared-memory
+//    ring (128-byte swizzled tiles, mbarrier-pipelined, one producer warp,
+//    four consumer warps) and writes fp32 logits for the G query heads of
+//    the group. HBM-bound: t * d * sizeof(T) bytes per KV head.
+//  * select_kernel one CTA per query head: softmax statistics, a three-digit
+//    radix select for the N-th largest logit, then an index-ordered compaction
+//    that emits the set ascending and sums the dropped mass.
+#include "kernels.h"
+
+namespace prhs {
+
+// -------------------------------------------------------------------------- //
+// scoring
+// -------------------------------------------------------------------------- //
+template <typename T, int D>
+struct ScoreShape {
+  static constexpr int RB = D * (int)sizeof(T);        // bytes per key row
+  static constexpr int NH = RB / 128;                  // 128-byte segments per row
+  static constexpr int EPC = 16 / (int)sizeof(T);      // elements per 16-byte chunk
+  static constexpr int EL = NH * EPC;                  // q elements per lane
+  static constexpr int TK = SCORE_TILE;                // keys per stage
+  static constexpr int NW = 4;                         // consumer warps (32 keys each)
+  static constexpr int STAGE_BYTES = TK * RB;
+  static constexpr int STAGES = RB == 128 ? 6 : (RB == 256 ? 3 : 2);
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 2 * STAGES * 8 + 1024;
+  static_assert(RB % 128 == 0, "row must be a whole number of 128-byte segments");
+};
+
+// Eight partial dot products per lane (one per key p) held by the 8 lanes of
+// a key slot; afterwards lane j of the slot holds the full sum for key p = j.
+__device__ __forceinline__ float transpose_reduce8(const float (&v)[8], int j) {
+  float a[4], b[2];
+  const bool h4 = j & 4, h2 = j & 2, h1 = j & 1;
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    float send = h4 ? v[i] : v[i + 4];
+    float keep = h4 ? v[i + 4] : v[i];
+    a[i] = keep + __shfl_xor_sync(FULL_MASK, send, 4);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; i++) {
+    float send = h2 ? a[i] : a[i + 2];
+    float keep = h2 ? a[i + 2] : a[i];
+    b[i] = keep + __shfl_xor_sync(FULL_MASK, send, 2);
+  }
+  float send = h1 ? b[0] : b[1];
+  float keep = h1 ? b[1] : b[0];
+  return keep + __shfl_xor_sync(FULL_MASK, send, 1);
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(160) score_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                    const ScoreLaunch a) {
+  using S = ScoreShape<T, D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::STAGES * S::STAGE_BYTES);
+  uint64_t* empty = full + S::STAGES;
+
+  const KVView& kv = a.kv;
+  const int unit = blockIdx.y;  // b * Hkv + kv head
+  const int b = unit / kv.Hkv, kvh = unit % kv.Hkv;
+  const int qh0 = b * kv.Hq + kvh * G;  // first query head of the group
+  if (a.head_skip != nullptr) {
+    bool need = false;
+#pragma unroll
+    for (int g = 0; g < G; g++) need |= a.head_skip[qh0 + g] == 0;
+    if (!need) return;
+  }
+  const int t = seq_len(kv, b);
+  const int k0 = blockIdx.x * a.chunk_keys;
+  if (k0 >= t) return;
+  const int k1 = min(t, k0 + a.chunk_keys);
+  const int ntiles = (k1 - k0 + S::TK - 1) / S::TK;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::STAGES; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], S::NW);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == S::NW) {
+    // ---------------- producer: one lane issues the TMA boxes ----------------
+    if (lane != 0) return;
+    prefetch_tmap(&tmap);
+    int issued = 0;
+    for (int it = 0; it < ntiles; it++) {
+      const int s = it % S::STAGES;
+      if (!mbar_wait(&empty[s], ((it / S::STAGES) & 1) ^ 1, kv.err)) break;
+      const int tile0 = k0 + it * S::TK;
+      uint8_t* dst = smem + s * S::STAGE_BYTES;
+      if (!a.paged) {
+        mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
+        tma_load_3d(dst, &tmap, 0, 0, unit * kv.t_max + tile0, &full[s]);
+      } else {
+        const int nbox = min(S::TK / PAGED_BOX_ROWS, (k1 - tile0 + PAGED_BOX_ROWS - 1) / PAGED_BOX_ROWS);
+        mbar_arrive_expect_tx(&full[s], nbox * PAGED_BOX_ROWS * S::RB);
+        for (int x = 0; x < nbox; x++) {
+          long long row = kv_row(kv, b, kvh, tile0 + x * PAGED_BOX_ROWS);
+          if (row < 0) {
+            raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
+            row = 0;
+          }
+          tma_load_3d(dst + x * PAGED_BOX_ROWS * S::RB, &tmap, 0, 0, (int)row, &full[s]);
+        }
+      }
+      issued = it + 1;
+    }
+    // never leave while a copy into this CTA's shared memory is in flight
+    for (int it = max(0, issued - S::STAGES); it < issued; it++)
+      mbar_wait(&full[it % S::STAGES], (it / S::STAGES) & 1, kv.err);
+    return;
+  }
+
+  // ---------------- consumers: 32 keys per warp per stage ----------------
+  const int r = lane >> 3;  // key slot 0..3 (8 keys each)
+  const int j = lane & 7;   // 16-byte chunk within each 128-byte segment
+  float qf[G][S::EL];
+#pragma unroll
+  for (int g = 0; g < G; g++) {
+    const long long qbase = (long long)(qh0 + g) * D;
+#pragma unroll
+    for (int h = 0; h < S::NH; h++)
+#pragma unroll
+      for (int e = 0; e < S::EPC; e++)
+        qf[g][h * S::EPC + e] = Elem<T>::load1(a.q, qbase + h * (128 / (int)sizeof(T)) + j * S::EPC + e);
+  }
+
+  for (int it = 0; it < ntiles; it++) {
+    const int s = it % S::STAGES;
+    if (!mbar_wait(&full[s], (it / S::STAGES) & 1, kv.err)) break;
+    const uint8_t* stage = smem + s * S::STAGE_BYTES;
+    float acc[G][8];
+#pragma unroll
+    for (int g = 0; g < G; g++)
+#pragma unroll
+      for (int p = 0; p < 8; p++) acc[g][p] = 0.f;
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+      const int key = warp * 32 + r * 8 + p;
+#pragma unroll
+      for (int h = 0; h < S::NH; h++) {
+        const int line = key * S::NH + h;  // 128-byte line in the stage
+        const uint4 c = *reinterpret_cast<const uint4*>(stage + line * 128 + ((j ^ (line & 7)) << 4));
+        float f[S::EPC];
+        Elem<T>::unpack(c, f);
+#pragma unroll
+        for (int g = 0; g < G; g++)
+#pragma unroll
+          for (int e = 0; e < S::EPC; e++) acc[g][p] = fmaf(qf[g][h * S::EPC + e], f[e], acc[g][p]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    const int key = k0 + it * S::TK + warp * 32 + lane;
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+      const float sc = transpose_reduce8(acc[g], j) * a.scale;
+      if (key < k1) a.scores[(long long)(qh0 + g) * kv.t_max + key] = sc;
+    }
+  }
+}
+
+template <typename T, int D>
+static cudaError_t score_dispatch_g(const ScoreLaunch& a, const CUtensorMap* tmap, int G,
+                                   cudaStream_t st) {
+  using S = ScoreShape<T, D>;
+  dim3 grid(a.nchunks, a.kv.B * a.kv.Hkv);
+  void (*k)(const CUtensorMap, const ScoreLaunch) = nullptr;
+  switch (G) {
+    case 1: k = score_kernel<T, D, 1>; break;
+    case 2: k = score_kernel<T, D, 2>; break;
+    case 4: k = score_kernel<T, D, 4>; break;
+    case 8: k = score_kernel<T, D, 8>; break;
+    default: return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
+  if (e != cudaSuccess) return e;
+  k<<<grid, 32 * (S::NW + 1), S::SMEM, st>>>(*tmap, a);
+  return cudaGetLastError();
+}
+
+size_t score_smem_bytes(prhs_dtype dt, int d) {
+  if (dt == PRHS_BF16) return d == 64 ? ScoreShape<__nv_bfloat16, 64>::SMEM : ScoreShape<__nv_bfloat16, 128>::SMEM;
+  return d == 64 ? ScoreShape<float, 64>::SMEM : ScoreShape<float, 128>::SMEM;
+}
+
+// -------------------------------------------------------------------------- //
+// selection
+// -------------------------------------------------------------------------- //
+struct SelShared {
+  unsigned hist[2048];
+  unsigned scan[32];
+  float red_m[32];
+  float red_z[32];
+  unsigned digit, krem;
+};
+
+// Block-wide inclusive scan of one unsigned per thread (1024 threads).
+__device__ __forceinline__ unsigned block_inclusive_scan(unsigned v, unsigned* warp_tot,
+                                                         unsigned& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    unsigned n = __shfl_up_sync(FULL_MASK, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      unsigned n = __shfl_up_sync(FULL_MASK, w, o);
+      if (lane >= o) w += n;
+    }
+    warp_tot[lane] = w;
+  }
+  __syncthreads();
+  total = warp_tot[(blockDim.x >> 5) - 1];
+  const unsigned add = warp > 0 ? warp_tot[warp - 1] : 0u;
+  __syncthreads();  // warp_tot may be reused right after
+  return v + add;
+}
+
+__device__ __forceinline__ void combine_mz(float& m, float& z, float m2, float z2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  z = (m == -INFINITY ? 0.f : z * expf(m - M)) + (m2 == -INFINITY ? 0.f : z2 * expf(m2 - M));
+  m = M;
+}
+
+template <typename T>
+__device__ __forceinline__ void copy_query(const SelectLaunch& a, int qh) {
+  const int d = a.kv.d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x)
+    copy_elem<T>(a.q_anchor, a.q, (long long)qh * d + i);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectLaunch a) {
+  extern __shared__ float cache[];
+  __shared__ SelShared sh;
+  const KVView& kv = a.kv;
+  const int qh = blockIdx.x;  // b * Hq + query head
+  const int b = qh / kv.Hq;
+  if (a.head_skip != nullptr && a.head_skip[qh] != 0) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x;
+  const int t = seq_len(kv, b);
+  int Nb = a.n_budget != nullptr ? a.n_budget[b] : a.N;
+  if (Nb < 0) Nb = 0;
+  const int lim = a.anchor_idx != nullptr ? min(a.cap, a.anchor_cap) : a.cap;
+  if (min(Nb, t) > lim) {
+    if (tid == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
+    Nb = lim;
+  }
+  int32_t* out = a.idx + (long long)qh * a.cap;
+  int32_t* aout = a.anchor_idx != nullptr ? a.anchor_idx + (long long)qh * a.anchor_cap : nullptr;
+
+  if (Nb >= t || Nb == 0) {  // keep everything (delta = 0) or nothing (delta = 1)
+    const int n = Nb >= t ? t : 0;
+    for (int i = tid; i < n; i += nthreads) {
+      out[i] = i;
+      if (aout) aout[i] = i;
+    }
+    if (tid == 0) {
+      a.n_sel[qh] = n;
+      a.delta[qh] = n == t ? 0.f : 1.f;
+      if (a.anchor_n) a.anchor_n[qh] = n;
+    }
+    if (a.q_anchor) copy_query<T>(a, qh);
+    return;
+  }
+
+  // ---- stage the logits (shared memory when they fit) ----
+  const float* src = a.scores + (long long)qh * kv.t_max;
+  const float* sp = src;
+  if (t <= SELECT_CACHE_FLOATS) {
+    for (int i = tid; i < t; i += nthreads) cache[i] = src[i];
+    sp = cache;
+  }
+  for (int i = tid; i < 2048; i += nthreads) sh.hist[i] = 0;
+  __syncthreads();
+
+  // ---- pass 1: softmax statistics (m, Z) and histogram of the top 11 bits ----
+  float m = -INFINITY, z = 0.f;
+  const int rounds = (t + nthreads - 1) / nthreads;
+  for (int rd = 0; rd < rounds; rd++) {
+    const int i = rd * nthreads + tid;
+    const bool in = i < t;
+    const float s = in ? sp[i] : -INFINITY;
+    if (in) {
+      if (s > m) {
+        z = z * expf(m - s) + 1.f;
+        m = s;
+      } else {
+        z += expf(s - m);
+      }
+    }
+    const unsigned dg = order_key(s) >> 21;
+    const unsigned act = __ballot_sync(FULL_MASK, in);
+    if (in) {
+      const unsigned peers = __match_any_sync(act, dg);
+      if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[dg], __popc(peers));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(FULL_MASK, m, o);
+    const float z2 = __shfl_xor_sync(FULL_MASK, z, o);
+    combine_mz(m, z, m2, z2);
+  }
+  if (lane == 0) {
+    sh.red_m[warp] = m;
+    sh.red_z[warp] = z;
+  }
+  if (tid == 0) sh.krem = (unsigned)Nb;
+  __syncthreads();
+  float M = sh.red_m[0], Z = sh.red_z[0];
+  for (int w = 1; w < (nthreads >> 5); w++) combine_mz(M, Z, sh.red_m[w], sh.red_z[w]);
+
+  // ---- radix select: digits of 11, 11 and 10 bits from the top ----
+  unsigned prefix = 0, mask = 0;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3; pass++) {
+    const int sh_ = shifts[pass];
+    const int nb = 1 << widths[pass];
+    if (pass > 0) {
+      for (int i = tid; i < nb; i += nthreads) sh.hist[i] = 0;
+      __syncthreads();
+      for (int rd = 0; rd < rounds; rd++) {
+        const int i = rd * nthreads + tid;
+        bool in = i < t;
+        const unsigned u = in ? order_key(sp[i]) : 0u;
+        in = in && (u & mask) == prefix;
+        const unsigned dg = (u >> sh_) & (nb - 1);
+        const unsigned act = __ballot_sync(FULL_MASK, in);
+        if (in) {
+          const unsigned peers = __match_any_sync(act, dg);
+          if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[dg], __popc(peers));
+        }
+      }
+      __syncthreads();
+    }
+    // descending cumulative counts: thread i owns bins nb-1-2i and nb-2-2i
+    const unsigned krem = sh.krem;
+    const int per = nb / nthreads;  // 2 or 1
+    unsigned c0 = 0, c1 = 0;
+    const int bin0 = nb - 1 - per * tid;
+    c0 = sh.hist[bin0];
+    if (per == 2) c1 = sh.hist[bin0 - 1];
+    unsigned tot;
+    const unsigned incl = block_inclusive_scan(c0 + c1, sh.scan, tot);
+    const unsigned excl = incl - c0 - c1;
+    // the bin holding the krem-th largest among the candidates
+    if (excl < krem && excl + c0 >= krem) {
+      sh.digit = (unsigned)bin0;
+      sh.krem = krem - excl;
+    } else if (per == 2 && excl + c0 < krem && excl + c0 + c1 >= krem) {
+      sh.digit = (unsigned)(bin0 - 1);
+      sh.krem = krem - excl - c0;
+    }
+    __syncthreads();
+    prefix |= sh.digit << sh_;
+    mask |= (unsigned)(nb - 1) << sh_;
+    __syncthreads();
+  }
+  const unsigned thr = prefix;        // key of the N-th largest logit
+  const unsigned keq = sh.krem;       // how many logits equal to it are kept
+  __syncthreads();
+
+  // ---- compaction in index order; dropped mass of the rest ----
+  constexpr int E = 4;
+  const int tile = nthreads * E;
+  unsigned carry_gt = 0, carry_eq = 0;
+  float dsum = 0.f;
+  for (int base = 0; base < t; base += tile) {
+    unsigned u[E];
+    float sv[E];
+    unsigned cgt = 0, ceq = 0;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+      const int i = base + tid * E + e;
+      sv[e] = i < t ? sp[i] : -INFINITY;
+      u[e] = i < t ? order_key(sv[e]) : 0u;
+      cgt += u[e] > thr;
+      ceq += (i < t) && u[e] == thr;
+    }
+    unsigned tot;
+    const unsigned packed = (cgt << 16) | ceq;
+    const unsigned incl = block_inclusive_scan(packed, sh.scan, tot);
+    const unsigned excl = incl - packed;
+    unsigned gt_before = carry_gt + (excl >> 16);
+    unsigned eq_before = carry_eq + (excl & 0xffffu);
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+      const int i = base + tid * E + e;
+      if (i >= t) break;
+      bool take = false;
+      int pos = 0;
+      if (u[e] > thr) {
+        take = true;
+        pos = (int)(gt_before + min(eq_before, keq));
+        gt_before++;
+      } else if (u[e] == thr) {
+        if (eq_before < keq) {
+          take = true;
+          pos = (int)(gt_before + eq_before);
+        }
+        eq_before++;
+      }
+      if (take) {
+        if (pos < Nb) {
+          out[pos] = i;
+          if (aout) aout[pos] = i;
+        } else {
+          raise_error(kv.err, PRHS_DEV_CAPACITY);
+        }
+      } else {
+        dsum += expf(sv[e] - M);
+      }
+    }
+    carry_gt += tot >> 16;
+    carry_eq += tot & 0xffffu;
+  }
+  dsum = warp_sum(dsum);
+  if (lane == 0) sh.red_z[warp] = dsum;
+  __syncthreads();
+  if (tid == 0) {
+    float tot = 0.f;
+    for (int w = 0; w < (nthreads >> 5); w++) tot += sh.red_z[w];
+    a.n_sel[qh] = Nb;
+    a.delta[qh] = tot / Z;
+    if (a.anchor_n) a.anchor_n[qh] = Nb;
+  }
+  if (a.q_anchor) copy_query<T>(a, qh);
+}
+
+cudaError_t launch_score(const ScoreLaunch& a, const CUtensorMap* tmap, cudaStream_t st) {
+  const int G = a.kv.Hq / a.kv.Hkv;
+  if (a.kv.dtype == PRHS_BF16) {
+    if (a.kv.d == 128) return score_dispatch_g<__nv_bfloat16, 128>(a, tmap, G, st);
+    if (a.kv.d == 64) return score_dispatch_g<__nv_bfloat16, 64>(a, tmap, G, st);
+  } else {
+    if (a.kv.d == 128) return score_dispatch_g<float, 128>(a, tmap, G, st);
+    if (a.kv.d == 64) return score_dispatch_g<float, 64>(a, tmap, G, st);
+  }
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_select(const SelectLaunch& a, cudaStream_t st) {
+  const size_t smem = (size_t)min(a.kv.t_max, SELECT_CACHE_FLOATS) * sizeof(float);
+  void (*k)(const SelectLaunch) = a.kv.dtype == PRHS_BF16 ? select_kernel<__nv_bfloat16>
+                                                          : select_kernel<float>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<a.kv.B * a.kv.Hq, SELECT_THREADS, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace prhs

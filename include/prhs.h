@@ -143,6 +143,26 @@ prhs_status prhs_sparse_attn(const prhs_kv* kv, const void* q, float scale,
                              float* out, float* lse, void* ws, size_t ws_bytes,
                              cudaStream_t stream);
 
+/* Sparse attention that allocates nothing, for callers that cannot call
+ * cudaMalloc and so cannot hand the library a workspace (a plugin host that
+ * owns all device memory, a serving loop that may not take cudaMalloc's
+ * device synchronisation). The paper has no counterpart: this is a library
+ * convenience. Same arguments and results as prhs_sparse_attn minus the
+ * workspace; the split-K scratch is a fixed device array of
+ * PRHS_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that
+ * loads it until the process exits. A batch whose scratch (256-byte-rounded
+ * B*Hq tickets plus B*Hq*splits*(d+2) floats) exceeds that size returns
+ * PRHS_EINVAL. The first call on each device resolves the array's device
+ * address (cudaGetSymbolAddress), so make that first call before any stream
+ * capture. Every call shares the array: calls that overlap on the GPU (other
+ * streams, other threads) race and give wrong results; serialise them. Each
+ * call clears its tickets with cudaMemsetAsync before the kernel runs; it
+ * calls no cudaMalloc, cudaFree or allocating routine. */
+#define PRHS_NOALLOC_SCRATCH_BYTES (4u << 20)
+prhs_status prhs_sparse_attn_noalloc(const prhs_kv* kv, const void* q, float scale,
+                                     const int32_t* idx, const int32_t* n_sel, int cap,
+                                     float* out, float* lse, cudaStream_t stream);
+
 /* Dense attention over all t_b keys (the dense baseline of Table IV). The
  * Hq/Hkv query heads of one KV head share each K/V row read. */
 prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float* out,

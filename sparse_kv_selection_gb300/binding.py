@@ -22,7 +22,7 @@ DEV_TIMEOUT, DEV_BAD_INDEX, DEV_BAD_LEN, DEV_BAD_BLOCK, DEV_CAPACITY = 1, 2, 4, 
 # Entry points declared in include/prhs.h, in declaration order.
 EXPORTS = ["prhs_workspace_size", "prhs_workspace_init", "prhs_score_select", "prhs_score",
            "prhs_select", "prhs_cis_dilate",
-           "prhs_sparse_attn", "prhs_dense_attn", "prhs_decode_step", "prhs_last_error",
+           "prhs_sparse_attn", "prhs_sparse_attn_noalloc", "prhs_dense_attn", "prhs_decode_step", "prhs_last_error",
            "prhs_device_error_bits", "prhs_status_str", "prhs_last_message", "prhs_num_sms"]
 
 
@@ -62,6 +62,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "prhs_select": (I, [KV, P, I, P, P, P, P, I, P, P, P, I, P, P, Z, P]),
         "prhs_cis_dilate": (I, [KV, P, P, I, P, P, I, D, P, P, I, P, P]),
         "prhs_sparse_attn": (I, [KV, P, F, P, P, I, P, P, P, Z, P]),
+        "prhs_sparse_attn_noalloc": (I, [KV, P, F, P, P, I, P, P, P]),
         "prhs_dense_attn": (I, [KV, P, F, P, P, P, Z, P]),
         "prhs_decode_step": (I, [KV, P, F, I, P, I, D, P, P, I, P, P, P, I, P, P, P, P, P, Z, P]),
         "prhs_last_error": (I, []),
@@ -206,6 +207,13 @@ def sparse_attn(kv, q, scale, idx, n_sel, out, lse, ws, stream=None) -> None:
     _check(load().prhs_sparse_attn(kv.ref(), _ptr(q), float(scale), _ptr(idx), _ptr(n_sel),
                                    idx.shape[-1], _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                                    _stream(stream)), "sparse_attn")
+
+
+def sparse_attn_noalloc(kv, q, scale, idx, n_sel, out, lse, stream=None) -> None:
+    """prhs_sparse_attn without a workspace (fixed in-library scratch)."""
+    _check(load().prhs_sparse_attn_noalloc(kv.ref(), _ptr(q), float(scale), _ptr(idx),
+                                           _ptr(n_sel), idx.shape[-1], _ptr(out), _ptr(lse),
+                                           _stream(stream)), "sparse_attn_noalloc")
 
 
 def dense_attn(kv, q, scale, out, lse, ws, stream=None) -> None:

@@ -357,6 +357,21 @@ bool dilated_fits(long long anchor_cap, int w, int tmax, int cap) {
 }
 
 }  // namespace
+
+// Internal hooks for other translation units of the library (no C linkage).
+prhs_status abi_check_kv(const prhs_kv* kv) { return check_kv(kv); }
+prhs_status abi_device(unsigned** err, int* sms) {
+  DeviceInfo* di = nullptr;
+  prhs_status s = device_info(&di);
+  if (s != PRHS_OK) return s;
+  *err = di->err;
+  *sms = di->sms;
+  return PRHS_OK;
+}
+prhs_status abi_fail(prhs_status s, const char* msg) { return fail(s, "%s", msg); }
+KVView abi_view(const prhs_kv& kv, unsigned* err) { return view_of(kv, err); }
+int abi_sparse_splits(const prhs_kv& kv, int sms) { return sparse_splits(kv, sms); }
+
 }  // namespace prhs
 
 using namespace prhs;

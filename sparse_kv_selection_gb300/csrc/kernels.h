@@ -80,6 +80,15 @@ cudaError_t launch_select(const SelectLaunch& a, cudaStream_t s);
 cudaError_t launch_cis(const CisLaunch& a, cudaStream_t s);
 cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t s);
 
+// Hooks into the C ABI layer for the library's other entry-point files:
+// descriptor checks, per-device facts (error word, SM count), the failure
+// message of prhs_last_message, and the split-K factor of sparse attention.
+prhs_status abi_check_kv(const prhs_kv* kv);
+prhs_status abi_device(unsigned** err, int* sms);
+prhs_status abi_fail(prhs_status s, const char* msg);
+KVView abi_view(const prhs_kv& kv, unsigned* err);
+int abi_sparse_splits(const prhs_kv& kv, int sms);
+
 // Bytes of dynamic shared memory the scoring kernel needs for this shape.
 size_t score_smem_bytes(prhs_dtype dt, int d);
 

@@ -49,6 +49,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="host time budget of the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kernels", action="store_true",
+                   help="time each kernel alone on the workload (all heads retrieving) instead")
     return p.parse_args()
 
 
@@ -253,6 +255,10 @@ def run_ours(args):
         anchor_n.zero_()
         for s in range(Sq):
             kv = kvs[s % R]
+            if ev is None:  # the product path: one prhs_decode_step per query
+                S.decode_step(kv, q[s], scale, N, wl.w, wl.tau, anchor_idx, anchor_n, q_anchor,
+                              idx, n_sel[s], reuse[s], delta[s], out[s], lse[s], ws, n_budget=nb)
+                continue
             if ev is not None:
                 ev[s][0].record()
             S.cis_dilate(kv, anchor_idx, anchor_n, q[s], q_anchor, wl.w, wl.tau, idx, n_sel[s],
@@ -271,7 +277,7 @@ def run_ours(args):
             if ev is not None:
                 ev[s][4].record()
 
-    launches_per_step = 4 * Sq
+    launches_per_step = 5 * Sq   # cis, score, select, and two sparse-attention branches
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -429,10 +435,111 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_kernels(args):
+    """Each kernel alone, every head retrieving: dense attention, scoring,
+    selection and sparse attention over the fresh top-N sets and over their
+    dilations. Launches are replayed from CUDA graphs over the rotating KV
+    copies; one JSON line with the per-launch time and achieved GB/s."""
+    import torch
+    import __graft_entry__ as entry
+    entry.build()
+    import sparse_kv_selection_gb300 as S
+    from workloads import preset
+    from workloads.torch_io import upload
+
+    wl = preset(args.config, seed=0)
+    dev = upload(wl)
+    B, Hq, d = wl.B, wl.Hq, wl.d
+    es = 2 if wl.dtype == "bf16" else 4
+    kv_bytes = wl.kv_bytes()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    R = max(1, math.ceil(2 * l2 / kv_bytes))
+    kvs = []
+    for r in range(R):
+        k = dev["k"] if r == 0 else dev["k"].clone()
+        v = dev["v"] if r == 0 else dev["v"].clone()
+        kvs.append(S.KVCache(k, v, dev["seq_lens"], Hq, block_table=dev["block_table"]))
+    varied = len(set(wl.budget.tolist())) > 1
+    N = 0 if varied else int(wl.budget[0])
+    nb = dev["budget"] if varied else None
+    acap = max(1, min(int(wl.budget.max()), kvs[0].t_max))
+    cap = max(1, min(kvs[0].t_max, acap * (2 * wl.w + 1)))
+    i32 = dict(device="cuda", dtype=torch.int32)
+    idx = torch.zeros(B, Hq, acap, **i32)
+    n_sel = torch.zeros(B, Hq, **i32)
+    didx = torch.zeros(B, Hq, cap, **i32)
+    dn = torch.zeros(B, Hq, **i32)
+    reuse = torch.zeros(B, Hq, device="cuda", dtype=torch.uint8)
+    delta = torch.zeros(B, Hq, device="cuda")
+    out = torch.zeros(B, Hq, d, device="cuda")
+    lse = torch.zeros(B, Hq, device="cuda")
+    ws = S.make_workspace(kvs[0], cap)
+    q = dev["q"][0]
+    # fresh sets, then their dilation (every head "reuses" its own query)
+    S.score_select(kvs[0], q, wl.scale, N, idx, n_sel, delta, ws, n_budget=nb)
+    S.cis_dilate(kvs[0], idx, n_sel, q, q, wl.w, -2.0, didx, dn, reuse)
+    torch.cuda.synchronize()
+    tl = wl.seq_lens.astype(np.int64)
+    n_h = n_sel.cpu().numpy().astype(np.int64)
+    dn_h = dn.cpu().numpy().astype(np.int64)
+    kv_rows = float(tl.sum() * wl.Hkv)
+    cases = {
+        "dense_attn": (lambda kv: S.dense_attn(kv, q, wl.scale, out, lse, ws),
+                       2 * kv_rows * d * es),
+        "score": (lambda kv: S.binding.score(kv, q, wl.scale, ws), kv_rows * d * es),
+        "select": (lambda kv: S.binding.select(kv, q, N, idx, n_sel, delta, ws, n_budget=nb),
+                   float(B * Hq * tl.mean() * 4)),
+        "sparse_attn_topN": (lambda kv: S.sparse_attn(kv, q, wl.scale, idx, n_sel, out, lse, ws),
+                             float(n_h.sum() * 2 * d * es)),
+        "sparse_attn_dilated": (lambda kv: S.sparse_attn(kv, q, wl.scale, didx, dn, out, lse, ws),
+                                float(dn_h.sum() * 2 * d * es)),
+    }
+    peak, peak_kind = measured_peak_gbs()
+    stream = torch.cuda.Stream()
+    reps = max(4, 32 // R) * R
+    res = {}
+    for name, (fn, nbytes) in cases.items():
+        if name == "select":
+            with torch.cuda.stream(stream):
+                S.binding.score(kvs[0], q, wl.scale, ws)
+        with torch.cuda.stream(stream):
+            for r in range(R):
+                fn(kvs[r])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                fn(kvs[i % R] if name != "select" else kvs[0])
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(args.steps):
+                g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / (args.steps * reps)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"us_per_launch": us, "alg_bytes": nbytes, "achieved_gbs": gbs,
+                     "frac_of_measured": gbs / peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
+    assert S.last_error() == 0
+    res["sparse_over_dense_time"] = (res["sparse_attn_dilated"]["us_per_launch"] /
+                                     res["dense_attn"]["us_per_launch"])
+    res["sparse_over_dense_bytes"] = (res["sparse_attn_dilated"]["alg_bytes"] /
+                                      res["dense_attn"]["alg_bytes"])
+    print(json.dumps({"mode": "kernels", "config": workload_label(wl), "peak_gbs": peak,
+                      "peak_kind": peak_kind, "kv_copies": R, "launches_per_replay": reps,
+                      "results": res}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernels:
+        run_kernels(args)
     else:
         run_ours(args)
 

@@ -151,8 +151,8 @@ prhs_status prhs_sparse_attn(const prhs_kv* kv, const void* q, float scale,
  * workspace; the split-K scratch is a fixed device array of
  * PRHS_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that
  * loads it until the process exits. A batch whose scratch (256-byte-rounded
- * B*Hq tickets plus B*Hq*splits*(d+2) floats) exceeds that size returns
- * PRHS_EINVAL. The first call on each device resolves the array's device
+ * B*Hq tickets plus (ctas + B*Hq)*(d+2) floats, ctas <= 4 per SM) exceeds
+ * that size returns PRHS_EINVAL. The first call on each device resolves the array's device
  * address (cudaGetSymbolAddress), so make that first call before any stream
  * capture. Every call shares the array: calls that overlap on the GPU (other
  * streams, other threads) race and give wrong results; serialise them. Each
@@ -163,8 +163,10 @@ prhs_status prhs_sparse_attn_noalloc(const prhs_kv* kv, const void* q, float sca
                                      const int32_t* idx, const int32_t* n_sel, int cap,
                                      float* out, float* lse, cudaStream_t stream);
 
-/* Dense attention over all t_b keys (the dense baseline of Table IV). The
- * Hq/Hkv query heads of one KV head share each K/V row read. */
+/* Dense attention over all t_b keys (the dense baseline of Table IV), with
+ * the same outputs as prhs_sparse_attn over idx = [0, t_b). Work is split by
+ * query head; the query heads of one KV head read its rows side by side, so
+ * HBM sees each row about once and the repeats are served from L2. */
 prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float* out,
                             float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
 

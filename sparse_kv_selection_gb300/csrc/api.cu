@@ -38,6 +38,8 @@ struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   unsigned* err = nullptr;
+  cudaStream_t side = nullptr;   // second branch of prhs_decode_step
+  cudaEvent_t fork = nullptr, join = nullptr;
 };
 DeviceInfo g_dev[MAX_DEVICES];
 std::mutex g_dev_mu;
@@ -57,6 +59,11 @@ prhs_status device_info(DeviceInfo** out) {
     e = cudaGetSymbolAddress(&p, g_error_word);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
     di.err = static_cast<unsigned*>(p);
+    e = cudaStreamCreateWithFlags(&di.side, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
+    e = cudaEventCreateWithFlags(&di.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&di.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreateWithFlags");
     di.ready = true;
   }
   *out = &di;
@@ -86,6 +93,8 @@ EncodeTiledFn encode_fn() {
 // ---------------------------------------------------------------------------
 // descriptor checks
 // ---------------------------------------------------------------------------
+constexpr int MAX_UNITS = 16384;  // B * Hq: bounds the kernels' shared prefix arrays
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int t_max_of(const prhs_kv& kv) {
@@ -99,6 +108,8 @@ prhs_status check_kv(const prhs_kv* kv) {
   if (kv->B <= 0 || kv->Hq <= 0 || kv->Hkv <= 0)
     return fail(PRHS_EINVAL, "B, Hq, Hkv must be positive (got %d, %d, %d)", kv->B, kv->Hq, kv->Hkv);
   if (kv->Hq % kv->Hkv != 0) return fail(PRHS_EINVAL, "Hq %% Hkv != 0");
+  if ((long long)kv->B * kv->Hq > MAX_UNITS)
+    return fail(PRHS_EUNSUPPORTED, "B * Hq = %lld above %d", (long long)kv->B * kv->Hq, MAX_UNITS);
   const int G = kv->Hq / kv->Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8)
     return fail(PRHS_EUNSUPPORTED, "query group Hq/Hkv = %d not built (1, 2, 4, 8)", G);
@@ -148,38 +159,36 @@ size_t elem_size(prhs_dtype dt) { return dt == PRHS_BF16 ? 2 : 4; }
 // launch geometry and workspace layout
 // ---------------------------------------------------------------------------
 constexpr int ATTN_CTAS_PER_SM = 4;
-constexpr int MAX_SPLITS = 256;
+constexpr int SCORE_CTAS_PER_SM = 2;
 
-int sparse_splits(const prhs_kv& kv, int sms) {
-  const int units = kv.B * kv.Hq;
-  int s = (ATTN_CTAS_PER_SM * sms + units - 1) / units;
-  return s < 1 ? 1 : (s > MAX_SPLITS ? MAX_SPLITS : s);
-}
-
-int dense_splits(const prhs_kv& kv, int sms) {
-  const int units = kv.B * kv.Hkv;
-  int s = (ATTN_CTAS_PER_SM * sms + units - 1) / units;
-  const int by_len = (t_max_of(kv) + 63) / 64;
-  if (s > by_len) s = by_len;
-  return s < 1 ? 1 : (s > MAX_SPLITS ? MAX_SPLITS : s);
+// CTAs of the attention kernels: enough for every SM to hold four, fewer
+// when the rows can be bounded from the host (about 32 rows per CTA).
+int attn_ctas(const prhs_kv& kv, bool sparse, int cap, int sms) {
+  const long long units = (long long)kv.B * kv.Hq;  // both kernels split by query head
+  const long long rows = units * (sparse ? cap : t_max_of(kv));
+  long long c = (rows + 31) / 32;
+  const long long most = (long long)ATTN_CTAS_PER_SM * sms;
+  if (c > most) c = most;
+  return c < 1 ? 1 : (int)c;
 }
 
 struct Layout {
-  size_t counters, partials, scores, total;
+  size_t counters, partials, partials2, scores, total;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 Layout layout_of(const prhs_kv& kv, int sms) {
   Layout L;
-  const int G = kv.Hq / kv.Hkv;
+  const KVView v = view_of(kv, nullptr);
+  const int most = ATTN_CTAS_PER_SM * sms;
+  const size_t ps = attn_partial_floats(v, true, most);
+  const size_t pd = attn_partial_floats(v, false, most);
   const size_t units = (size_t)kv.B * kv.Hq;  // >= B * Hkv
-  const size_t ps = (size_t)kv.B * kv.Hq * sparse_splits(kv, sms);
-  const size_t pd = (size_t)kv.B * kv.Hkv * G * dense_splits(kv, sms);
-  const size_t prec = (size_t)(kv.d + 2) * sizeof(float);
   L.counters = 0;
   L.partials = round_up(units * sizeof(unsigned), 256);
-  L.scores = round_up(L.partials + (ps > pd ? ps : pd) * prec, 256);
+  L.partials2 = round_up(L.partials + (ps > pd ? ps : pd) * sizeof(float), 256);
+  L.scores = round_up(L.partials2 + ps * sizeof(float), 256);
   L.total = round_up(L.scores + (size_t)kv.B * kv.Hq * t_max_of(kv) * sizeof(float), 256);
   return L;
 }
@@ -216,26 +225,6 @@ prhs_status make_tmap(const prhs_kv& kv, int box_rows, CUtensorMap* map) {
   return PRHS_OK;
 }
 
-// Keys per scoring CTA: fill every SM (two resident CTAs each) in one wave
-// when the cache is small, bounded chunks when it is large.
-void score_geometry(const prhs_kv& kv, int sms, int* chunk_keys, int* nchunks) {
-  const int tmax = t_max_of(kv);
-  const int tiles = (tmax + SCORE_TILE - 1) / SCORE_TILE;
-  const int units = kv.B * kv.Hkv;
-  const int slots = 2 * sms;
-  int per;
-  if (units <= slots) {
-    int nc = slots / units;
-    if (nc < 1) nc = 1;
-    per = (tiles + nc - 1) / nc;
-  } else {
-    per = tiles < 16 ? tiles : 16;
-  }
-  if (per < 1) per = 1;
-  *chunk_keys = per * SCORE_TILE;
-  *nchunks = (tiles + per - 1) / per;
-}
-
 prhs_status launch_result(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return PRHS_OK;
   if (e == cudaErrorNotSupported) return fail(PRHS_EUNSUPPORTED, "%s: shape not built", what);
@@ -255,7 +244,7 @@ prhs_status do_score(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* w
   sl.head_skip = head_skip;
   sl.scores = reinterpret_cast<float*>(static_cast<char*>(ws) + L.scores);
   sl.paged = paged;
-  score_geometry(kv, di->sms, &sl.chunk_keys, &sl.nchunks);
+  sl.ctas = SCORE_CTAS_PER_SM * di->sms;
   return launch_result(launch_score(sl, &map, st), "score kernel");
 }
 
@@ -314,19 +303,22 @@ prhs_status check_select_args(const prhs_kv& kv, const void* q, int N, const int
 
 prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws, const void* q,
                     float scale, const int32_t* idx, const int32_t* n_sel, int cap, float* out,
-                    float* lse, bool sparse, cudaStream_t st) {
+                    float* lse, bool sparse, cudaStream_t st, const uint8_t* unit_mask = nullptr,
+                    int mask_want = 0, bool second_region = false) {
   AttnLaunch a;
   a.kv = view_of(kv, di->err);
   a.q = q;
   a.scale = scale;
   a.idx = idx;
   a.n_sel = n_sel;
+  a.unit_mask = unit_mask;
+  a.mask_want = mask_want;
   a.cap = cap;
   a.out = out;
   a.lse = lse;
-  a.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partials);
+  a.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + (second_region ? L.partials2 : L.partials));
   a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.counters);
-  a.splits = sparse ? sparse_splits(kv, di->sms) : dense_splits(kv, di->sms);
+  a.ctas = attn_ctas(kv, sparse, cap, di->sms);
   return launch_result(launch_attn(a, sparse, st), sparse ? "sparse attention" : "dense attention");
 }
 
@@ -370,7 +362,9 @@ prhs_status abi_device(unsigned** err, int* sms) {
 }
 prhs_status abi_fail(prhs_status s, const char* msg) { return fail(s, "%s", msg); }
 KVView abi_view(const prhs_kv& kv, unsigned* err) { return view_of(kv, err); }
-int abi_sparse_splits(const prhs_kv& kv, int sms) { return sparse_splits(kv, sms); }
+int abi_attn_ctas(const prhs_kv& kv, bool sparse, int cap, int sms) {
+  return attn_ctas(kv, sparse, cap, sms);
+}
 
 }  // namespace prhs
 
@@ -507,10 +501,25 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if ((s = do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, tau, idx, n_sel, cap,
                   reuse, stream)) != PRHS_OK)
     return s;
+  // Two branches after the gate: heads that reuse their anchor only need the
+  // dilated sets and attend on the side stream, while the retrieving heads
+  // score, select and attend on the caller's stream; the caller's stream then
+  // waits for the side branch.
+  cudaError_t e = cudaEventRecord(di->fork, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(di->side, di->fork, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "decode: fork");
+  if ((s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, di->side, reuse, 1,
+                   true)) != PRHS_OK)
+    return s;
   if ((s = do_score_select(*kv, di, L, ws, q, scale, N, n_budget, reuse, idx, n_sel, cap, delta,
                            anchor_idx, anchor_n, anchor_cap, q_anchor, stream)) != PRHS_OK)
     return s;
-  return do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, stream);
+  if ((s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, stream, reuse, 0,
+                   false)) != PRHS_OK)
+    return s;
+  e = cudaEventRecord(di->join, di->side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, di->join, 0);
+  return e == cudaSuccess ? PRHS_OK : cuda_fail(e, "decode: join");
 }
 
 prhs_status prhs_last_error(void) {

@@ -1,22 +1,33 @@
-// Split-K decode attention over a selected index set (sparse) or over the
-// whole cache (dense baseline).
+// Decode attention over a selected index set (sparse) or over the whole
+// cache (dense baseline), split over CTAs with equal row counts.
 // "Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference":
 // the Table V caption's sparse-attention kernel over the selected KV entries,
 // and Table IV's dense ("Flash") operator as the baseline.
 //
-// Each CTA (4 warps) takes a contiguous slice of one head's rows. Eight lanes
-// share a row: lane j reads 16-byte chunks j, j+8, ... of the K and V rows
-// (128 contiguous bytes per 8 lanes per load), so every gathered row is read
-// with full cache lines. A warp has 4 rows in flight per step and UNROLL steps
-// per iteration. Softmax is online in fp32, in base 2 (logits pre-scaled by
-// log2 e). The dense kernel computes all G query heads of a KV head from the
-// same loaded rows. The last CTA of a head (atomic ticket, no waiting) merges
-// the per-CTA partials into out and lse and resets the ticket.
+// Work split. A unit is a query head (sparse) or a KV head with its G query
+// heads (dense); unit u owns rows(u) rows (n_sel or t_b). Every CTA reads
+// all rows(u), forms their prefix sums P and takes rows [c*per, (c+1)*per)
+// of the concatenation, per = ceil(total / CTAs): each CTA gets the same
+// number of rows whatever the mix of set sizes, and a CTA may cover the end
+// of one unit and the start of the next. A unit covered by one CTA is
+// written directly; otherwise each covering CTA writes a partial softmax
+// state into slot c + u and the last one to arrive (atomic ticket, no
+// waiting) merges them into out and lse and resets the ticket.
+//
+// Gather. Eight lanes share a row: lane j reads 16-byte chunks j, j+8, ... of
+// the K and V rows (128 contiguous bytes per 8 lanes per load), so every
+// gathered row arrives as full cache lines. A warp keeps 4 rows per step and
+// UNROLL steps in flight; the row numbers of a segment are staged in shared
+// memory first. Softmax is online in fp32 and base 2 (logits pre-scaled by
+// log2 e). Units are query heads in both kernels; the kernel template can
+// also give one unit the G query heads of a KV head (registers per thread
+// grow with G, which costs more occupancy than the L2 re-reads it saves).
 #include "kernels.h"
 
 namespace prhs {
 
 constexpr int ATTN_THREADS = 128;
+constexpr int ATTN_IDX_STAGE = 2048;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -30,247 +41,360 @@ struct AttnShape {
   static_assert(CPR % 8 == 0, "row must be a multiple of 128 bytes");
 };
 
-template <typename T, int D, int G, bool SPARSE, int UNROLL>
+template <int CPL, int G>
+struct AttnUnroll {
+  static constexpr int base = G <= 2 ? 4 : (G == 4 ? 2 : 1);
+  static constexpr int value = CPL >= 4 ? (base > 1 ? base / 2 : 1) : base;
+};
+
+// Merge two online-softmax states (m, l, o) in base 2.
+__device__ __forceinline__ void merge_coeffs(float m1, float m2, float& M, float& c1, float& c2) {
+  M = fmaxf(m1, m2);
+  c1 = M == -INFINITY ? 0.f : exp2f(m1 - M);
+  c2 = M == -INFINITY ? 0.f : exp2f(m2 - M);
+}
+
+template <typename T, int D, int G, bool SPARSE>
 __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(const AttnLaunch a) {
   using S = AttnShape<T, D>;
+  constexpr int UNROLL = AttnUnroll<S::CPL, G>::value;
+  constexpr int STEP = 16 * UNROLL;  // rows per CTA iteration
+  constexpr int PW = D + 2;          // partial record: m, l, o[D]
+  extern __shared__ int sh_prefix[];  // [units + 1]
+  __shared__ int sh_idx[SPARSE ? ATTN_IDX_STAGE : 1];
+  __shared__ float sm_m[4][G], sm_l[4][G];
+  __shared__ float sm_o[4][G][D];
+  __shared__ int sh_wsum[ATTN_THREADS / 32];
+  __shared__ int sh_last;
+
+  pdl_wait();
+  pdl_trigger();
+
   const KVView& kv = a.kv;
-  const int unit = blockIdx.y;  // sparse: b * Hq + h;  dense: b * Hkv + kv head
-  const int split = blockIdx.x;
-  const int group = kv.Hq / kv.Hkv;
-  int b, kvh, qh0;
-  if (SPARSE) {
-    b = unit / kv.Hq;
-    qh0 = unit;
-    kvh = (unit % kv.Hq) / group;
-  } else {
-    b = unit / kv.Hkv;
-    kvh = unit % kv.Hkv;
-    qh0 = b * kv.Hq + kvh * G;
-  }
-  const int t = seq_len(kv, b);
-  int n;
-  const int32_t* rows = nullptr;
-  if (SPARSE) {
-    n = a.n_sel[unit];
-    if (n < 0 || n > a.cap) {
-      if (threadIdx.x == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
-      n = n < 0 ? 0 : a.cap;
-    }
-    rows = a.idx + (long long)unit * a.cap;
-  } else {
-    n = t;
-  }
-  const int chunk = (n + a.splits - 1) / a.splits;
-  const int r0 = min(n, split * chunk);
-  const int r1 = min(n, r0 + chunk);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sg = lane >> 3, j = lane & 7;
-  const float qscale = a.scale * LOG2E;
+  // units are query heads unless G query heads share one dense unit
+  constexpr bool PER_QUERY = SPARSE || G == 1;
+  const int U = PER_QUERY ? kv.B * kv.Hq : kv.B * kv.Hkv;
+  const int C = gridDim.x, c = blockIdx.x;
+  const int group = kv.Hq / kv.Hkv;
 
-  float qf[G][S::EL];
+  // ---- rows per unit and their prefix sums (every CTA computes the same) ----
+  {
+    const int per_t = (U + ATTN_THREADS - 1) / ATTN_THREADS;
+    const int u0 = tid * per_t;
+    int loc = 0;
+    for (int k = 0; k < per_t; k++) {
+      const int u = u0 + k;
+      if (u >= U) break;
+      int r;
+      if (SPARSE && a.unit_mask != nullptr && (a.unit_mask[u] != 0) != (a.mask_want != 0)) {
+        r = 0;  // another launch attends this unit
+      } else if (SPARSE) {
+        r = a.n_sel[u];
+        if (r < 0 || r > a.cap) {
+          raise_error(kv.err, PRHS_DEV_CAPACITY);
+          r = r < 0 ? 0 : a.cap;
+        }
+      } else {
+        r = seq_len(kv, PER_QUERY ? u / kv.Hq : u / kv.Hkv);
+      }
+      sh_prefix[u] = r;  // temporarily the count
+      loc += r;
+    }
+    int v = loc;
 #pragma unroll
-  for (int g = 0; g < G; g++)
-#pragma unroll
-    for (int c = 0; c < S::CPL; c++)
-#pragma unroll
-      for (int e = 0; e < S::EPC; e++)
-        qf[g][c * S::EPC + e] =
-            Elem<T>::load1(a.q, (long long)(qh0 + g) * D + (c * 8 + j) * S::EPC + e) * qscale;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) sh_wsum[warp] = v;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; w++) before += sh_wsum[w];
+    int run = before + v - loc;
+    for (int k = 0; k < per_t; k++) {
+      const int u = u0 + k;
+      if (u >= U) break;
+      const int r = sh_prefix[u];
+      sh_prefix[u] = run;
+      run += r;
+    }
+    if (tid == ATTN_THREADS - 1) sh_prefix[U] = run;
+    __syncthreads();
+  }
+  const int total = sh_prefix[U];
 
-  float m[G], l[G], o[G][S::EL];
-#pragma unroll
-  for (int g = 0; g < G; g++) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < S::EL; e++) o[g][e] = 0.f;
+  // ---- units with no rows: out = 0, lse = -inf ----
+  for (int u = c; u < U; u += C) {
+    if (sh_prefix[u + 1] != sh_prefix[u]) continue;
+    if (SPARSE && a.unit_mask != nullptr && (a.unit_mask[u] != 0) != (a.mask_want != 0)) continue;
+    const int qh0 = PER_QUERY ? u : (u / kv.Hkv) * kv.Hq + (u % kv.Hkv) * G;
+    for (int x = tid; x < G * D; x += ATTN_THREADS) {
+      a.out[(long long)(qh0 + x / D) * D + x % D] = 0.f;
+      if (x % D == 0) a.lse[qh0 + x / D] = -INFINITY;
+    }
+  }
+  if (total == 0) return;
+  const int per = (total + C - 1) / C;
+  const int lo = c * per, hi = min(total, lo + per);
+  if (lo >= hi) return;
+
+  // first unit with rows overlapping [lo, hi): largest u with P[u] <= lo
+  int ulo = 0, uhi = U - 1;
+  while (ulo < uhi) {
+    const int mid = (ulo + uhi + 1) >> 1;
+    if (sh_prefix[mid] <= lo) ulo = mid; else uhi = mid - 1;
   }
 
   const char* kbase = static_cast<const char*>(kv.k);
   const char* vbase = static_cast<const char*>(kv.v);
-  constexpr int STEP = 16 * UNROLL;  // rows per CTA iteration
-  for (int base = r0; base < r1; base += STEP) {
-    long long row[UNROLL];
+  const float qscale = a.scale * LOG2E;
+
+  for (int u = ulo; u < U && sh_prefix[u] < hi; u++) {
+    const int P0 = sh_prefix[u], P1 = sh_prefix[u + 1];
+    const int r0 = max(lo, P0) - P0, r1 = min(hi, P1) - P0;
+    if (r0 >= r1) continue;
+    int b, kvh, qh0;
+    if (PER_QUERY) {
+      b = u / kv.Hq;
+      qh0 = u;
+      kvh = (u % kv.Hq) / group;
+    } else {
+      b = u / kv.Hkv;
+      kvh = u % kv.Hkv;
+      qh0 = b * kv.Hq + kvh * G;
+    }
+    const int t = seq_len(kv, b);
+
+    float qf[G][S::EL];
 #pragma unroll
-    for (int u = 0; u < UNROLL; u++) {
-      const int r = base + u * 16 + warp * 4 + sg;
-      row[u] = -1;
-      if (r < r1) {
-        const int key = SPARSE ? rows[r] : r;
-        if ((unsigned)key < (unsigned)t) {
-          row[u] = kv_row(kv, b, kvh, key);
-          if (row[u] < 0) raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
-        } else {
-          raise_error(kv.err, PRHS_DEV_BAD_INDEX);
+    for (int g = 0; g < G; g++)
+#pragma unroll
+      for (int cc = 0; cc < S::CPL; cc++)
+#pragma unroll
+        for (int e = 0; e < S::EPC; e++)
+          qf[g][cc * S::EPC + e] =
+              Elem<T>::load1(a.q, (long long)(qh0 + g) * D + (cc * 8 + j) * S::EPC + e) * qscale;
+    float m[G], l[G], o[G][S::EL];
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < S::EL; e++) o[g][e] = 0.f;
+    }
+
+    const int32_t* rows = SPARSE ? a.idx + (long long)u * a.cap : nullptr;
+    for (int sb = r0; sb < r1; sb += (SPARSE ? ATTN_IDX_STAGE : (r1 - r0))) {
+      const int se = SPARSE ? min(r1, sb + ATTN_IDX_STAGE) : r1;
+      if (SPARSE) {
+        __syncthreads();
+        for (int x = tid; x < se - sb; x += ATTN_THREADS) sh_idx[x] = rows[sb + x];
+        __syncthreads();
+      }
+      for (int base = sb; base < se; base += STEP) {
+        long long row[UNROLL];
+#pragma unroll
+        for (int uu = 0; uu < UNROLL; uu++) {
+          const int r = base + uu * 16 + warp * 4 + sg;
+          row[uu] = -1;
+          if (r < se) {
+            const int key = SPARSE ? sh_idx[r - sb] : r;
+            if ((unsigned)key < (unsigned)t) {
+              row[uu] = kv_row(kv, b, kvh, key);
+              if (row[uu] < 0) raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
+            } else {
+              raise_error(kv.err, PRHS_DEV_BAD_INDEX);
+            }
+          }
+        }
+        uint4 kc[UNROLL][S::CPL], vc[UNROLL][S::CPL];
+#pragma unroll
+        for (int uu = 0; uu < UNROLL; uu++)
+#pragma unroll
+          for (int cc = 0; cc < S::CPL; cc++) {
+            if (row[uu] >= 0) {
+              kc[uu][cc] = ldg_stream(kbase + row[uu] * S::RB + (cc * 8 + j) * 16);
+              vc[uu][cc] = ldg_stream(vbase + row[uu] * S::RB + (cc * 8 + j) * 16);
+            } else {
+              kc[uu][cc] = make_uint4(0, 0, 0, 0);
+              vc[uu][cc] = make_uint4(0, 0, 0, 0);
+            }
+          }
+        float s[UNROLL][G];
+#pragma unroll
+        for (int uu = 0; uu < UNROLL; uu++) {
+          float kf[S::EL];
+#pragma unroll
+          for (int cc = 0; cc < S::CPL; cc++) Elem<T>::unpack(kc[uu][cc], kf + cc * S::EPC);
+#pragma unroll
+          for (int g = 0; g < G; g++) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < S::EL; e++) acc = fmaf(qf[g][e], kf[e], acc);
+            acc += __shfl_xor_sync(FULL_MASK, acc, 1);
+            acc += __shfl_xor_sync(FULL_MASK, acc, 2);
+            acc += __shfl_xor_sync(FULL_MASK, acc, 4);
+            s[uu][g] = row[uu] >= 0 ? acc : -INFINITY;
+          }
+        }
+        float vf[UNROLL][S::EL];
+#pragma unroll
+        for (int uu = 0; uu < UNROLL; uu++)
+#pragma unroll
+          for (int cc = 0; cc < S::CPL; cc++) Elem<T>::unpack(vc[uu][cc], vf[uu] + cc * S::EPC);
+#pragma unroll
+        for (int g = 0; g < G; g++) {
+          float mx = m[g];
+#pragma unroll
+          for (int uu = 0; uu < UNROLL; uu++) mx = fmaxf(mx, s[uu][g]);
+          if (mx == -INFINITY) continue;
+          const float corr = exp2f(m[g] - mx);
+          l[g] *= corr;
+#pragma unroll
+          for (int e = 0; e < S::EL; e++) o[g][e] *= corr;
+#pragma unroll
+          for (int uu = 0; uu < UNROLL; uu++) {
+            const float p = exp2f(s[uu][g] - mx);
+            l[g] += p;
+#pragma unroll
+            for (int e = 0; e < S::EL; e++) o[g][e] = fmaf(p, vf[uu][e], o[g][e]);
+          }
+          m[g] = mx;
         }
       }
     }
-    uint4 kc[UNROLL][S::CPL], vc[UNROLL][S::CPL];
+
+    // ---- merge the 4 row groups of each warp, then the 4 warps ----
 #pragma unroll
-    for (int u = 0; u < UNROLL; u++)
+    for (int g = 0; g < G; g++) {
 #pragma unroll
-      for (int c = 0; c < S::CPL; c++) {
-        if (row[u] >= 0) {
-          kc[u][c] = ldg_stream(kbase + row[u] * S::RB + (c * 8 + j) * 16);
-          vc[u][c] = ldg_stream(vbase + row[u] * S::RB + (c * 8 + j) * 16);
-        } else {
-          kc[u][c] = make_uint4(0, 0, 0, 0);
-          vc[u][c] = make_uint4(0, 0, 0, 0);
+      for (int off = 8; off <= 16; off <<= 1) {
+        const float m2 = __shfl_xor_sync(FULL_MASK, m[g], off);
+        const float l2 = __shfl_xor_sync(FULL_MASK, l[g], off);
+        float M, c1, c2;
+        merge_coeffs(m[g], m2, M, c1, c2);
+        l[g] = l[g] * c1 + l2 * c2;
+#pragma unroll
+        for (int e = 0; e < S::EL; e++) {
+          const float o2 = __shfl_xor_sync(FULL_MASK, o[g][e], off);
+          o[g][e] = o[g][e] * c1 + o2 * c2;
         }
+        m[g] = M;
       }
-    float s[UNROLL][G];
-#pragma unroll
-    for (int u = 0; u < UNROLL; u++) {
-      float kf[S::EL];
-#pragma unroll
-      for (int c = 0; c < S::CPL; c++) Elem<T>::unpack(kc[u][c], kf + c * S::EPC);
+    }
+    __syncthreads();  // shared state of the previous segment fully consumed
+    if (lane < 8) {
 #pragma unroll
       for (int g = 0; g < G; g++) {
-        float acc = 0.f;
+        if (lane == 0) {
+          sm_m[warp][g] = m[g];
+          sm_l[warp][g] = l[g];
+        }
 #pragma unroll
-        for (int e = 0; e < S::EL; e++) acc = fmaf(qf[g][e], kf[e], acc);
-        acc += __shfl_xor_sync(FULL_MASK, acc, 1);
-        acc += __shfl_xor_sync(FULL_MASK, acc, 2);
-        acc += __shfl_xor_sync(FULL_MASK, acc, 4);
-        s[u][g] = row[u] >= 0 ? acc : -INFINITY;
+        for (int cc = 0; cc < S::CPL; cc++)
+#pragma unroll
+          for (int e = 0; e < S::EPC; e++)
+            sm_o[warp][g][(cc * 8 + j) * S::EPC + e] = o[g][cc * S::EPC + e];
       }
     }
-    float vf[UNROLL][S::EL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; u++)
-#pragma unroll
-      for (int c = 0; c < S::CPL; c++) Elem<T>::unpack(vc[u][c], vf[u] + c * S::EPC);
-#pragma unroll
-    for (int g = 0; g < G; g++) {
-      float mx = m[g];
-#pragma unroll
-      for (int u = 0; u < UNROLL; u++) mx = fmaxf(mx, s[u][g]);
-      if (mx == -INFINITY) continue;
-      const float corr = exp2f(m[g] - mx);
-      l[g] *= corr;
-#pragma unroll
-      for (int e = 0; e < S::EL; e++) o[g][e] *= corr;
-#pragma unroll
-      for (int u = 0; u < UNROLL; u++) {
-        const float p = exp2f(s[u][g] - mx);
-        l[g] += p;
-#pragma unroll
-        for (int e = 0; e < S::EL; e++) o[g][e] = fmaf(p, vf[u][e], o[g][e]);
-      }
-      m[g] = mx;
-    }
-  }
+    __syncthreads();
 
-  // ---- merge the 4 row groups of the warp (lanes j, j+8, j+16, j+24) ----
+    const int cf = P0 / per, cl = (P1 - 1) / per;  // CTAs covering this unit
+    if (cf == cl) {
+      // the whole unit is in this CTA: final result
+      for (int x = tid; x < G * D; x += ATTN_THREADS) {
+        const int g = x / D, e = x % D;
+        float M = -INFINITY;
 #pragma unroll
-  for (int g = 0; g < G; g++) {
+        for (int w = 0; w < 4; w++) M = fmaxf(M, sm_m[w][g]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
 #pragma unroll
-    for (int off = 8; off <= 16; off <<= 1) {
-      const float m2 = __shfl_xor_sync(FULL_MASK, m[g], off);
-      const float l2 = __shfl_xor_sync(FULL_MASK, l[g], off);
-      const float M = fmaxf(m[g], m2);
-      const float c1 = M == -INFINITY ? 0.f : exp2f(m[g] - M);
-      const float c2 = M == -INFINITY ? 0.f : exp2f(m2 - M);
-      l[g] = l[g] * c1 + l2 * c2;
-#pragma unroll
-      for (int e = 0; e < S::EL; e++) {
-        const float o2 = __shfl_xor_sync(FULL_MASK, o[g][e], off);
-        o[g][e] = o[g][e] * c1 + o2 * c2;
+          for (int w = 0; w < 4; w++) {
+            const float cw = exp2f(sm_m[w][g] - M);
+            L += cw * sm_l[w][g];
+            O += cw * sm_o[w][g][e];
+          }
+        }
+        a.out[(long long)(qh0 + g) * D + e] = L > 0.f ? O / L : 0.f;
+        if (e == 0) a.lse[qh0 + g] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
       }
-      m[g] = M;
+      continue;
     }
+    for (int x = tid; x < G * D; x += ATTN_THREADS) {
+      const int g = x / D, e = x % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; w++) M = fmaxf(M, sm_m[w][g]);
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < 4; w++) {
+          const float cw = exp2f(sm_m[w][g] - M);
+          L += cw * sm_l[w][g];
+          O += cw * sm_o[w][g][e];
+        }
+      }
+      float* rec = a.partials + ((long long)(c + u) * G + g) * PW;
+      rec[2 + e] = O;
+      if (e == 0) {
+        rec[0] = M;
+        rec[1] = L;
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sh_last = atomicAdd(&a.counters[u], 1u) == (unsigned)(cl - cf);
+    __syncthreads();
+    if (!sh_last) continue;
+    __threadfence();
+    for (int x = tid; x < G * D; x += ATTN_THREADS) {
+      const int g = x / D, e = x % D;
+      float M = -INFINITY;
+      for (int cs = cf; cs <= cl; cs++)
+        M = fmaxf(M, __ldcg(a.partials + ((long long)(cs + u) * G + g) * PW));
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+        for (int cs = cf; cs <= cl; cs++) {
+          const float* rec = a.partials + ((long long)(cs + u) * G + g) * PW;
+          const float cw = exp2f(__ldcg(rec) - M);
+          L += cw * __ldcg(rec + 1);
+          O += cw * __ldcg(rec + 2 + e);
+        }
+      }
+      a.out[(long long)(qh0 + g) * D + e] = L > 0.f ? O / L : 0.f;
+      if (e == 0) a.lse[qh0 + g] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+    }
+    if (tid == 0) a.counters[u] = 0u;
   }
+}
 
-  // ---- merge the 4 warps through shared memory, write this CTA's partial ----
-  __shared__ float sm_m[4][G], sm_l[4][G];
-  __shared__ float sm_o[4][G][D];
-  __shared__ int sh_last;
-  if (lane < 8) {
-#pragma unroll
-    for (int g = 0; g < G; g++) {
-      if (lane == 0) {
-        sm_m[warp][g] = m[g];
-        sm_l[warp][g] = l[g];
-      }
-#pragma unroll
-      for (int c = 0; c < S::CPL; c++)
-#pragma unroll
-        for (int e = 0; e < S::EPC; e++) sm_o[warp][g][(c * 8 + j) * S::EPC + e] = o[g][c * S::EPC + e];
-    }
-  }
-  __syncthreads();
-  constexpr int PW = D + 2;  // partial record: m, l, o[D]
-  float* part = a.partials + ((long long)unit * G * a.splits) * PW;
-  for (int x = threadIdx.x; x < G * D; x += ATTN_THREADS) {
-    const int g = x / D, e = x % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; w++) M = fmaxf(M, sm_m[w][g]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < 4; w++) {
-        const float c = exp2f(sm_m[w][g] - M);
-        L += c * sm_l[w][g];
-        O += c * sm_o[w][g][e];
-      }
-    }
-    float* rec = part + ((long long)g * a.splits + split) * PW;
-    rec[2 + e] = O;
-    if (e == 0) {
-      rec[0] = M;
-      rec[1] = L;
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) sh_last = atomicAdd(&a.counters[unit], 1u) == (unsigned)(a.splits - 1);
-  __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
+// Both kernels split by query head: the dense one reads each K/V row once per
+// query head of the group, and the group's CTAs, running side by side, find
+// the rows their neighbours just brought into L2.
+int attn_units(const KVView& kv, bool sparse) { (void)sparse; return kv.B * kv.Hq; }
 
-  // ---- last CTA of this unit: combine every split ----
-  for (int x = threadIdx.x; x < G * D; x += ATTN_THREADS) {
-    const int g = x / D, e = x % D;
-    const float* recs = part + (long long)g * a.splits * PW;
-    float M = -INFINITY;
-    for (int sp = 0; sp < a.splits; sp++) M = fmaxf(M, __ldcg(recs + (long long)sp * PW));
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-      for (int sp = 0; sp < a.splits; sp++) {
-        const float* rec = recs + (long long)sp * PW;
-        const float c = exp2f(__ldcg(rec) - M);
-        L += c * __ldcg(rec + 1);
-        O += c * __ldcg(rec + 2 + e);
-      }
-    }
-    const long long qh = qh0 + g;
-    a.out[qh * D + e] = L > 0.f ? O / L : 0.f;
-    if (e == 0) a.lse[qh] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
-  }
-  if (threadIdx.x == 0) a.counters[unit] = 0u;
+size_t attn_partial_floats(const KVView& kv, bool sparse, int ctas) {
+  return ((size_t)ctas + attn_units(kv, sparse)) * (kv.d + 2);
 }
 
 template <typename T, int D, int G, bool SPARSE>
-static cudaError_t attn_go(const AttnLaunch& a, int units, cudaStream_t st) {
-  dim3 grid(a.splits, units);
-  attn_kernel<T, D, G, SPARSE, 2><<<grid, ATTN_THREADS, 0, st>>>(a);
-  return cudaGetLastError();
+static cudaError_t attn_go(const AttnLaunch& a, cudaStream_t st) {
+  const size_t smem = ((size_t)attn_units(a.kv, SPARSE) + 1) * sizeof(int);
+  auto k = attn_kernel<T, D, G, SPARSE>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(k, dim3(a.ctas), dim3(ATTN_THREADS), smem, st, a);
 }
 
 template <typename T, int D>
 static cudaError_t attn_dispatch(const AttnLaunch& a, bool sparse, cudaStream_t st) {
-  const KVView& kv = a.kv;
-  if (sparse) return attn_go<T, D, 1, true>(a, kv.B * kv.Hq, st);
-  const int units = kv.B * kv.Hkv;
-  switch (kv.Hq / kv.Hkv) {
-    case 1: return attn_go<T, D, 1, false>(a, units, st);
-    case 2: return attn_go<T, D, 2, false>(a, units, st);
-    case 4: return attn_go<T, D, 4, false>(a, units, st);
-    case 8: return attn_go<T, D, 8, false>(a, units, st);
-  }
-  return cudaErrorNotSupported;
+  if (sparse) return attn_go<T, D, 1, true>(a, st);
+  return attn_go<T, D, 1, false>(a, st);
 }
 
 cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t st) {

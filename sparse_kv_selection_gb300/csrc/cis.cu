@@ -28,12 +28,24 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   __shared__ double red[3][CIS_THREADS / 32];
   __shared__ int sh_reuse;
   __shared__ int warp_tot[CIS_THREADS / 32];
+  pdl_wait();
+  pdl_trigger();
   const KVView& kv = a.kv;
   const int qh = blockIdx.x;
   const int b = qh / kv.Hq;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int d = kv.d;
 
+  // everything this CTA may need is requested before any result is used
+  int n = a.anchor_n[qh];
+  const int t = seq_len(kv, b);
+  const int32_t* anc = a.anchor_idx + (long long)qh * a.anchor_cap;
+  const int ncap = min(n, a.anchor_cap);
+  int pre_x = -1, pre_prev = -1;
+  if (tid < ncap) {
+    pre_x = anc[tid];
+    pre_prev = tid > 0 ? anc[tid - 1] : -1;
+  }
   double dot = 0.0, nq = 0.0, na = 0.0;
   for (int i = tid; i < d; i += CIS_THREADS) {
     const double x = (double)Elem<T>::load1(a.q, (long long)qh * d + i);
@@ -59,8 +71,7 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
       A += red[2][w];
     }
     const double den = sqrt(Q) * sqrt(A);
-    const int n_anchor = a.anchor_n[qh];
-    const int reuse = n_anchor > 0 && den > 0.0 && (D / den) >= a.tau;
+    const int reuse = n > 0 && den > 0.0 && (D / den) >= a.tau;
     sh_reuse = reuse;
     a.reuse[qh] = (uint8_t)reuse;
   }
@@ -68,13 +79,10 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   if (!sh_reuse) return;
 
   // ---- dilation of the anchor set ----
-  const int t = seq_len(kv, b);
-  int n = a.anchor_n[qh];
   if (n > a.anchor_cap) {
     if (tid == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
     n = a.anchor_cap;
   }
-  const int32_t* anc = a.anchor_idx + (long long)qh * a.anchor_cap;
   int32_t* out = a.idx + (long long)qh * a.cap;
   const int w = a.w;
   int carry = 0;
@@ -82,8 +90,8 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
     const int jdx = base + tid;
     int start = 0, cnt = 0;
     if (jdx < n) {
-      const int x = anc[jdx];
-      const int prev = jdx > 0 ? anc[jdx - 1] : -1;
+      const int x = base == 0 ? pre_x : anc[jdx];
+      const int prev = base == 0 ? pre_prev : anc[jdx - 1];
       if (x < 0 || x >= t || x <= prev) {
         raise_error(kv.err, PRHS_DEV_BAD_INDEX);
       } else {
@@ -124,11 +132,8 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
 }
 
 cudaError_t launch_cis(const CisLaunch& a, cudaStream_t st) {
-  if (a.kv.dtype == PRHS_BF16)
-    cis_kernel<__nv_bfloat16><<<a.kv.B * a.kv.Hq, CIS_THREADS, 0, st>>>(a);
-  else
-    cis_kernel<float><<<a.kv.B * a.kv.Hq, CIS_THREADS, 0, st>>>(a);
-  return cudaGetLastError();
+  void (*k)(const CisLaunch) = a.kv.dtype == PRHS_BF16 ? cis_kernel<__nv_bfloat16> : cis_kernel<float>;
+  return launch_pdl(k, dim3(a.kv.B * a.kv.Hq), dim3(CIS_THREADS), 0, st, a);
 }
 
 }  // namespace prhs

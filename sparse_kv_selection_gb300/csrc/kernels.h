@@ -17,6 +17,12 @@ constexpr int PAGED_BOX_ROWS = 16;
 // Scores cached in shared memory by the selection kernel (floats).
 constexpr int SELECT_CACHE_FLOATS = 48 * 1024;
 constexpr int SELECT_THREADS = 1024;
+// Logits held in shared memory per CTA by the cluster selection kernel: one
+// CTA takes up to SELECT_SLICE_ONE, a cluster of 2..8 CTAs up to
+// SELECT_SLICE_MAX each; longer caches use the single-CTA kernel that streams
+// them from L2.
+constexpr int SELECT_SLICE_ONE = 44032;
+constexpr int SELECT_SLICE_MAX = 16384;
 
 struct ScoreLaunch {
   KVView kv;
@@ -24,8 +30,7 @@ struct ScoreLaunch {
   float scale;
   const uint8_t* head_skip;  // [B][Hq] or null
   float* scores;             // [B][Hq][t_max]
-  int chunk_keys;            // keys per CTA (multiple of SCORE_TILE)
-  int nchunks;               // CTAs per (b, kv head)
+  int ctas;                  // CTAs sharing the key tiles of all retrieving KV heads
   bool paged;
 };
 
@@ -67,27 +72,35 @@ struct AttnLaunch {
   float scale;
   const int32_t* idx;    // sparse: [B][Hq][cap]; dense: null
   const int32_t* n_sel;  // sparse: [B][Hq]
+  const uint8_t* unit_mask;  // sparse, nullable: attend only units u with (mask[u] != 0) == mask_want
+  int mask_want;
   int cap;
   float* out;
   float* lse;
-  float* partials;       // [units][G][splits][d + 2]
+  float* partials;       // [ctas + units][G][d + 2]
   unsigned* counters;    // [units], zero on entry, left zero
-  int splits;
+  int ctas;              // CTAs sharing the rows of all units
 };
+
+// Units of the attention split (query heads when sparse, KV heads when dense)
+// and the floats of partial records the kernel may write for `ctas` CTAs.
+int attn_units(const KVView& kv, bool sparse);
+size_t attn_partial_floats(const KVView& kv, bool sparse, int ctas);
 
 cudaError_t launch_score(const ScoreLaunch& a, const CUtensorMap* tmap, cudaStream_t s);
 cudaError_t launch_select(const SelectLaunch& a, cudaStream_t s);
+cudaError_t launch_select_global(const SelectLaunch& a, cudaStream_t s);
 cudaError_t launch_cis(const CisLaunch& a, cudaStream_t s);
 cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t s);
 
 // Hooks into the C ABI layer for the library's other entry-point files:
 // descriptor checks, per-device facts (error word, SM count), the failure
-// message of prhs_last_message, and the split-K factor of sparse attention.
+// message of prhs_last_message, and the CTA count of the attention kernels.
 prhs_status abi_check_kv(const prhs_kv* kv);
 prhs_status abi_device(unsigned** err, int* sms);
 prhs_status abi_fail(prhs_status s, const char* msg);
 KVView abi_view(const prhs_kv& kv, unsigned* err);
-int abi_sparse_splits(const prhs_kv& kv, int sms);
+int abi_attn_ctas(const prhs_kv& kv, bool sparse, int cap, int sms);
 
 // Bytes of dynamic shared memory the scoring kernel needs for this shape.
 size_t score_smem_bytes(prhs_dtype dt, int d);

@@ -67,9 +67,10 @@ extern "C" prhs_status prhs_sparse_attn_noalloc(const prhs_kv* kv, const void* q
   if ((s = scratch_address(&scratch)) != PRHS_OK) return s;
 
   const int units = kv->B * kv->Hq;
-  const int splits = abi_sparse_splits(*kv, sms);
+  const KVView view = abi_view(*kv, err);
+  const int ctas = abi_attn_ctas(*kv, true, cap, sms);
   const size_t tickets = ((size_t)units * sizeof(unsigned) + 255) / 256 * 256;
-  const size_t need = tickets + (size_t)units * splits * (kv->d + 2) * sizeof(float);
+  const size_t need = tickets + attn_partial_floats(view, true, ctas) * sizeof(float);
   if (need > (size_t)PRHS_NOALLOC_SCRATCH_BYTES) {
     std::string m = "sparse_attn_noalloc: this batch needs " + std::to_string(need) +
                     " bytes of scratch, more than the fixed " +
@@ -81,17 +82,19 @@ extern "C" prhs_status prhs_sparse_attn_noalloc(const prhs_kv* kv, const void* q
   if (e != cudaSuccess) return abi_fail(PRHS_ECUDA, cudaGetErrorString(e));
 
   AttnLaunch a;
-  a.kv = abi_view(*kv, err);
+  a.kv = view;
   a.q = q;
   a.scale = scale;
   a.idx = idx;
   a.n_sel = n_sel;
+  a.unit_mask = nullptr;
+  a.mask_want = 0;
   a.cap = cap;
   a.out = out;
   a.lse = lse;
   a.counters = static_cast<unsigned*>(scratch);
   a.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + tickets);
-  a.splits = splits;
+  a.ctas = ctas;
   e = launch_attn(a, true, stream);
   if (e != cudaSuccess) return abi_fail(PRHS_ECUDA, cudaGetErrorString(e));
   return PRHS_OK;

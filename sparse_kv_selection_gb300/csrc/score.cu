@@ -65,24 +65,74 @@ __global__ void __launch_bounds__(160) score_kernel(const __grid_constant__ CUte
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::STAGES * S::STAGE_BYTES);
   uint64_t* empty = full + S::STAGES;
+  int* tprefix = reinterpret_cast<int*>(empty + S::STAGES);  // [units + 1] tile prefix
+  __shared__ int sh_wsum[5];
+
+  pdl_wait();
+  pdl_trigger();
 
   const KVView& kv = a.kv;
-  const int unit = blockIdx.y;  // b * Hkv + kv head
-  const int b = unit / kv.Hkv, kvh = unit % kv.Hkv;
-  const int qh0 = b * kv.Hq + kvh * G;  // first query head of the group
-  if (a.head_skip != nullptr) {
-    bool need = false;
-#pragma unroll
-    for (int g = 0; g < G; g++) need |= a.head_skip[qh0 + g] == 0;
-    if (!need) return;
-  }
-  const int t = seq_len(kv, b);
-  const int k0 = blockIdx.x * a.chunk_keys;
-  if (k0 >= t) return;
-  const int k1 = min(t, k0 + a.chunk_keys);
-  const int ntiles = (k1 - k0 + S::TK - 1) / S::TK;
-
+  const int U = kv.B * kv.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nthr = blockDim.x;
+
+  // ---- key tiles of every retrieving KV head, and their prefix sums ----
+  {
+    const int per_t = (U + nthr - 1) / nthr;
+    const int u0 = threadIdx.x * per_t;
+    int loc = 0;
+    for (int k = 0; k < per_t; k++) {
+      const int u = u0 + k;
+      if (u >= U) break;
+      const int b = u / kv.Hkv, kvh = u % kv.Hkv;
+      bool need = a.head_skip == nullptr;
+      if (!need) {
+        const int qh0 = b * kv.Hq + kvh * G;
+#pragma unroll
+        for (int g = 0; g < G; g++) need |= a.head_skip[qh0 + g] == 0;
+      }
+      const int tiles = need ? (seq_len(kv, b) + S::TK - 1) / S::TK : 0;
+      tprefix[u] = tiles;
+      loc += tiles;
+    }
+    int v = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) sh_wsum[warp] = v;
+    __syncthreads();
+    int run = v - loc;
+    for (int w = 0; w < warp; w++) run += sh_wsum[w];
+    for (int k = 0; k < per_t; k++) {
+      const int u = u0 + k;
+      if (u >= U) break;
+      const int tl = tprefix[u];
+      tprefix[u] = run;
+      run += tl;
+    }
+    if (threadIdx.x == nthr - 1) tprefix[U] = run;
+    __syncthreads();
+  }
+  const int total = tprefix[U];
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  const int g0 = blockIdx.x * per;
+  const int ntiles = min(total, g0 + per) - g0;
+  if (ntiles <= 0) return;
+
+  // unit and first key of the it-th tile of this CTA
+  auto tile_at = [&](int it, int& u, int& key0) {
+    const int g = g0 + it;
+    int lo = 0, hi = U - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tprefix[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    u = lo;
+    key0 = (g - tprefix[lo]) * S::TK;
+  };
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::STAGES; s++) {
       mbar_init(&full[s], 1);
@@ -93,35 +143,45 @@ __global__ void __launch_bounds__(160) score_kernel(const __grid_constant__ CUte
   __syncthreads();
 
   if (warp == S::NW) {
-    // ---------------- producer: one lane issues the TMA boxes ----------------
-    if (lane != 0) return;
-    prefetch_tmap(&tmap);
+    // ------- producer warp: lane 0 paces the ring, lanes issue the TMA boxes -------
+    if (lane == 0) prefetch_tmap(&tmap);
     int issued = 0;
     for (int it = 0; it < ntiles; it++) {
       const int s = it % S::STAGES;
-      if (!mbar_wait(&empty[s], ((it / S::STAGES) & 1) ^ 1, kv.err)) break;
-      const int tile0 = k0 + it * S::TK;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&empty[s], ((it / S::STAGES) & 1) ^ 1, kv.err);
+      if (!__shfl_sync(FULL_MASK, ok, 0)) break;
+      int u, tile0;
+      tile_at(it, u, tile0);
+      const int b = u / kv.Hkv, kvh = u % kv.Hkv;
       uint8_t* dst = smem + s * S::STAGE_BYTES;
       if (!a.paged) {
-        mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
-        tma_load_3d(dst, &tmap, 0, 0, unit * kv.t_max + tile0, &full[s]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
+          tma_load_3d(dst, &tmap, 0, 0, u * kv.t_max + tile0, &full[s]);
+        }
       } else {
+        // one 16-row box per page slice; the page ids are read in parallel
+        const int k1 = min(seq_len(kv, b), tile0 + S::TK);
         const int nbox = min(S::TK / PAGED_BOX_ROWS, (k1 - tile0 + PAGED_BOX_ROWS - 1) / PAGED_BOX_ROWS);
-        mbar_arrive_expect_tx(&full[s], nbox * PAGED_BOX_ROWS * S::RB);
-        for (int x = 0; x < nbox; x++) {
-          long long row = kv_row(kv, b, kvh, tile0 + x * PAGED_BOX_ROWS);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], nbox * PAGED_BOX_ROWS * S::RB);
+        __syncwarp();
+        if (lane < nbox) {
+          long long row = kv_row(kv, b, kvh, tile0 + lane * PAGED_BOX_ROWS);
           if (row < 0) {
             raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
             row = 0;
           }
-          tma_load_3d(dst + x * PAGED_BOX_ROWS * S::RB, &tmap, 0, 0, (int)row, &full[s]);
+          tma_load_3d(dst + lane * PAGED_BOX_ROWS * S::RB, &tmap, 0, 0, (int)row, &full[s]);
         }
       }
+      __syncwarp();
       issued = it + 1;
     }
     // never leave while a copy into this CTA's shared memory is in flight
-    for (int it = max(0, issued - S::STAGES); it < issued; it++)
-      mbar_wait(&full[it % S::STAGES], (it / S::STAGES) & 1, kv.err);
+    if (lane == 0)
+      for (int it = max(0, issued - S::STAGES); it < issued; it++)
+        mbar_wait(&full[it % S::STAGES], (it / S::STAGES) & 1, kv.err);
     return;
   }
 
@@ -129,17 +189,27 @@ __global__ void __launch_bounds__(160) score_kernel(const __grid_constant__ CUte
   const int r = lane >> 3;  // key slot 0..3 (8 keys each)
   const int j = lane & 7;   // 16-byte chunk within each 128-byte segment
   float qf[G][S::EL];
-#pragma unroll
-  for (int g = 0; g < G; g++) {
-    const long long qbase = (long long)(qh0 + g) * D;
-#pragma unroll
-    for (int h = 0; h < S::NH; h++)
-#pragma unroll
-      for (int e = 0; e < S::EPC; e++)
-        qf[g][h * S::EPC + e] = Elem<T>::load1(a.q, qbase + h * (128 / (int)sizeof(T)) + j * S::EPC + e);
-  }
+  int cur_u = -1, qh0 = 0, k1 = 0;
 
   for (int it = 0; it < ntiles; it++) {
+    int u, tile0;
+    tile_at(it, u, tile0);
+    if (u != cur_u) {
+      cur_u = u;
+      const int b = u / kv.Hkv, kvh = u % kv.Hkv;
+      qh0 = b * kv.Hq + kvh * G;
+      k1 = seq_len(kv, b);
+#pragma unroll
+      for (int g = 0; g < G; g++) {
+        const long long qbase = (long long)(qh0 + g) * D;
+#pragma unroll
+        for (int h = 0; h < S::NH; h++)
+#pragma unroll
+          for (int e = 0; e < S::EPC; e++)
+            qf[g][h * S::EPC + e] =
+                Elem<T>::load1(a.q, qbase + h * (128 / (int)sizeof(T)) + j * S::EPC + e);
+      }
+    }
     const int s = it % S::STAGES;
     if (!mbar_wait(&full[s], (it / S::STAGES) & 1, kv.err)) break;
     const uint8_t* stage = smem + s * S::STAGE_BYTES;
@@ -165,7 +235,7 @@ __global__ void __launch_bounds__(160) score_kernel(const __grid_constant__ CUte
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    const int key = k0 + it * S::TK + warp * 32 + lane;
+    const int key = tile0 + warp * 32 + lane;
 #pragma unroll
     for (int g = 0; g < G; g++) {
       const float sc = transpose_reduce8(acc[g], j) * a.scale;
@@ -178,7 +248,6 @@ template <typename T, int D>
 static cudaError_t score_dispatch_g(const ScoreLaunch& a, const CUtensorMap* tmap, int G,
                                    cudaStream_t st) {
   using S = ScoreShape<T, D>;
-  dim3 grid(a.nchunks, a.kv.B * a.kv.Hkv);
   void (*k)(const CUtensorMap, const ScoreLaunch) = nullptr;
   switch (G) {
     case 1: k = score_kernel<T, D, 1>; break;
@@ -187,10 +256,10 @@ static cudaError_t score_dispatch_g(const ScoreLaunch& a, const CUtensorMap* tma
     case 8: k = score_kernel<T, D, 8>; break;
     default: return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
+  const size_t smem = S::SMEM + ((size_t)a.kv.B * a.kv.Hkv + 1) * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, 32 * (S::NW + 1), S::SMEM, st>>>(*tmap, a);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(a.ctas), dim3(32 * (S::NW + 1)), smem, st, *tmap, a);
 }
 
 size_t score_smem_bytes(prhs_dtype dt, int d) {
@@ -207,6 +276,7 @@ struct SelShared {
   float red_m[32];
   float red_z[32];
   unsigned digit, krem;
+  float M, Z;
 };
 
 // Block-wide inclusive scan of one unsigned per thread (1024 threads).
@@ -254,6 +324,8 @@ template <typename T>
 __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectLaunch a) {
   extern __shared__ float cache[];
   __shared__ SelShared sh;
+  pdl_wait();
+  pdl_trigger();
   const KVView& kv = a.kv;
   const int qh = blockIdx.x;  // b * Hq + query head
   const int b = qh / kv.Hq;
@@ -311,12 +383,7 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectLaun
         z += expf(s - m);
       }
     }
-    const unsigned dg = order_key(s) >> 21;
-    const unsigned act = __ballot_sync(FULL_MASK, in);
-    if (in) {
-      const unsigned peers = __match_any_sync(act, dg);
-      if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[dg], __popc(peers));
-    }
+    if (in) atomicAdd(&sh.hist[order_key(s) >> 21], 1u);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -330,8 +397,20 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectLaun
   }
   if (tid == 0) sh.krem = (unsigned)Nb;
   __syncthreads();
-  float M = sh.red_m[0], Z = sh.red_z[0];
-  for (int w = 1; w < (nthreads >> 5); w++) combine_mz(M, Z, sh.red_m[w], sh.red_z[w]);
+  if (warp == 0) {  // one warp merges the per-warp softmax statistics
+    float m2 = lane < (nthreads >> 5) ? sh.red_m[lane] : -INFINITY;
+    float z2 = lane < (nthreads >> 5) ? sh.red_z[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m3 = __shfl_xor_sync(FULL_MASK, m2, o);
+      const float z3 = __shfl_xor_sync(FULL_MASK, z2, o);
+      combine_mz(m2, z2, m3, z3);
+    }
+    if (lane == 0) {
+      sh.M = m2;
+      sh.Z = z2;
+    }
+  }
 
   // ---- radix select: digits of 11, 11 and 10 bits from the top ----
   unsigned prefix = 0, mask = 0;
@@ -348,12 +427,7 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectLaun
         bool in = i < t;
         const unsigned u = in ? order_key(sp[i]) : 0u;
         in = in && (u & mask) == prefix;
-        const unsigned dg = (u >> sh_) & (nb - 1);
-        const unsigned act = __ballot_sync(FULL_MASK, in);
-        if (in) {
-          const unsigned peers = __match_any_sync(act, dg);
-          if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[dg], __popc(peers));
-        }
+        if (in) atomicAdd(&sh.hist[(u >> sh_) & (nb - 1)], 1u);
       }
       __syncthreads();
     }
@@ -382,6 +456,7 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectLaun
   }
   const unsigned thr = prefix;        // key of the N-th largest logit
   const unsigned keq = sh.krem;       // how many logits equal to it are kept
+  const float M = sh.M, Z = sh.Z;     // written before the radix passes' barriers
   __syncthreads();
 
   // ---- compaction in index order; dropped mass of the rest ----
@@ -463,14 +538,13 @@ cudaError_t launch_score(const ScoreLaunch& a, const CUtensorMap* tmap, cudaStre
   return cudaErrorNotSupported;
 }
 
-cudaError_t launch_select(const SelectLaunch& a, cudaStream_t st) {
+cudaError_t launch_select_global(const SelectLaunch& a, cudaStream_t st) {
   const size_t smem = (size_t)min(a.kv.t_max, SELECT_CACHE_FLOATS) * sizeof(float);
   void (*k)(const SelectLaunch) = a.kv.dtype == PRHS_BF16 ? select_kernel<__nv_bfloat16>
                                                           : select_kernel<float>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k<<<a.kv.B * a.kv.Hq, SELECT_THREADS, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(a.kv.B * a.kv.Hq), dim3(SELECT_THREADS), smem, st, a);
 }
 
 }  // namespace prhs

@@ -1,0 +1,504 @@
+// Top-N selection and dropped mass from the logits of prhs_score, one
+// thread-block cluster per query head.
+// "Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference":
+// abstract (top-k oracle selection; the dropped mass delta) and Table I
+// (S_t, N, tau(.), delta(.)).
+//
+// The CL CTAs of a cluster each hold a contiguous slice of the head's logits
+// in shared memory (one read of the logits from L2/HBM). Softmax statistics
+// and three radix histograms (11, 11, 10 bits of an order-preserving key) are
+// built per CTA and summed across the cluster through distributed shared
+// memory; every CTA then takes the same digit decision. The index-ordered
+// compaction gets each CTA's output offset from the counts of the lower
+// ranks, so the set comes out ascending with ties resolved to the lowest
+// index, and the dropped mass is the cluster sum of the unselected weights.
+#include <cooperative_groups.h>
+
+#include "kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace prhs {
+
+constexpr int SEL_THREADS = 512;
+constexpr int SEL_WARPS = SEL_THREADS / 32;
+
+constexpr int SEL_CANDS = 256;  // candidates ranked exactly after the two bin passes
+
+struct SelClusterShared {
+  unsigned hist[2048];        // this CTA's histogram of the current bin pass
+  unsigned histg[2][2048];    // rank 0: cluster totals of the two value-bin passes
+  unsigned fb[2][2048];       // fallback radix passes: this CTA's histograms
+  unsigned cand[SEL_CANDS];   // rank 0: gathered candidate keys; every rank: a copy
+  unsigned lcand[SEL_CANDS];  // this CTA's own candidate keys
+  unsigned ncand, nlcand;
+  unsigned scan[32];
+  float red[SEL_WARPS];
+  float lmin, lmax;           // this CTA's logit range
+  float Zp;                   // this CTA's sum of exp(s - max)
+  unsigned cnt_gt, cnt_eq;    // this CTA's logits above / equal to the threshold
+  float dsum;                 // this CTA's dropped weight
+  unsigned digit, krem, cnt_bin, thr, keq;
+};
+
+__device__ __forceinline__ void merge_mz(float& m, float& z, float m2, float z2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  z = (m == -INFINITY ? 0.f : z * expf(m - M)) + (m2 == -INFINITY ? 0.f : z2 * expf(m2 - M));
+  m = M;
+}
+
+// Block-wide inclusive scan of one unsigned per thread.
+__device__ __forceinline__ unsigned scan_block(unsigned v, unsigned* warp_tot, unsigned& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned n = __shfl_up_sync(FULL_MASK, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned w = lane < nw ? warp_tot[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned n = __shfl_up_sync(FULL_MASK, w, o);
+      if (lane >= o) w += n;
+    }
+    warp_tot[lane] = w;
+  }
+  __syncthreads();
+  total = warp_tot[nw - 1];
+  const unsigned add = warp > 0 ? warp_tot[warp - 1] : 0u;
+  __syncthreads();
+  return v + add;
+}
+
+template <typename T>
+__device__ __forceinline__ void mirror_query(const SelectLaunch& a, int qh) {
+  for (int i = threadIdx.x; i < a.kv.d; i += blockDim.x)
+    copy_elem<T>(a.q_anchor, a.q, (long long)qh * a.kv.d + i);
+}
+
+// Bin of a histogram (nb bins, highest first) holding the krem-th largest
+// element; `h` may live in another CTA's shared memory. Sets sh.digit, the
+// rank sh.krem inside that bin and its count sh.cnt_bin.
+__device__ __forceinline__ void find_bin(const unsigned* h, int nb, unsigned krem,
+                                         SelClusterShared& sh) {
+  const int per = nb / SEL_THREADS;  // 4 or 2
+  const int top = nb - 1 - per * threadIdx.x;
+  unsigned c[4] = {0u, 0u, 0u, 0u};
+  unsigned sum = 0;
+  for (int k = 0; k < per; k++) {
+    c[k] = h[top - k];
+    sum += c[k];
+  }
+  unsigned total;
+  unsigned run = scan_block(sum, sh.scan, total) - sum;
+  for (int k = 0; k < per; k++) {
+    if (run < krem && run + c[k] >= krem) {
+      sh.digit = (unsigned)(top - k);
+      sh.krem = krem - run;
+      sh.cnt_bin = c[k];
+    }
+    run += c[k];
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ float float_of_key(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Value bins: monotone non-decreasing in s, clamped to [0, 2047].
+__device__ __forceinline__ int vbin(float s, float lo, float inv) {
+  const float x = (s - lo) * inv;
+  return x <= 0.f ? 0 : (x >= 2047.f ? 2047 : (int)x);
+}
+
+// Barrier over the head's CTAs: the cluster when the head is split, the block
+// otherwise (a one-CTA cluster barrier would add a cluster-scope fence).
+template <bool ONE>
+__device__ __forceinline__ void head_sync(cg::cluster_group& cluster) {
+  if (ONE) __syncthreads(); else cluster.sync();
+}
+
+template <bool ONE>
+__device__ __forceinline__ SelClusterShared* rank_shared(cg::cluster_group& cluster,
+                                                         SelClusterShared& sh, int r) {
+  if (ONE) return &sh;
+  return cluster.map_shared_rank(&sh, r);
+}
+
+template <typename T, bool ONE>
+__global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const SelectLaunch a, int chunk) {
+  extern __shared__ float cache[];
+  __shared__ SelClusterShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = ONE ? 1 : (int)cluster.num_blocks();
+  const int rank = ONE ? 0 : (int)cluster.block_rank();
+  pdl_wait();
+  pdl_trigger();
+
+  const KVView& kv = a.kv;
+  const int qh = blockIdx.x / CL;  // the cluster's query head (b * Hq + h)
+  const int b = qh / kv.Hq;
+  if (a.head_skip != nullptr && a.head_skip[qh] != 0) return;  // uniform over the cluster
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = seq_len(kv, b);
+  int Nb = a.n_budget != nullptr ? a.n_budget[b] : a.N;
+  if (Nb < 0) Nb = 0;
+  const int lim = a.anchor_idx != nullptr ? min(a.cap, a.anchor_cap) : a.cap;
+  if (min(Nb, t) > lim) {
+    if (tid == 0 && rank == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
+    Nb = lim;
+  }
+  int32_t* out = a.idx + (long long)qh * a.cap;
+  int32_t* aout = a.anchor_idx != nullptr ? a.anchor_idx + (long long)qh * a.anchor_cap : nullptr;
+  const int lo = min(t, rank * chunk), hi = min(t, lo + chunk), cnt = hi - lo;
+
+  if (Nb >= t || Nb == 0) {  // keep everything (delta = 0) or nothing (delta = 1)
+    const int n = Nb >= t ? t : 0;
+    for (int i = lo + tid; i < min(hi, n); i += SEL_THREADS) {
+      out[i] = i;
+      if (aout) aout[i] = i;
+    }
+    if (rank == 0) {
+      if (tid == 0) {
+        a.n_sel[qh] = n;
+        a.delta[qh] = n == t ? 0.f : 1.f;
+        if (a.anchor_n) a.anchor_n[qh] = n;
+      }
+      if (a.q_anchor) mirror_query<T>(a, qh);
+    }
+    return;
+  }
+
+  // ---- load this CTA's slice; its logit range ----
+  const float* src = a.scores + (long long)qh * kv.t_max + lo;
+  float vmin = INFINITY, vmax = -INFINITY;
+  for (int i = tid; i < cnt; i += SEL_THREADS) {
+    const float s = src[i];
+    cache[i] = s;
+    vmin = fminf(vmin, s);
+    vmax = fmaxf(vmax, s);
+  }
+  for (int i = tid; i < 2048; i += SEL_THREADS) sh.hist[i] = 0;
+  if (rank == 0)
+    for (int i = tid; i < 2 * 2048; i += SEL_THREADS) (&sh.histg[0][0])[i] = 0;
+  if (tid == 0) {
+    sh.ncand = 0;
+    sh.nlcand = 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    vmin = fminf(vmin, __shfl_xor_sync(FULL_MASK, vmin, o));
+    vmax = fmaxf(vmax, __shfl_xor_sync(FULL_MASK, vmax, o));
+  }
+  if (lane == 0) {
+    sh.red[warp] = vmin;
+    sh.scan[warp] = __float_as_uint(vmax);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float mn = INFINITY, mx = -INFINITY;
+    for (int w = 0; w < SEL_WARPS; w++) {
+      mn = fminf(mn, sh.red[w]);
+      mx = fmaxf(mx, __uint_as_float(sh.scan[w]));
+    }
+    sh.lmin = mn;
+    sh.lmax = mx;
+  }
+  __syncthreads();
+  head_sync<ONE>(cluster);  // ranges published; rank 0's accumulators are zero
+  float smin = INFINITY, smax = -INFINITY;
+  for (int r = 0; r < CL; r++) {
+    const SelClusterShared* rs = rank_shared<ONE>(cluster, sh, r);
+    smin = fminf(smin, rs->lmin);
+    smax = fmaxf(smax, rs->lmax);
+  }
+  SelClusterShared* root = rank_shared<ONE>(cluster, sh, 0);
+  const bool flat = !(smax > smin);
+  const float w1 = (smax - smin) * (1.f / 2048.f);
+  const float inv1 = flat ? 0.f : 2048.f / (smax - smin);
+
+  // ---- pass 1: softmax partial sum and value histogram over [smin, smax] ----
+  float z = 0.f;
+  for (int i = tid; i < cnt; i += SEL_THREADS) {
+    const float s = cache[i];
+    z += expf(s - smax);
+    if (!flat) atomicAdd(&sh.hist[vbin(s, smin, inv1)], 1u);
+  }
+  z = warp_sum(z);
+  if (lane == 0) sh.red[warp] = z;
+  __syncthreads();
+  if (tid == 0) {
+    float zz = 0.f;
+    for (int w = 0; w < SEL_WARPS; w++) zz += sh.red[w];
+    sh.Zp = zz;
+  }
+  if (!flat)
+    for (int i = tid; i < 2048; i += SEL_THREADS)
+      if (sh.hist[i]) atomicAdd(&root->histg[0][i], sh.hist[i]);
+  __syncthreads();
+  head_sync<ONE>(cluster);
+  float Z = 0.f;
+  for (int r = 0; r < CL; r++) Z += rank_shared<ONE>(cluster, sh, r)->Zp;
+
+  // ---- threshold: the key of the N-th largest logit, and how many ties to keep ----
+  unsigned thr = 0, keq = 0, cta_gt = 0, cta_eq = 0;
+  bool fallback = false;
+  if (flat) {  // every logit of the head is equal: the lowest indices win
+    thr = order_key(smax);
+    keq = (unsigned)Nb;
+    cta_eq = (unsigned)cnt;
+  } else {
+    find_bin(root->histg[0], 2048, (unsigned)Nb, sh);
+    const int b1 = (int)sh.digit;
+    const unsigned krem1 = sh.krem;
+    const float lo1 = smin + (float)b1 * w1;
+    const float inv2 = w1 > 0.f ? 2048.f / w1 : 0.f;
+    // pass 2: second value histogram inside bin b1
+    for (int i = tid; i < 2048; i += SEL_THREADS) sh.hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < cnt; i += SEL_THREADS) {
+      const float s = cache[i];
+      if (vbin(s, smin, inv1) == b1) atomicAdd(&sh.hist[vbin(s, lo1, inv2)], 1u);
+    }
+    __syncthreads();
+    for (int i = tid; i < 2048; i += SEL_THREADS)
+      if (sh.hist[i]) atomicAdd(&root->histg[1][i], sh.hist[i]);
+    __syncthreads();
+    head_sync<ONE>(cluster);
+    find_bin(root->histg[1], 2048, krem1, sh);
+    const int b2 = (int)sh.digit;
+    const unsigned krem2 = sh.krem;
+    if (sh.cnt_bin <= SEL_CANDS) {
+      // pass 3: gather the candidates of bin (b1, b2); count the logits above them
+      unsigned dgt = 0;
+      for (int i = tid; i < cnt; i += SEL_THREADS) {
+        const float s = cache[i];
+        const int c1 = vbin(s, smin, inv1);
+        if (c1 > b1) {
+          dgt++;
+        } else if (c1 == b1) {
+          const int c2 = vbin(s, lo1, inv2);
+          if (c2 > b2) {
+            dgt++;
+          } else if (c2 == b2) {
+            const unsigned u = order_key(s);
+            const unsigned slot = atomicAdd(&root->ncand, 1u);
+            if (slot < SEL_CANDS) root->cand[slot] = u;
+            const unsigned ls = atomicAdd(&sh.nlcand, 1u);
+            if (ls < SEL_CANDS) sh.lcand[ls] = u;
+          }
+        }
+      }
+      unsigned dgt_cta;
+      scan_block(dgt, sh.scan, dgt_cta);
+      head_sync<ONE>(cluster);
+      const unsigned nc = min(root->ncand, (unsigned)SEL_CANDS);
+      unsigned myc = 0;
+      if (tid < (int)nc) myc = root->cand[tid];
+      __syncthreads();
+      if (tid < (int)nc) sh.cand[tid] = myc;
+      __syncthreads();
+      if (tid < (int)nc) {  // exact rank of each candidate among all candidates
+        unsigned g = 0, e = 0;
+        for (unsigned jj = 0; jj < nc; jj++) {
+          g += sh.cand[jj] > myc;
+          e += sh.cand[jj] == myc;
+        }
+        if (g < krem2 && g + e >= krem2) {
+          sh.thr = myc;
+          sh.keq = krem2 - g;
+        }
+      }
+      __syncthreads();
+      thr = sh.thr;
+      keq = sh.keq;
+      const unsigned nl = min(sh.nlcand, (unsigned)SEL_CANDS);
+      cta_gt = dgt_cta;
+      for (unsigned jj = 0; jj < nl; jj++) {
+        cta_gt += sh.lcand[jj] > thr;
+        cta_eq += sh.lcand[jj] == thr;
+      }
+    } else {
+      fallback = true;  // heavy ties or a very dense spot: exact radix over all logits
+    }
+  }
+  if (fallback) {
+    unsigned prefix = 0, mask = 0, krem = (unsigned)Nb;
+    for (int pass = 0; pass < 3; pass++) {
+      const int buf = pass & 1;
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const int nb = pass == 2 ? 1024 : 2048;
+      for (int i = tid; i < nb; i += SEL_THREADS) sh.fb[buf][i] = 0;
+      __syncthreads();
+      for (int i = tid; i < cnt; i += SEL_THREADS) {
+        const unsigned u = order_key(cache[i]);
+        if ((u & mask) == prefix) atomicAdd(&sh.fb[buf][(u >> shift) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      head_sync<ONE>(cluster);
+      for (int i = tid; i < nb; i += SEL_THREADS) {
+        unsigned tot = 0;
+        for (int r = 0; r < CL; r++) tot += rank_shared<ONE>(cluster, sh, r)->fb[buf][i];
+        sh.hist[i] = tot;
+      }
+      __syncthreads();
+      find_bin(sh.hist, nb, krem, sh);
+      prefix |= sh.digit << shift;
+      mask |= (unsigned)(nb - 1) << shift;
+      krem = sh.krem;
+    }
+    thr = prefix;
+    keq = krem;
+    unsigned lgt = 0, leq = 0;
+    for (int i = tid; i < cnt; i += SEL_THREADS) {
+      const unsigned u = order_key(cache[i]);
+      lgt += u > thr;
+      leq += u == thr;
+    }
+    scan_block(lgt, sh.scan, cta_gt);
+    scan_block(leq, sh.scan, cta_eq);
+  }
+  if (tid == 0) {
+    sh.cnt_gt = cta_gt;
+    sh.cnt_eq = cta_eq;
+  }
+  __syncthreads();
+  head_sync<ONE>(cluster);
+  unsigned carry_gt = 0, carry_eq = 0;
+  for (int r = 0; r < rank; r++) {
+    const SelClusterShared* rs = rank_shared<ONE>(cluster, sh, r);
+    carry_gt += rs->cnt_gt;
+    carry_eq += rs->cnt_eq;
+  }
+
+  // ---- index-ordered compaction; dropped weight of the rest ----
+  constexpr int E = 4;
+  constexpr int TILE = SEL_THREADS * E;
+  float dsum = 0.f;
+  for (int base = 0; base < cnt; base += TILE) {
+    unsigned u[E];
+    float sv[E];
+    unsigned cgt = 0, ceq = 0;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+      const int i = base + tid * E + e;
+      sv[e] = i < cnt ? cache[i] : -INFINITY;
+      u[e] = i < cnt ? order_key(sv[e]) : 0u;
+      cgt += u[e] > thr;
+      ceq += (i < cnt) && u[e] == thr;
+    }
+    unsigned tot;
+    const unsigned packed = (cgt << 16) | ceq;
+    const unsigned excl = scan_block(packed, sh.scan, tot) - packed;
+    unsigned gt_before = carry_gt + (excl >> 16);
+    unsigned eq_before = carry_eq + (excl & 0xffffu);
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+      const int i = base + tid * E + e;
+      if (i >= cnt) break;
+      bool take = false;
+      int pos = 0;
+      if (u[e] > thr) {
+        take = true;
+        pos = (int)(gt_before + min(eq_before, keq));
+        gt_before++;
+      } else if (u[e] == thr) {
+        if (eq_before < keq) {
+          take = true;
+          pos = (int)(gt_before + eq_before);
+        }
+        eq_before++;
+      }
+      if (take) {
+        if (pos < Nb) {
+          out[pos] = lo + i;
+          if (aout) aout[pos] = lo + i;
+        } else {
+          raise_error(kv.err, PRHS_DEV_CAPACITY);
+        }
+      } else {
+        dsum += expf(sv[e] - smax);
+      }
+    }
+    carry_gt += tot >> 16;
+    carry_eq += tot & 0xffffu;
+  }
+  dsum = warp_sum(dsum);
+  if (lane == 0) sh.red[warp] = dsum;
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.f;
+    for (int w = 0; w < SEL_WARPS; w++) s += sh.red[w];
+    sh.dsum = s;
+  }
+  __syncthreads();
+  head_sync<ONE>(cluster);
+  if (rank == 0) {
+    if (tid == 0) {
+      float s = 0.f;
+      for (int r = 0; r < CL; r++) s += rank_shared<ONE>(cluster, sh, r)->dsum;
+      a.n_sel[qh] = Nb;
+      a.delta[qh] = s / Z;
+      if (a.anchor_n) a.anchor_n[qh] = Nb;
+    }
+    if (a.q_anchor) mirror_query<T>(a, qh);
+  }
+  head_sync<ONE>(cluster);  // shared memory stays valid until every remote read is done
+}
+
+// Cluster size and slice length: one CTA holds up to SELECT_SLICE_ONE logits;
+// longer caches spread a head over 2..8 CTAs. (Splitting shorter caches to
+// fill the GPU costs more in cluster barriers than it saves.)
+static void select_geometry(const KVView& kv, int sms, int* cl, int* chunk) {
+  const int tmax = kv.t_max;
+  int c = 1;
+  if (tmax > SELECT_SLICE_ONE) {
+    c = 2;
+    while (c < 8 && (tmax + c - 1) / c > SELECT_SLICE_MAX) c *= 2;
+  }
+  (void)sms;
+  *cl = c;
+  *chunk = ((tmax + c - 1) / c + 3) / 4 * 4;
+}
+
+cudaError_t launch_select(const SelectLaunch& a, cudaStream_t st) {
+  int sms = 0, dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  int cl = 1, chunk = 0;
+  select_geometry(a.kv, sms, &cl, &chunk);
+  if (chunk > (cl == 1 ? SELECT_SLICE_ONE : SELECT_SLICE_MAX)) return launch_select_global(a, st);
+  void (*k)(const SelectLaunch, int);
+  if (a.kv.dtype == PRHS_BF16)
+    k = cl == 1 ? select_cluster_kernel<__nv_bfloat16, true> : select_cluster_kernel<__nv_bfloat16, false>;
+  else
+    k = cl == 1 ? select_cluster_kernel<float, true> : select_cluster_kernel<float, false>;
+  const size_t smem = (size_t)chunk * sizeof(float);
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.kv.B * a.kv.Hq * cl);
+  cfg.blockDim = dim3(SEL_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = cl == 1 ? attr + 1 : attr;  // no cluster attribute for a single CTA
+  cfg.numAttrs = cl == 1 ? 1 : 2;
+  return cudaLaunchKernelEx(&cfg, k, a, chunk);
+}
+
+}  // namespace prhs

@@ -197,15 +197,20 @@ def test_score_select(name):
     print(f"{name}: near-tie positions left uncompared: {ties}")
 
 
-def test_score_select_exact_ties_lowest_index():
+@pytest.mark.parametrize("t,dup_end,Ns", [
+    (700, 400, (1, 2, 150, 301, 302, 650)),
+    # 8192 keys: the logits are split over a cluster of CTAs, ties cross slices
+    (8192, 6000, (1, 500, 3000, 5901, 5902, 7000)),
+])
+def test_score_select_exact_ties_lowest_index(t, dup_end, Ns):
     """Duplicated key rows give bit-identical logits: the lowest indices win."""
     import sparse_kv_selection_gb300 as S
-    t, d = 700, 128
+    d = 128
     rng = np.random.default_rng(3)
     K = rng.normal(size=(t, d)).astype(np.float32)
-    K[100:400] = K[50]          # 301 identical rows (index 50 and 100..399)
+    K[100:dup_end] = K[50]      # identical rows: index 50 and 100..dup_end-1
     q = (K[50] * 0.5 + rng.normal(size=d) * 0.1).astype(np.float32)
-    for N in (1, 2, 150, 301, 302, 650):
+    for N in Ns:
         kt = torch.from_numpy(K).reshape(1, 1, t, d).cuda()
         kv = S.KVCache(kt, kt, torch.tensor([t], dtype=torch.int32).cuda(), 1)
         idx = torch.empty(1, 1, N, dtype=torch.int32, device="cuda")
@@ -246,9 +251,10 @@ def test_score_select_head_skip_and_full_budget():
             assert gn[b, h] == t and gd[b, h] == 0.0 and (gi[b, h] == np.arange(t)).all()
 
 
-@pytest.mark.parametrize("t,N", [(70001, 1500), (49153, 3)])
+@pytest.mark.parametrize("t,N", [(70001, 1500), (49153, 3), (200003, 777)])
 def test_score_select_long_cache(t, N):
-    """Caches too long for the shared-memory copy of the logits."""
+    """Long caches: logits split over a cluster of CTAs, and (200003 keys,
+    beyond eight shared-memory slices) streamed by one CTA from L2."""
     import sparse_kv_selection_gb300 as S
     from workloads.torch_io import upload
     wl = make_workload("long", dtype="bf16", B=1, Hq=2, Hkv=1, d=128, t=t, n_clusters=40,

@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--kernels", action="store_true",
                    help="time each kernel alone on the workload (all heads retrieving) instead")
+    p.add_argument("--only", default=None,
+                   help="with --kernels: time just this case (e.g. sparse_attn_dilated)")
     return p.parse_args()
 
 
@@ -241,7 +243,7 @@ def run_ours(args):
     anchor_idx = torch.zeros(B, Hq, acap, **i32)
     anchor_n = torch.zeros(B, Hq, **i32)
     q_anchor = torch.zeros_like(dev["q"][0])
-    idx = torch.zeros(B, Hq, cap, **i32)
+    idx = torch.zeros(Sq, B, Hq, cap, **i32)  # each query's sets, kept for the per-kernel replays
     n_sel = torch.zeros(Sq, B, Hq, **i32)
     reuse = torch.zeros(Sq, B, Hq, device="cuda", dtype=torch.uint8)
     delta = torch.full((Sq, B, Hq), float("nan"), device="cuda")
@@ -251,33 +253,13 @@ def run_ours(args):
     q = dev["q"]
     scale = wl.scale
 
-    def enqueue(ev=None):
+    def enqueue():
         anchor_n.zero_()
-        for s in range(Sq):
-            kv = kvs[s % R]
-            if ev is None:  # the product path: one prhs_decode_step per query
-                S.decode_step(kv, q[s], scale, N, wl.w, wl.tau, anchor_idx, anchor_n, q_anchor,
-                              idx, n_sel[s], reuse[s], delta[s], out[s], lse[s], ws, n_budget=nb)
-                continue
-            if ev is not None:
-                ev[s][0].record()
-            S.cis_dilate(kv, anchor_idx, anchor_n, q[s], q_anchor, wl.w, wl.tau, idx, n_sel[s],
-                         reuse[s])
-            if ev is not None:
-                ev[s][1].record()
-            S.binding.score(kv, q[s], scale, ws, head_skip=reuse[s])
-            if ev is not None:
-                ev[s][2].record()
-            S.binding.select(kv, q[s], N, idx, n_sel[s], delta[s], ws, n_budget=nb,
-                             head_skip=reuse[s], anchor_idx=anchor_idx, anchor_n=anchor_n,
-                             q_anchor=q_anchor)
-            if ev is not None:
-                ev[s][3].record()
-            S.sparse_attn(kv, q[s], scale, idx, n_sel[s], out[s], lse[s], ws)
-            if ev is not None:
-                ev[s][4].record()
+        for s in range(Sq):  # one prhs_decode_step per decode query
+            S.decode_step(kvs[s % R], q[s], scale, N, wl.w, wl.tau, anchor_idx, anchor_n, q_anchor,
+                          idx[s], n_sel[s], reuse[s], delta[s], out[s], lse[s], ws, n_budget=nb)
 
-    launches_per_step = 5 * Sq   # cis, score, select, and two sparse-attention branches
+    launches_per_step = 5 * Sq   # cis, score, select and the two sparse-attention branches
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -287,16 +269,6 @@ def run_ours(args):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         enqueue()
-
-    # instrumented copy: timing events between the kernels of every query
-    try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-               for _ in range(Sq)]
-        graph_i = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_i, stream=stream):
-            enqueue(evs)
-    except TypeError:
-        graph_i = None
 
     def barrier():
         if world > 1:
@@ -324,15 +296,62 @@ def run_ours(args):
     value = units / (elapsed_ms / 1e3)
 
     # ---------------- per-kernel durations over the same steps ----------------
+    # Each kernel's launches of one timed step, replayed back to back from a
+    # graph of their own, on the per-step inputs the timed run produced
+    # (reuse flags, index sets). Selection is timed as (score + select) minus
+    # score, since it consumes the logits of the score launch before it; the
+    # gate/dilation kernel runs on the anchors left by the last query.
     names = ["cis", "score", "select", "sparse_attn"]
-    ktime = {n: 0.0 for n in names}
-    if graph_i is not None:
-        for _ in range(args.steps):
-            graph_i.replay()
-            torch.cuda.synchronize()
-            for s in range(Sq):
-                for i, n in enumerate(names):
-                    ktime[n] += evs[s][i].elapsed_time(evs[s][i + 1])
+    cis_idx = torch.zeros(B, Hq, cap, **i32)
+    cis_n = torch.zeros(B, Hq, **i32)
+    cis_r = torch.zeros(B, Hq, device="cuda", dtype=torch.uint8)
+    sel_i = torch.zeros(B, Hq, acap, **i32)
+    sel_n = torch.zeros(B, Hq, **i32)
+    sel_d = torch.zeros(B, Hq, device="cuda")
+    o_tmp = torch.zeros(B, Hq, d, device="cuda")
+    l_tmp = torch.zeros(B, Hq, device="cuda")
+
+    def k_cis():
+        for s in range(Sq):
+            S.cis_dilate(kvs[s % R], anchor_idx, anchor_n, q[s], q_anchor, wl.w, wl.tau, cis_idx,
+                         cis_n, cis_r)
+
+    def k_score(with_select):
+        for s in range(Sq):
+            S.binding.score(kvs[s % R], q[s], scale, ws, head_skip=reuse[s])
+            if with_select:
+                S.binding.select(kvs[s % R], q[s], N, sel_i, sel_n, sel_d, ws, n_budget=nb,
+                                 head_skip=reuse[s])
+
+    def k_attn():
+        for s in range(Sq):
+            S.sparse_attn(kvs[s % R], q[s], scale, idx[s], n_sel[s], o_tmp, l_tmp, ws)
+
+    def time_graph(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(args.steps):
+                g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    t_cis = time_graph(k_cis)
+    t_score = time_graph(lambda: k_score(False))
+    t_ss = time_graph(lambda: k_score(True))
+    t_attn = time_graph(k_attn)
+    assert S.last_error() == 0
+    ktime = {"cis": t_cis, "score": t_score, "select": max(0.0, t_ss - t_score),
+             "sparse_attn": t_attn}
     launches = {n: Sq * args.steps for n in names}
 
     # algorithmic bytes per launch, from the flags and set sizes the run produced
@@ -499,6 +518,8 @@ def run_kernels(args):
     reps = max(4, 32 // R) * R
     res = {}
     for name, (fn, nbytes) in cases.items():
+        if args.only is not None and name != args.only:
+            continue
         if name == "select":
             with torch.cuda.stream(stream):
                 S.binding.score(kvs[0], q, wl.scale, ws)
@@ -525,10 +546,16 @@ def run_kernels(args):
         res[name] = {"us_per_launch": us, "alg_bytes": nbytes, "achieved_gbs": gbs,
                      "frac_of_measured": gbs / peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
     assert S.last_error() == 0
-    res["sparse_over_dense_time"] = (res["sparse_attn_dilated"]["us_per_launch"] /
-                                     res["dense_attn"]["us_per_launch"])
-    res["sparse_over_dense_bytes"] = (res["sparse_attn_dilated"]["alg_bytes"] /
-                                      res["dense_attn"]["alg_bytes"])
+    if "sparse_attn_dilated" in res and "dense_attn" in res:
+        res["sparse_over_dense_time"] = (res["sparse_attn_dilated"]["us_per_launch"] /
+                                         res["dense_attn"]["us_per_launch"])
+        res["sparse_over_dense_bytes"] = (res["sparse_attn_dilated"]["alg_bytes"] /
+                                          res["dense_attn"]["alg_bytes"])
+    if "sparse_attn_topN" in res and "dense_attn" in res:
+        res["topN_over_dense_time"] = (res["sparse_attn_topN"]["us_per_launch"] /
+                                       res["dense_attn"]["us_per_launch"])
+        res["topN_over_dense_bytes"] = (res["sparse_attn_topN"]["alg_bytes"] /
+                                        res["dense_attn"]["alg_bytes"])
     print(json.dumps({"mode": "kernels", "config": workload_label(wl), "peak_gbs": peak,
                       "peak_kind": peak_kind, "kv_copies": R, "launches_per_replay": reps,
                       "results": res}), flush=True)

@@ -183,7 +183,8 @@ Layout layout_of(const prhs_kv& kv, int sms) {
   const KVView v = view_of(kv, nullptr);
   const int most = ATTN_CTAS_PER_SM * sms;
   const size_t ps = attn_partial_floats(v, true, most);
-  const size_t pd = attn_partial_floats(v, false, most);
+  const size_t pd0 = dense_partial_floats(v, sms);
+  const size_t pd = pd0 > ps ? pd0 : ps;
   const size_t units = (size_t)kv.B * kv.Hq;  // >= B * Hkv
   L.counters = 0;
   L.partials = round_up(units * sizeof(unsigned), 256);
@@ -204,7 +205,7 @@ prhs_status check_ws(const prhs_kv& kv, int sms, void* ws, size_t ws_bytes, Layo
 
 // TMA descriptor over K viewed as [rows][d*esize/128][128 bytes] with the
 // 128-byte swizzle; boxes of `box_rows` rows.
-prhs_status make_tmap(const prhs_kv& kv, int box_rows, CUtensorMap* map) {
+prhs_status make_tmap(const prhs_kv& kv, int box_rows, CUtensorMap* map, const void* base = nullptr) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return fail(PRHS_ECUDA, "cuTensorMapEncodeTiled unavailable");
   const size_t es = elem_size(kv.dtype);
@@ -218,7 +219,8 @@ prhs_status make_tmap(const prhs_kv& kv, int box_rows, CUtensorMap* map) {
   const cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)segs, (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, kv.dtype == PRHS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                   3, const_cast<void*>(kv.k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   3, const_cast<void*>(base != nullptr ? base : kv.k), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PRHS_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -304,7 +306,7 @@ prhs_status check_select_args(const prhs_kv& kv, const void* q, int N, const int
 prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws, const void* q,
                     float scale, const int32_t* idx, const int32_t* n_sel, int cap, float* out,
                     float* lse, bool sparse, cudaStream_t st, const uint8_t* unit_mask = nullptr,
-                    int mask_want = 0, bool second_region = false) {
+                    int mask_want = 0, bool second_region = false, int max_ctas = 0) {
   AttnLaunch a;
   a.kv = view_of(kv, di->err);
   a.q = q;
@@ -319,6 +321,7 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
   a.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + (second_region ? L.partials2 : L.partials));
   a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.counters);
   a.ctas = attn_ctas(kv, sparse, cap, di->sms);
+  if (max_ctas > 0 && a.ctas > max_ctas) a.ctas = max_ctas;
   return launch_result(launch_attn(a, sparse, st), sparse ? "sparse attention" : "dense attention");
 }
 
@@ -474,7 +477,19 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
   if ((s = device_info(&di)) != PRHS_OK) return s;
   Layout L;
   if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
-  return do_attn(*kv, di, L, ws, q, scale, nullptr, nullptr, 0, out, lse, false, stream);
+  if (kv->Hq == kv->Hkv)  // no query group to share K/V tiles: the gather kernel streams faster
+    return do_attn(*kv, di, L, ws, q, scale, nullptr, nullptr, 0, out, lse, false, stream);
+  const bool paged = kv->block_table != nullptr;
+  const KVView v = view_of(*kv, di->err);
+  const int box = paged ? PAGED_BOX_ROWS : dense_rows_per_stage(v);
+  CUtensorMap kmap, vmap;
+  if ((s = make_tmap(*kv, box, &kmap, kv->k)) != PRHS_OK) return s;
+  if ((s = make_tmap(*kv, box, &vmap, kv->v)) != PRHS_OK) return s;
+  float* partials = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partials);
+  unsigned* counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.counters);
+  return launch_result(launch_dense(v, q, scale, out, lse, partials, counters, di->sms, paged,
+                                    &kmap, &vmap, stream),
+                       "dense attention");
 }
 
 prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int N,

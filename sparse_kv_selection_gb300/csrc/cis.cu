@@ -23,6 +23,8 @@ __device__ __forceinline__ double warp_sum_f64(double v) {
   return v;
 }
 
+constexpr int CIS_PER = 4;  // anchor entries per thread per chunk
+
 template <typename T>
 __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   __shared__ double red[3][CIS_THREADS / 32];
@@ -35,37 +37,43 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   const int b = qh / kv.Hq;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int d = kv.d;
+  constexpr int CHUNK = CIS_THREADS * CIS_PER;
 
-  // everything this CTA may need is requested before any result is used
+  // every input of the first chunk is requested before any result is used
   int n = a.anchor_n[qh];
   const int t = seq_len(kv, b);
   const int32_t* anc = a.anchor_idx + (long long)qh * a.anchor_cap;
   const int ncap = min(n, a.anchor_cap);
-  int pre_x = -1, pre_prev = -1;
-  if (tid < ncap) {
-    pre_x = anc[tid];
-    pre_prev = tid > 0 ? anc[tid - 1] : -1;
+  int x[CIS_PER];
+  int prev0;
+  {
+    const int j0 = tid * CIS_PER;
+#pragma unroll
+    for (int k = 0; k < CIS_PER; k++) x[k] = j0 + k < ncap ? anc[j0 + k] : 0;
+    prev0 = j0 > 0 && j0 - 1 < ncap ? anc[j0 - 1] : -1;
   }
   double dot = 0.0, nq = 0.0, na = 0.0;
   for (int i = tid; i < d; i += CIS_THREADS) {
-    const double x = (double)Elem<T>::load1(a.q, (long long)qh * d + i);
-    const double y = (double)Elem<T>::load1(a.q_anchor, (long long)qh * d + i);
-    dot = fma(x, y, dot);
-    nq = fma(x, x, nq);
-    na = fma(y, y, na);
+    const double u = (double)Elem<T>::load1(a.q, (long long)qh * d + i);
+    const double v = (double)Elem<T>::load1(a.q_anchor, (long long)qh * d + i);
+    dot = fma(u, v, dot);
+    nq = fma(u, u, nq);
+    na = fma(v, v, na);
   }
-  dot = warp_sum_f64(dot);
-  nq = warp_sum_f64(nq);
-  na = warp_sum_f64(na);
-  if (lane == 0) {
-    red[0][warp] = dot;
-    red[1][warp] = nq;
-    red[2][warp] = na;
+  if (warp * 32 < d) {  // only the warps that hold elements take part
+    dot = warp_sum_f64(dot);
+    nq = warp_sum_f64(nq);
+    na = warp_sum_f64(na);
+    if (lane == 0) {
+      red[0][warp] = dot;
+      red[1][warp] = nq;
+      red[2][warp] = na;
+    }
   }
   __syncthreads();
   if (tid == 0) {
     double D = 0, Q = 0, A = 0;
-    for (int w = 0; w < CIS_THREADS / 32; w++) {
+    for (int w = 0; w * 32 < d && w < CIS_THREADS / 32; w++) {
       D += red[0][w];
       Q += red[1][w];
       A += red[2][w];
@@ -78,7 +86,7 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   __syncthreads();
   if (!sh_reuse) return;
 
-  // ---- dilation of the anchor set ----
+  // ---- dilation of the anchor set: CIS_PER consecutive entries per thread ----
   if (n > a.anchor_cap) {
     if (tid == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
     n = a.anchor_cap;
@@ -86,24 +94,37 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   int32_t* out = a.idx + (long long)qh * a.cap;
   const int w = a.w;
   int carry = 0;
-  for (int base = 0; base < n; base += CIS_THREADS) {
-    const int jdx = base + tid;
-    int start = 0, cnt = 0;
-    if (jdx < n) {
-      const int x = base == 0 ? pre_x : anc[jdx];
-      const int prev = base == 0 ? pre_prev : anc[jdx - 1];
-      if (x < 0 || x >= t || x <= prev) {
-        raise_error(kv.err, PRHS_DEV_BAD_INDEX);
-      } else {
-        const int lo = max(0, x - w);
-        const int hi = min(t - 1, x + w);
-        const int prev_hi = jdx > 0 ? min(t - 1, prev + w) : -1;
-        start = max(lo, prev_hi + 1);
-        cnt = max(0, hi - start + 1);
-      }
+  for (int base = 0; base < n; base += CHUNK) {
+    const int j0 = base + tid * CIS_PER;
+    if (base > 0) {
+#pragma unroll
+      for (int k = 0; k < CIS_PER; k++) x[k] = j0 + k < n ? anc[j0 + k] : 0;
+      prev0 = j0 - 1 < n ? anc[j0 - 1] : -1;
     }
-    // block exclusive scan of cnt
-    int v = cnt;
+    int start[CIS_PER], cnt[CIS_PER];
+    int local = 0;
+    int prev = prev0;
+#pragma unroll
+    for (int k = 0; k < CIS_PER; k++) {
+      start[k] = 0;
+      cnt[k] = 0;
+      if (j0 + k < n) {
+        const int xv = x[k];
+        if (xv < 0 || xv >= t || xv <= prev) {
+          raise_error(kv.err, PRHS_DEV_BAD_INDEX);
+        } else {
+          const int lo = max(0, xv - w);
+          const int hi = min(t - 1, xv + w);
+          const int prev_hi = j0 + k > 0 ? min(t - 1, prev + w) : -1;
+          start[k] = max(lo, prev_hi + 1);
+          cnt[k] = max(0, hi - start[k] + 1);
+        }
+        prev = xv;
+      }
+      local += cnt[k];
+    }
+    // block exclusive scan of the per-thread counts
+    int v = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(FULL_MASK, v, o);
@@ -112,21 +133,26 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
     if (lane == 31) warp_tot[warp] = v;
     __syncthreads();
     int before = 0, total = 0;
+#pragma unroll
     for (int w2 = 0; w2 < CIS_THREADS / 32; w2++) {
-      if (w2 < warp) before += warp_tot[w2];
+      before += w2 < warp ? warp_tot[w2] : 0;
       total += warp_tot[w2];
     }
-    const int pos = carry + before + v - cnt;
-    for (int e = 0; e < cnt; e++) {
-      if (pos + e < a.cap) {
-        out[pos + e] = start + e;
-      } else {
-        raise_error(kv.err, PRHS_DEV_CAPACITY);
-        break;
+    int pos = carry + before + v - local;
+#pragma unroll
+    for (int k = 0; k < CIS_PER; k++) {
+      for (int e = 0; e < cnt[k]; e++) {
+        if (pos + e < a.cap) {
+          out[pos + e] = start[k] + e;
+        } else {
+          raise_error(kv.err, PRHS_DEV_CAPACITY);
+          break;
+        }
       }
+      pos += cnt[k];
     }
     carry += total;
-    __syncthreads();  // warp_tot reused by the next chunk
+    if (base + CHUNK < n) __syncthreads();  // warp_tot is reused by the next chunk
   }
   if (tid == 0) a.n_sel[qh] = min(carry, a.cap);
 }

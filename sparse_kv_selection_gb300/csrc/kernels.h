@@ -102,6 +102,13 @@ prhs_status abi_fail(prhs_status s, const char* msg);
 KVView abi_view(const prhs_kv& kv, unsigned* err);
 int abi_attn_ctas(const prhs_kv& kv, bool sparse, int cap, int sms);
 
+// Dense attention through TMA-staged K/V tiles (one launch per call).
+cudaError_t launch_dense(const KVView& kv, const void* q, float scale, float* out, float* lse,
+                         float* partials, unsigned* counters, int ctas, bool paged,
+                         const CUtensorMap* kmap, const CUtensorMap* vmap, cudaStream_t st);
+size_t dense_partial_floats(const KVView& kv, int ctas);
+int dense_rows_per_stage(const KVView& kv);
+
 // Bytes of dynamic shared memory the scoring kernel needs for this shape.
 size_t score_smem_bytes(prhs_dtype dt, int d);
 

@@ -33,9 +33,9 @@ struct SelClusterShared {
   unsigned lcand[SEL_CANDS];  // this CTA's own candidate keys
   unsigned ncand, nlcand;
   unsigned scan[32];
-  float red[SEL_WARPS];
+  float red[SEL_WARPS], red2[SEL_WARPS];
   float lmin, lmax;           // this CTA's logit range
-  float Zp;                   // this CTA's sum of exp(s - max)
+  float Zp;                   // this CTA's sum of exp(s - max) over all its logits
   unsigned cnt_gt, cnt_eq;    // this CTA's logits above / equal to the threshold
   float dsum;                 // this CTA's dropped weight
   unsigned digit, krem, cnt_bin, thr, keq;
@@ -223,28 +223,15 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   const float w1 = (smax - smin) * (1.f / 2048.f);
   const float inv1 = flat ? 0.f : 2048.f / (smax - smin);
 
-  // ---- pass 1: softmax partial sum and value histogram over [smin, smax] ----
-  float z = 0.f;
-  for (int i = tid; i < cnt; i += SEL_THREADS) {
-    const float s = cache[i];
-    z += expf(s - smax);
-    if (!flat) atomicAdd(&sh.hist[vbin(s, smin, inv1)], 1u);
-  }
-  z = warp_sum(z);
-  if (lane == 0) sh.red[warp] = z;
-  __syncthreads();
-  if (tid == 0) {
-    float zz = 0.f;
-    for (int w = 0; w < SEL_WARPS; w++) zz += sh.red[w];
-    sh.Zp = zz;
-  }
-  if (!flat)
+  // ---- pass 1: value histogram over [smin, smax] ----
+  if (!flat) {
+    for (int i = tid; i < cnt; i += SEL_THREADS) atomicAdd(&sh.hist[vbin(cache[i], smin, inv1)], 1u);
+    __syncthreads();
     for (int i = tid; i < 2048; i += SEL_THREADS)
       if (sh.hist[i]) atomicAdd(&root->histg[0][i], sh.hist[i]);
+  }
   __syncthreads();
   head_sync<ONE>(cluster);
-  float Z = 0.f;
-  for (int r = 0; r < CL; r++) Z += rank_shared<ONE>(cluster, sh, r)->Zp;
 
   // ---- threshold: the key of the N-th largest logit, and how many ties to keep ----
   unsigned thr = 0, keq = 0, cta_gt = 0, cta_eq = 0;
@@ -256,43 +243,51 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   } else {
     find_bin(root->histg[0], 2048, (unsigned)Nb, sh);
     const int b1 = (int)sh.digit;
-    const unsigned krem1 = sh.krem;
+    unsigned krem = sh.krem;
     const float lo1 = smin + (float)b1 * w1;
     const float inv2 = w1 > 0.f ? 2048.f / w1 : 0.f;
-    // pass 2: second value histogram inside bin b1
-    for (int i = tid; i < 2048; i += SEL_THREADS) sh.hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < cnt; i += SEL_THREADS) {
-      const float s = cache[i];
-      if (vbin(s, smin, inv1) == b1) atomicAdd(&sh.hist[vbin(s, lo1, inv2)], 1u);
+    int b2 = -1;  // -1: the candidates are all of bin b1
+    if (sh.cnt_bin > SEL_CANDS) {
+      // pass 2: second value histogram inside bin b1
+      for (int i = tid; i < 2048; i += SEL_THREADS) sh.hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < cnt; i += SEL_THREADS) {
+        const float s = cache[i];
+        if (vbin(s, smin, inv1) == b1) atomicAdd(&sh.hist[vbin(s, lo1, inv2)], 1u);
+      }
+      __syncthreads();
+      for (int i = tid; i < 2048; i += SEL_THREADS)
+        if (sh.hist[i]) atomicAdd(&root->histg[1][i], sh.hist[i]);
+      __syncthreads();
+      head_sync<ONE>(cluster);
+      find_bin(root->histg[1], 2048, krem, sh);
+      b2 = (int)sh.digit;
+      krem = sh.krem;
     }
-    __syncthreads();
-    for (int i = tid; i < 2048; i += SEL_THREADS)
-      if (sh.hist[i]) atomicAdd(&root->histg[1][i], sh.hist[i]);
-    __syncthreads();
-    head_sync<ONE>(cluster);
-    find_bin(root->histg[1], 2048, krem1, sh);
-    const int b2 = (int)sh.digit;
-    const unsigned krem2 = sh.krem;
     if (sh.cnt_bin <= SEL_CANDS) {
-      // pass 3: gather the candidates of bin (b1, b2); count the logits above them
+      // pass 3: gather the candidates; count the logits above them
       unsigned dgt = 0;
       for (int i = tid; i < cnt; i += SEL_THREADS) {
         const float s = cache[i];
         const int c1 = vbin(s, smin, inv1);
+        bool cand = false;
         if (c1 > b1) {
           dgt++;
         } else if (c1 == b1) {
-          const int c2 = vbin(s, lo1, inv2);
-          if (c2 > b2) {
-            dgt++;
-          } else if (c2 == b2) {
-            const unsigned u = order_key(s);
-            const unsigned slot = atomicAdd(&root->ncand, 1u);
-            if (slot < SEL_CANDS) root->cand[slot] = u;
-            const unsigned ls = atomicAdd(&sh.nlcand, 1u);
-            if (ls < SEL_CANDS) sh.lcand[ls] = u;
+          if (b2 < 0) {
+            cand = true;
+          } else {
+            const int c2 = vbin(s, lo1, inv2);
+            if (c2 > b2) dgt++;
+            cand = c2 == b2;
           }
+        }
+        if (cand) {
+          const unsigned u = order_key(s);
+          const unsigned slot = atomicAdd(&root->ncand, 1u);
+          if (slot < SEL_CANDS) root->cand[slot] = u;
+          const unsigned ls = atomicAdd(&sh.nlcand, 1u);
+          if (ls < SEL_CANDS) sh.lcand[ls] = u;
         }
       }
       unsigned dgt_cta;
@@ -310,9 +305,9 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
           g += sh.cand[jj] > myc;
           e += sh.cand[jj] == myc;
         }
-        if (g < krem2 && g + e >= krem2) {
+        if (g < krem && g + e >= krem) {
           sh.thr = myc;
-          sh.keq = krem2 - g;
+          sh.keq = krem - g;
         }
       }
       __syncthreads();
@@ -380,7 +375,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   // ---- index-ordered compaction; dropped weight of the rest ----
   constexpr int E = 4;
   constexpr int TILE = SEL_THREADS * E;
-  float dsum = 0.f;
+  float dsum = 0.f, ssum = 0.f;  // weights exp(s - max) of dropped / kept logits
   for (int base = 0; base < cnt; base += TILE) {
     unsigned u[E];
     float sv[E];
@@ -415,7 +410,9 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
         }
         eq_before++;
       }
+      const float wgt = expf(sv[e] - smax);
       if (take) {
+        ssum += wgt;
         if (pos < Nb) {
           out[pos] = lo + i;
           if (aout) aout[pos] = lo + i;
@@ -423,26 +420,38 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
           raise_error(kv.err, PRHS_DEV_CAPACITY);
         }
       } else {
-        dsum += expf(sv[e] - smax);
+        dsum += wgt;
       }
     }
     carry_gt += tot >> 16;
     carry_eq += tot & 0xffffu;
   }
   dsum = warp_sum(dsum);
-  if (lane == 0) sh.red[warp] = dsum;
+  ssum = warp_sum(ssum);
+  if (lane == 0) {
+    sh.red[warp] = dsum;
+    sh.red2[warp] = ssum;
+  }
   __syncthreads();
   if (tid == 0) {
-    float s = 0.f;
-    for (int w = 0; w < SEL_WARPS; w++) s += sh.red[w];
+    float s = 0.f, s2 = 0.f;
+    for (int w = 0; w < SEL_WARPS; w++) {
+      s += sh.red[w];
+      s2 += sh.red2[w];
+    }
     sh.dsum = s;
+    sh.Zp = s + s2;
   }
   __syncthreads();
   head_sync<ONE>(cluster);
   if (rank == 0) {
     if (tid == 0) {
-      float s = 0.f;
-      for (int r = 0; r < CL; r++) s += rank_shared<ONE>(cluster, sh, r)->dsum;
+      float s = 0.f, Z = 0.f;
+      for (int r = 0; r < CL; r++) {
+        const SelClusterShared* rs = rank_shared<ONE>(cluster, sh, r);
+        s += rs->dsum;
+        Z += rs->Zp;
+      }
       a.n_sel[qh] = Nb;
       a.delta[qh] = s / Z;
       if (a.anchor_n) a.anchor_n[qh] = Nb;

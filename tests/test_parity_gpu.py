@@ -369,3 +369,57 @@ def test_decode_matches_oracle(name):
     compared, r = compare_decode(wl, dev, kv, _heads(wl))
     assert compared >= len(_heads(wl)) * wl.steps // 2
     assert r[1:].any() or wl.steps < 3   # some head reused its anchor
+
+
+# --------------------------------------------------------------------------- #
+# the split entry points and graph capture of the decode step
+# --------------------------------------------------------------------------- #
+def test_score_then_select_equals_score_select():
+    S, wl, dev, kv = _setup("gqa4_bf16")
+    N = int(wl.budget[0])
+    outs = []
+    for split in (False, True):
+        idx = torch.full((wl.B, wl.Hq, N), -1, dtype=torch.int32, device="cuda")
+        n_sel = torch.zeros(wl.B, wl.Hq, dtype=torch.int32, device="cuda")
+        delta = torch.zeros(wl.B, wl.Hq, device="cuda")
+        ws = S.make_workspace(kv, N)
+        if split:
+            S.binding.score(kv, dev["q"][3], wl.scale, ws)
+            S.binding.select(kv, dev["q"][3], N, idx, n_sel, delta, ws)
+        else:
+            S.score_select(kv, dev["q"][3], wl.scale, N, idx, n_sel, delta, ws)
+        outs.append((idx.cpu(), n_sel.cpu(), delta.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][2], outs[1][2])
+
+
+@pytest.mark.parametrize("name", ["mha_bf16_ragged", "paged_bf16"])
+def test_decode_step_in_cuda_graph_matches_eager(name):
+    """prhs_decode_step forks onto a side stream; captured in a CUDA graph and
+    replayed, it must give the eager results bit for bit."""
+    S, wl, dev, kv = _setup(name)
+    nb = dev["budget"] if len(set(wl.budget.tolist())) > 1 else None
+    N = None if nb is not None else int(wl.budget[0])
+
+    def run(graph):
+        dec = S.SparseDecoder(kv, N=N, n_budget=nb, w=wl.w, tau=wl.tau, scale=wl.scale)
+        outs = dec.alloc_outputs(wl.steps)
+        stream = torch.cuda.Stream()
+        if not graph:
+            with torch.cuda.stream(stream):
+                dec.run(dev["q"], outs)
+        else:
+            with torch.cuda.stream(stream):   # eager warm-up resolves per-device state
+                dec.run(dev["q"], dec.alloc_outputs(wl.steps))
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                dec.reset()
+                dec.run(dev["q"], outs)
+            g.replay()
+        torch.cuda.synchronize()
+        return [x.cpu() for x in outs]
+
+    eager, graphed = run(False), run(True)
+    for a, b in zip(eager, graphed):
+        assert torch.equal(a.nan_to_num(), b.nan_to_num())

@@ -123,15 +123,21 @@ prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* 
 
 /* Critical-index-set reuse with dilation (Fig. 2, Fig. 4, Fig. 8, Table VIII).
  * Per query head: c = <q, q_anchor> / (|q| |q_anchor|) evaluated in float64;
- * reuse = anchor_n > 0 and |q| |q_anchor| > 0 and c >= tau.
+ * reuse = anchor_n > 0 and |q| |q_anchor| > 0 and c >= tau, and, when
+ * max_run > 0, anchor_age < max_run - 1: the CIS block size s of Tables IV,
+ * V and VIII read as the most consecutive queries one retrieval serves.
+ * anchor_age [B][Hq] int32 counts reuses since the anchor retrieved; it is
+ * required when max_run > 0 (nullable otherwise) and is updated to
+ * reuse ? age + 1 : 0.
  * When reuse: idx = union over anchor entries a of [a - w, a + w] clipped to
  * [0, t_b), ascending without repeats, n_sel its size (<= cap required).
  * When not: idx and n_sel rows are left untouched. reuse [B][Hq] is always
  * written. anchor_idx rows must be ascending and inside [0, t_b). */
 prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx,
                             const int32_t* anchor_n, int anchor_cap, const void* q,
-                            const void* q_anchor, int w, double tau, int32_t* idx,
-                            int32_t* n_sel, int cap, uint8_t* reuse, cudaStream_t stream);
+                            const void* q_anchor, int w, double tau, int max_run,
+                            int32_t* anchor_age, int32_t* idx, int32_t* n_sel, int cap,
+                            uint8_t* reuse, cudaStream_t stream);
 
 /* Sparse attention over the selected rows (Table V caption: sparse-attention
  * kernel over the selected KV): per query head with n = n_sel entries of idx,
@@ -176,10 +182,12 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
  *   prhs_sparse_attn(idx).
  * Heads that reuse attend the dilated anchor set; the others retrieve a fresh
  * top-N set, attend it and make it (with q) the new anchor. delta is written
- * for retrieving heads only. Start a sequence with anchor_n all zero. */
+ * for retrieving heads only. Start a sequence with anchor_n (and anchor_age)
+ * all zero; max_run and anchor_age as in prhs_cis_dilate. */
 prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int N,
-                             const int32_t* n_budget, int w, double tau,
-                             int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
+                             const int32_t* n_budget, int w, double tau, int max_run,
+                             int32_t* anchor_age, int32_t* anchor_idx, int32_t* anchor_n,
+                             int anchor_cap,
                              void* q_anchor, int32_t* idx, int32_t* n_sel, int cap,
                              uint8_t* reuse, float* delta, float* out, float* lse,
                              void* ws, size_t ws_bytes, cudaStream_t stream);

@@ -161,7 +161,8 @@ class HeadStep:
 
 
 def decode_head(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, N: int, w: int,
-                tau: float, scale: float, keep_scores: bool = False) -> list[HeadStep]:
+                tau: float, scale: float, keep_scores: bool = False,
+                max_run: int = 0) -> list[HeadStep]:
     """One head through a sequence of decode queries with CIS reuse.
 
     Reading of Fig. 4 ("critical tokens from query 405 are shared to queries
@@ -170,6 +171,12 @@ def decode_head(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, N: int, w: in
     retrieving query (the anchor) is >= tau attends the anchor's top-N set
     dilated by +/- w; otherwise it retrieves and becomes the new anchor.
     Dilation is applied to the anchor set once, never compounded.
+
+    max_run > 0 reads the CIS block size s of Tables IV, V and VIII ("CIS-8",
+    "CIS-16") as the most consecutive queries one retrieval may serve: after
+    s - 1 reuses the next query retrieves whatever its similarity. 0 = no
+    bound. Parity unpinned beyond its two limits (s = 1 always retrieves;
+    s = 2 with every gate open alternates), which the tests check.
     """
     K = np.asarray(K, np.float64)
     V = np.asarray(V, np.float64)
@@ -177,8 +184,12 @@ def decode_head(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, N: int, w: in
     anchor_S = None
     anchor_q = None
     rec = []
+    age = 0  # reuses since the anchor retrieved
     for q in np.asarray(q_steps, np.float64):
         c, reuse = (None, False) if anchor_S is None else cis_gate(q, anchor_q, tau)
+        if max_run > 0 and age >= max_run - 1:
+            reuse = False
+        age = age + 1 if reuse else 0
         s = scores(q, K, scale)
         delta = s_nth = None
         if reuse:
@@ -196,7 +207,7 @@ def decode_head(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, N: int, w: in
     return rec
 
 
-def decode_workload(wl, heads=None, steps=None, keep_scores=False):
+def decode_workload(wl, heads=None, steps=None, keep_scores=False, max_run=0):
     """Run decode_head over (b, query head) pairs of a ``workloads.Workload``.
 
     Query head hq reads KV head hq // (Hq / Hkv) (consecutive grouping, the
@@ -215,5 +226,5 @@ def decode_workload(wl, heads=None, steps=None, keep_scores=False):
         K, V = cache[(b, kvh)]
         qs = widen(wl.q[:nsteps, b, hq], wl.dtype)
         res[(b, hq)] = decode_head(qs, K, V, int(wl.budget[b]), wl.w, wl.tau, wl.scale,
-                                   keep_scores=keep_scores)
+                                   keep_scores=keep_scores, max_run=max_run)
     return res

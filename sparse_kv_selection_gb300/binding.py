@@ -60,11 +60,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "prhs_score_select": (I, [KV, P, F, I, P, P, P, P, I, P, P, P, I, P, P, Z, P]),
         "prhs_score": (I, [KV, P, F, P, P, Z, P]),
         "prhs_select": (I, [KV, P, I, P, P, P, P, I, P, P, P, I, P, P, Z, P]),
-        "prhs_cis_dilate": (I, [KV, P, P, I, P, P, I, D, P, P, I, P, P]),
+        "prhs_cis_dilate": (I, [KV, P, P, I, P, P, I, D, I, P, P, P, I, P, P]),
         "prhs_sparse_attn": (I, [KV, P, F, P, P, I, P, P, P, Z, P]),
         "prhs_sparse_attn_noalloc": (I, [KV, P, F, P, P, I, P, P, P]),
         "prhs_dense_attn": (I, [KV, P, F, P, P, P, Z, P]),
-        "prhs_decode_step": (I, [KV, P, F, I, P, I, D, P, P, I, P, P, P, I, P, P, P, P, P, Z, P]),
+        "prhs_decode_step": (I, [KV, P, F, I, P, I, D, I, P, P, P, I, P, P, P, I, P, P, P, P, P, Z, P]),
         "prhs_last_error": (I, []),
         "prhs_device_error_bits": (ctypes.c_uint, []),
         "prhs_status_str": (ctypes.c_char_p, [I]),
@@ -196,11 +196,12 @@ def select(kv, q, N, idx, n_sel, delta, ws, *, n_budget=None, head_skip=None, an
                               _stream(stream)), "select")
 
 
-def cis_dilate(kv, anchor_idx, anchor_n, q, q_anchor, w, tau, idx, n_sel, reuse, stream=None) -> None:
+def cis_dilate(kv, anchor_idx, anchor_n, q, q_anchor, w, tau, idx, n_sel, reuse, *, max_run=0,
+               anchor_age=None, stream=None) -> None:
     _check(load().prhs_cis_dilate(kv.ref(), _ptr(anchor_idx), _ptr(anchor_n), anchor_idx.shape[-1],
-                                  _ptr(q), _ptr(q_anchor), int(w), float(tau), _ptr(idx),
-                                  _ptr(n_sel), idx.shape[-1], _ptr(reuse), _stream(stream)),
-           "cis_dilate")
+                                  _ptr(q), _ptr(q_anchor), int(w), float(tau), int(max_run),
+                                  _ptr(anchor_age), _ptr(idx), _ptr(n_sel), idx.shape[-1],
+                                  _ptr(reuse), _stream(stream)), "cis_dilate")
 
 
 def sparse_attn(kv, q, scale, idx, n_sel, out, lse, ws, stream=None) -> None:
@@ -222,9 +223,10 @@ def dense_attn(kv, q, scale, out, lse, ws, stream=None) -> None:
 
 
 def decode_step(kv, q, scale, N, w, tau, anchor_idx, anchor_n, q_anchor, idx, n_sel, reuse, delta,
-                out, lse, ws, *, n_budget=None, stream=None) -> None:
+                out, lse, ws, *, n_budget=None, max_run=0, anchor_age=None, stream=None) -> None:
     _check(load().prhs_decode_step(kv.ref(), _ptr(q), float(scale), int(N), _ptr(n_budget), int(w),
-                                   float(tau), _ptr(anchor_idx), _ptr(anchor_n),
+                                   float(tau), int(max_run), _ptr(anchor_age), _ptr(anchor_idx),
+                                   _ptr(anchor_n),
                                    anchor_idx.shape[-1], _ptr(q_anchor), _ptr(idx), _ptr(n_sel),
                                    idx.shape[-1], _ptr(reuse), _ptr(delta), _ptr(out), _ptr(lse),
                                    _ptr(ws), ws.numel(), _stream(stream)), "decode_step")

@@ -327,8 +327,8 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
 
 prhs_status do_cis(const prhs_kv& kv, DeviceInfo* di, const int32_t* anchor_idx,
                    const int32_t* anchor_n, int anchor_cap, const void* q, const void* q_anchor,
-                   int w, double tau, int32_t* idx, int32_t* n_sel, int cap, uint8_t* reuse,
-                   cudaStream_t st) {
+                   int w, double tau, int max_run, int32_t* anchor_age, int32_t* idx,
+                   int32_t* n_sel, int cap, uint8_t* reuse, cudaStream_t st) {
   CisLaunch c;
   c.kv = view_of(kv, di->err);
   c.anchor_idx = anchor_idx;
@@ -338,6 +338,8 @@ prhs_status do_cis(const prhs_kv& kv, DeviceInfo* di, const int32_t* anchor_idx,
   c.q_anchor = q_anchor;
   c.w = w;
   c.tau = tau;
+  c.max_run = max_run;
+  c.anchor_age = anchor_age;
   c.idx = idx;
   c.n_sel = n_sel;
   c.cap = cap;
@@ -438,20 +440,22 @@ prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* 
 
 prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx, const int32_t* anchor_n,
                             int anchor_cap, const void* q, const void* q_anchor, int w, double tau,
-                            int32_t* idx, int32_t* n_sel, int cap, uint8_t* reuse,
-                            cudaStream_t stream) {
+                            int max_run, int32_t* anchor_age, int32_t* idx, int32_t* n_sel, int cap,
+                            uint8_t* reuse, cudaStream_t stream) {
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
   if (!anchor_idx || !anchor_n || !q || !q_anchor || !idx || !n_sel || !reuse)
     return fail(PRHS_EINVAL, "cis: null pointer argument");
   if (w < 0) return fail(PRHS_EINVAL, "w must be >= 0 (got %d)", w);
+  if (max_run < 0) return fail(PRHS_EINVAL, "max_run must be >= 0 (got %d)", max_run);
+  if (max_run > 0 && anchor_age == nullptr) return fail(PRHS_EINVAL, "max_run > 0 needs anchor_age");
   if (anchor_cap <= 0 || cap <= 0) return fail(PRHS_EINVAL, "capacities must be positive");
   if (!dilated_fits(anchor_cap, w, t_max_of(*kv), cap))
     return fail(PRHS_EINVAL, "cap %d < min(t_max, anchor_cap * (2w + 1))", cap);
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
-  return do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, tau, idx, n_sel, cap,
-                reuse, stream);
+  return do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, tau, max_run,
+                anchor_age, idx, n_sel, cap, reuse, stream);
 }
 
 prhs_status prhs_sparse_attn(const prhs_kv* kv, const void* q, float scale, const int32_t* idx,
@@ -493,7 +497,8 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
 }
 
 prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int N,
-                             const int32_t* n_budget, int w, double tau, int32_t* anchor_idx,
+                             const int32_t* n_budget, int w, double tau, int max_run,
+                             int32_t* anchor_age, int32_t* anchor_idx,
                              int32_t* anchor_n, int anchor_cap, void* q_anchor, int32_t* idx,
                              int32_t* n_sel, int cap, uint8_t* reuse, float* delta, float* out,
                              float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -503,6 +508,8 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
     return fail(PRHS_EINVAL, "decode: null pointer argument");
   if (n_budget == nullptr && N <= 0) return fail(PRHS_EINVAL, "N must be positive (got %d)", N);
   if (w < 0) return fail(PRHS_EINVAL, "w must be >= 0 (got %d)", w);
+  if (max_run < 0) return fail(PRHS_EINVAL, "max_run must be >= 0 (got %d)", max_run);
+  if (max_run > 0 && anchor_age == nullptr) return fail(PRHS_EINVAL, "max_run > 0 needs anchor_age");
   const int tmax = t_max_of(*kv);
   if (anchor_cap <= 0 || cap <= 0) return fail(PRHS_EINVAL, "capacities must be positive");
   if (n_budget == nullptr && anchor_cap < (N < tmax ? N : tmax))
@@ -513,8 +520,8 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if ((s = device_info(&di)) != PRHS_OK) return s;
   Layout L;
   if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
-  if ((s = do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, tau, idx, n_sel, cap,
-                  reuse, stream)) != PRHS_OK)
+  if ((s = do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, tau, max_run,
+                  anchor_age, idx, n_sel, cap, reuse, stream)) != PRHS_OK)
     return s;
   // Two branches after the gate: heads that reuse their anchor only need the
   // dilated sets and attend on the side stream, while the retrieving heads

@@ -2,7 +2,8 @@
 // "Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference":
 // Fig. 2 (adjacent queries with cosine similarity above 0.8 share critical
 // indices), Fig. 8 (sharing triggers when sim(q, q') >= tau), Fig. 4 and
-// Table VIII (the shared set is dilated; radius r).
+// Table VIII (the shared set is dilated; radius r), and the CIS block size s
+// of Tables IV, V and VIII read as a bound on consecutive reuses.
 //
 // One CTA per query head. The gate is evaluated in float64 so that it takes
 // the same decision as a float64 reference. The dilated set
@@ -41,6 +42,7 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
 
   // every input of the first chunk is requested before any result is used
   int n = a.anchor_n[qh];
+  const int age = a.anchor_age != nullptr ? a.anchor_age[qh] : 0;
   const int t = seq_len(kv, b);
   const int32_t* anc = a.anchor_idx + (long long)qh * a.anchor_cap;
   const int ncap = min(n, a.anchor_cap);
@@ -79,9 +81,11 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
       A += red[2][w];
     }
     const double den = sqrt(Q) * sqrt(A);
-    const int reuse = n > 0 && den > 0.0 && (D / den) >= a.tau;
+    const int reuse = n > 0 && den > 0.0 && (D / den) >= a.tau &&
+                      (a.max_run <= 0 || age < a.max_run - 1);
     sh_reuse = reuse;
     a.reuse[qh] = (uint8_t)reuse;
+    if (a.anchor_age != nullptr) a.anchor_age[qh] = reuse ? age + 1 : 0;
   }
   __syncthreads();
   if (!sh_reuse) return;

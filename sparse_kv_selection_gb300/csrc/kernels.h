@@ -60,6 +60,8 @@ struct CisLaunch {
   const void* q_anchor;
   int w;
   double tau;
+  int max_run;           // 0: reuse runs are unbounded
+  int32_t* anchor_age;   // [B][Hq] reuses since the anchor retrieved (null when max_run == 0)
   int32_t* idx;
   int32_t* n_sel;
   int cap;

@@ -17,7 +17,7 @@ from . import binding as _b
 
 class SparseDecoder:
     def __init__(self, kv: _b.KVCache, *, N: int | None = None, n_budget=None, w: int = 2,
-                 tau: float = 0.8, scale: float | None = None, stream=None):
+                 tau: float = 0.8, scale: float | None = None, max_run: int = 0, stream=None):
         dev = kv.k.device
         self.kv, self.w, self.tau = kv, int(w), float(tau)
         self.scale = scale if scale is not None else kv.desc.d ** -0.5
@@ -32,6 +32,8 @@ class SparseDecoder:
         i32 = dict(device=dev, dtype=torch.int32)
         self.anchor_idx = torch.zeros(B, Hq, self.anchor_cap, **i32)
         self.anchor_n = torch.zeros(B, Hq, **i32)
+        self.max_run = int(max_run)
+        self.anchor_age = torch.zeros(B, Hq, **i32)
         self.q_anchor = torch.zeros(B, Hq, d, device=dev, dtype=qdt)
         self.idx = torch.zeros(B, Hq, self.cap, **i32)
         self.n_sel = torch.zeros(B, Hq, **i32)
@@ -45,6 +47,7 @@ class SparseDecoder:
     def reset(self) -> None:
         """Forget every anchor: the next step retrieves for all heads."""
         self.anchor_n.zero_()
+        self.anchor_age.zero_()
 
     def step(self, q: torch.Tensor, out=None, lse=None, delta=None, reuse=None, n_sel=None) -> None:
         """One decode query per head (q [B][Hq][d] on the device). Results go
@@ -57,7 +60,8 @@ class SparseDecoder:
                        self.delta if delta is None else delta,
                        self.out if out is None else out,
                        self.lse if lse is None else lse,
-                       self.ws, n_budget=self.n_budget, stream=self.stream)
+                       self.ws, n_budget=self.n_budget, max_run=self.max_run,
+                       anchor_age=self.anchor_age, stream=self.stream)
 
     def run(self, q_steps: torch.Tensor, outs=None):
         """Decode a [S][B][Hq][d] device sequence; returns stacked per-step

@@ -90,10 +90,15 @@ def test_null_arguments_rejected(lib):
     assert lib.prhs_score_select(ctypes.byref(kv), 64, 0.1, 8, None, None, 64, 64, 8, 64, 64,
                                  None, 8, None, 256, 1 << 20, None) == binding.PRHS_EINVAL
     # dilation radius and dilated capacity
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, -1, 0.8, 64, 64, 64, 64,
-                               None) == binding.PRHS_EINVAL
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0.8, 64, 64, 39, 64,
-                               None) == binding.PRHS_EINVAL
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, -1, 0.8, 0, None, 64, 64, 64,
+                               64, None) == binding.PRHS_EINVAL
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0.8, 0, None, 64, 64, 39,
+                               64, None) == binding.PRHS_EINVAL
+    # a bounded reuse run needs the per-head age counters; a negative bound is invalid
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0.8, 4, None, 64, 64, 64,
+                               64, None) == binding.PRHS_EINVAL
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0.8, -1, 64, 64, 64, 64,
+                               64, None) == binding.PRHS_EINVAL
     assert lib.prhs_dense_attn(ctypes.byref(kv), None, 0.1, 64, 64, 256, 1 << 20, None) == binding.PRHS_EINVAL
     assert lib.prhs_workspace_init(None, 0, None) == binding.PRHS_EWORKSPACE
 

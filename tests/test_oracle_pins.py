@@ -225,6 +225,26 @@ def check_decode_schedule(rng):
         assert np.allclose(o, r.out) and abs(l - r.lse) < 1e-14
 
 
+def check_max_run(rng):
+    t, d, N, w = 90, 16, 8, 1
+    K = rng.normal(size=(t, d))
+    V = rng.normal(size=(t, d))
+    qs = rng.normal(size=(7, d))
+    sc = 1 / math.sqrt(d)
+    # s = 1: every query retrieves even with every gate open
+    assert not any(r.reuse for r in P.decode_head(qs, K, V, N, w, -1.5, sc, max_run=1))
+    # s = 2 with every gate open: retrieve, reuse, retrieve, reuse, ...
+    pat = [r.reuse for r in P.decode_head(qs, K, V, N, w, -1.5, sc, max_run=2)]
+    assert pat == [False, True, False, True, False, True, False]
+    # s = 3: two reuses per retrieval; a retrieval resets the count
+    pat = [r.reuse for r in P.decode_head(qs, K, V, N, w, -1.5, sc, max_run=3)]
+    assert pat == [False, True, True, False, True, True, False]
+    # unbounded equals a bound longer than the sequence
+    a = [r.reuse for r in P.decode_head(qs, K, V, N, w, 0.2, sc)]
+    b = [r.reuse for r in P.decode_head(qs, K, V, N, w, 0.2, sc, max_run=50)]
+    assert a == b
+
+
 def check_widen():
     bits = np.array([0x3F80, 0xC020, 0x0000, 0x8000, 0x7F7F], np.uint16)
     v = P.widen(bits, "bf16")
@@ -286,6 +306,10 @@ def test_decode_schedule(rng):
 
 def test_widen():
     check_widen()
+
+
+def test_max_run(rng):
+    check_max_run(rng)
 
 
 # --------------------------------------------------------------------------- #
@@ -365,6 +389,15 @@ def test_mutation_gate_strict(monkeypatch):
         return c, (c is not None and c > tau)
     monkeypatch.setattr(P, "cis_gate", bad)
     assert _caught(check_cosine_gate, np.random.default_rng(0))
+
+
+def test_mutation_max_run_off_by_one(monkeypatch, rng):
+    good = P.decode_head
+
+    def bad(q_steps, K, V, N, w, tau, scale, keep_scores=False, max_run=0):
+        return good(q_steps, K, V, N, w, tau, scale, keep_scores, max_run + 1 if max_run else 0)
+    monkeypatch.setattr(P, "decode_head", bad)
+    assert _caught(check_max_run, rng)
 
 
 def test_mutation_gate_sign(monkeypatch):

@@ -332,16 +332,16 @@ def test_cis_dilate(dtype, d):
 # --------------------------------------------------------------------------- #
 # whole decode loop
 # --------------------------------------------------------------------------- #
-def compare_decode(wl, dev, kv, heads, steps=None, N=None):
+def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0):
     """Run the device decoder and compare with oracle.decode_head per head,
     up to the first step that holds a near-tie or a near-threshold gate."""
     import sparse_kv_selection_gb300 as S
     steps = wl.steps if steps is None else steps
     nb = dev["budget"] if len(set(wl.budget.tolist())) > 1 else None
     dec = S.SparseDecoder(kv, N=int(wl.budget[0]) if nb is None else None, n_budget=nb, w=wl.w,
-                          tau=wl.tau, scale=wl.scale)
+                          tau=wl.tau, scale=wl.scale, max_run=max_run)
     o, l, dl, r, n = [x.cpu().numpy() for x in dec.run(dev["q"][:steps])]
-    ref = P.decode_workload(wl, heads=heads, steps=steps, keep_scores=True)
+    ref = P.decode_workload(wl, heads=heads, steps=steps, keep_scores=True, max_run=max_run)
     compared = 0
     for (b, h), recs in ref.items():
         for s, rec in enumerate(recs):
@@ -361,6 +361,21 @@ def compare_decode(wl, dev, kv, heads, steps=None, N=None):
             assert abs(l[s, b, h] - rec.lse) <= LSE_TOL, (b, h, s)
             compared += 1
     return compared, r
+
+
+@pytest.mark.parametrize("max_run", [1, 2, 3])
+def test_decode_max_run_matches_oracle(max_run):
+    """CIS block size s as a bound on consecutive reuses (Tables IV/V/VIII)."""
+    S, wl, dev, kv = _setup("gqa4_bf16")
+    compared, r = compare_decode(wl, dev, kv, _heads(wl), max_run=max_run)
+    assert compared >= len(_heads(wl)) * wl.steps // 2
+    if max_run == 1:
+        assert not r.any()
+    else:  # no head reuses more than max_run - 1 times in a row
+        run = np.zeros(r.shape[1:], int)
+        for s in range(r.shape[0]):
+            run = np.where(r[s] != 0, run + 1, 0)
+            assert (run <= max_run - 1).all()
 
 
 @pytest.mark.parametrize("name", list(CASES))

@@ -47,3 +47,50 @@ def kv_rows64(wl, b, kvh):
 
 def q64(wl, step, b, hq):
     return P.widen(wl.q[step, b, hq], wl.dtype)
+
+
+def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0):
+    """Decode on the device query by query and compare sampled heads with
+    oracle.decode_head: reuse flags, the attended set, its size, delta, out
+    and lse. A retrieving step whose set differs from the oracle's only at
+    near-ties is accepted (check_topn) and ends the comparison of that head,
+    since later sets may legitimately differ; so does a gate within
+    GATE_GAP of tau. Returns (steps compared, reuse flags [S][B][Hq])."""
+    import torch
+
+    import sparse_kv_selection_gb300 as S
+    steps = wl.steps if steps is None else steps
+    nb = dev["budget"] if len(set(wl.budget.tolist())) > 1 else None
+    dec = S.SparseDecoder(kv, N=int(wl.budget[0]) if nb is None else None, n_budget=nb, w=wl.w,
+                          tau=wl.tau, scale=wl.scale, max_run=max_run)
+    o, l, dl, r, n = dec.alloc_outputs(steps)
+    dl.fill_(float("nan"))
+    bi = torch.tensor([b for b, _ in heads], device="cuda")
+    hi = torch.tensor([h for _, h in heads], device="cuda")
+    gpu_sets = []
+    for s in range(steps):
+        dec.step(dev["q"][s], o[s], l[s], dl[s], r[s], n[s])
+        gpu_sets.append((dec.idx[bi, hi].cpu().numpy(), n[s][bi, hi].cpu().numpy()))
+    o, l, dl, r, n = [x.cpu().numpy() for x in (o, l, dl, r, n)]
+    ref = P.decode_workload(wl, heads=heads, steps=steps, keep_scores=True, max_run=max_run)
+    compared = 0
+    for k, ((b, h), recs) in enumerate(ref.items()):
+        for s, rec in enumerate(recs):
+            if rec.cos is not None and abs(rec.cos - wl.tau) < GATE_GAP:
+                break
+            assert bool(r[s, b, h]) == rec.reuse, (b, h, s)
+            g_idx, g_n = gpu_sets[s]
+            gset = g_idx[k, :g_n[k]]
+            same = gset.size == rec.S.size and (gset == rec.S).all()
+            if not rec.reuse:
+                assert abs(dl[s, b, h] - rec.delta) <= DELTA_TOL, (b, h, s)
+            else:
+                assert same, ("dilated set differs", b, h, s)
+            assert np.abs(o[s, b, h] - rec.out).max() <= OUT_TOL, (b, h, s)
+            assert abs(l[s, b, h] - rec.lse) <= LSE_TOL, (b, h, s)
+            compared += 1
+            if not same:
+                check_topn(gset, rec.scores, int(wl.budget[b]))  # differs only at near-ties
+                break
+            assert n[s, b, h] == len(rec.S), (b, h, s)
+    return compared, r

@@ -7,8 +7,8 @@ import numpy as np
 import pytest
 
 import oracle.prhs as P
-from parity_util import (DELTA_TOL, GATE_GAP, LSE_TOL, OUT_TOL, TIE_GAP, check_topn, kv_rows64,
-                         q64)
+from parity_util import (DELTA_TOL, GATE_GAP, LSE_TOL, OUT_TOL, TIE_GAP, check_topn,
+                         compare_decode, kv_rows64, q64)
 from workloads import make_workload
 
 torch = pytest.importorskip("torch")
@@ -332,37 +332,6 @@ def test_cis_dilate(dtype, d):
 # --------------------------------------------------------------------------- #
 # whole decode loop
 # --------------------------------------------------------------------------- #
-def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0):
-    """Run the device decoder and compare with oracle.decode_head per head,
-    up to the first step that holds a near-tie or a near-threshold gate."""
-    import sparse_kv_selection_gb300 as S
-    steps = wl.steps if steps is None else steps
-    nb = dev["budget"] if len(set(wl.budget.tolist())) > 1 else None
-    dec = S.SparseDecoder(kv, N=int(wl.budget[0]) if nb is None else None, n_budget=nb, w=wl.w,
-                          tau=wl.tau, scale=wl.scale, max_run=max_run)
-    o, l, dl, r, n = [x.cpu().numpy() for x in dec.run(dev["q"][:steps])]
-    ref = P.decode_workload(wl, heads=heads, steps=steps, keep_scores=True, max_run=max_run)
-    compared = 0
-    for (b, h), recs in ref.items():
-        for s, rec in enumerate(recs):
-            if rec.cos is not None and abs(rec.cos - wl.tau) < GATE_GAP:
-                break
-            assert bool(r[s, b, h]) == rec.reuse, (b, h, s)
-            if not rec.reuse:
-                sc = rec.scores
-                Nb = int(wl.budget[b])
-                if Nb < sc.size:
-                    s_n = np.sort(sc)[::-1][Nb - 1]
-                    if (np.abs(sc - s_n) < TIE_GAP).sum() > 1:
-                        break     # the selected set may differ from here on
-                assert abs(dl[s, b, h] - rec.delta) <= DELTA_TOL, (b, h, s)
-            assert n[s, b, h] == len(rec.S), (b, h, s)
-            assert np.abs(o[s, b, h] - rec.out).max() <= OUT_TOL, (b, h, s)
-            assert abs(l[s, b, h] - rec.lse) <= LSE_TOL, (b, h, s)
-            compared += 1
-    return compared, r
-
-
 @pytest.mark.parametrize("max_run", [1, 2, 3])
 def test_decode_max_run_matches_oracle(max_run):
     """CIS block size s as a bound on consecutive reuses (Tables IV/V/VIII)."""

@@ -170,9 +170,11 @@ prhs_status prhs_sparse_attn_noalloc(const prhs_kv* kv, const void* q, float sca
                                      float* out, float* lse, cudaStream_t stream);
 
 /* Dense attention over all t_b keys (the dense baseline of Table IV), with
- * the same outputs as prhs_sparse_attn over idx = [0, t_b). Work is split by
- * query head; the query heads of one KV head read its rows side by side, so
- * HBM sees each row about once and the repeats are served from L2. */
+ * the same outputs as prhs_sparse_attn over idx = [0, t_b). One query head per
+ * KV head (MHA): the row-gather attention kernel over [0, t_b). Grouped heads:
+ * K and V tiles are staged in shared memory by TMA and every query head of the
+ * group is computed from the same tile, so each row is read from HBM once.
+ * Errors as prhs_sparse_attn; ws from prhs_workspace_size(kv, 0). */
 prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float* out,
                             float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
 

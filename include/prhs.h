@@ -157,7 +157,7 @@ prhs_status prhs_sparse_attn(const prhs_kv* kv, const void* q, float scale,
  * workspace; the split-K scratch is a fixed device array of
  * PRHS_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that
  * loads it until the process exits. A batch whose scratch (256-byte-rounded
- * B*Hq tickets plus (ctas + B*Hq)*(d+2) floats, ctas <= 4 per SM) exceeds
+ * B*Hq tickets plus (ctas + B*Hq)*(d+4) floats, ctas <= 4 per SM) exceeds
  * that size returns PRHS_EINVAL. The first call on each device resolves the array's device
  * address (cudaGetSymbolAddress), so make that first call before any stream
  * capture. Every call shares the array: calls that overlap on the GPU (other

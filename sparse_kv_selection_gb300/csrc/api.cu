@@ -307,6 +307,10 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
                     float scale, const int32_t* idx, const int32_t* n_sel, int cap, float* out,
                     float* lse, bool sparse, cudaStream_t st, const uint8_t* unit_mask = nullptr,
                     int mask_want = 0, bool second_region = false, int max_ctas = 0) {
+  // the kernels index the concatenated rows of all units with 32-bit integers
+  if ((long long)kv.B * kv.Hq * (sparse ? cap : t_max_of(kv)) >= (1ll << 30))
+    return fail(PRHS_EUNSUPPORTED, "B * Hq * %s = %lld rows above 2^30", sparse ? "cap" : "t_max",
+                (long long)kv.B * kv.Hq * (sparse ? cap : t_max_of(kv)));
   AttnLaunch a;
   a.kv = view_of(kv, di->err);
   a.q = q;
@@ -321,6 +325,7 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
   a.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + (second_region ? L.partials2 : L.partials));
   a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.counters);
   a.ctas = attn_ctas(kv, sparse, cap, di->sms);
+  a.min_rows = ATTN_MIN_ROWS;
   if (max_ctas > 0 && a.ctas > max_ctas) a.ctas = max_ctas;
   return launch_result(launch_attn(a, sparse, st), sparse ? "sparse attention" : "dense attention");
 }

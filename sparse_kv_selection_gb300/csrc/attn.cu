@@ -7,12 +7,13 @@
 // Work split. A unit is a query head (sparse) or a KV head with its G query
 // heads (dense); unit u owns rows(u) rows (n_sel or t_b). Every CTA reads
 // all rows(u), forms their prefix sums P and takes rows [c*per, (c+1)*per)
-// of the concatenation, per = ceil(total / CTAs): each CTA gets the same
-// number of rows whatever the mix of set sizes, and a CTA may cover the end
-// of one unit and the start of the next. A unit covered by one CTA is
-// written directly; otherwise each covering CTA writes a partial softmax
-// state into slot c + u and the last one to arrive (atomic ticket, no
-// waiting) merges them into out and lse and resets the ticket.
+// of the concatenation, per = max(ceil(total / CTAs), ATTN_MIN_ROWS): each
+// CTA gets the same number of rows whatever the mix of set sizes (small
+// batches leave the surplus CTAs idle), and a CTA may cover the end of one
+// unit and the start of the next. A unit covered by one CTA is written
+// directly; otherwise each covering CTA writes a partial softmax state into
+// slot c + u and the last one to arrive (atomic ticket, no waiting) merges
+// them, with all its threads at once, into out and lse and resets the ticket.
 //
 // Gather. Eight lanes share a row: lane j reads 16-byte chunks j, j+8, ... of
 // the K and V rows (128 contiguous bytes per 8 lanes per load), so every
@@ -55,16 +56,19 @@ __device__ __forceinline__ void merge_coeffs(float m1, float m2, float& M, float
 }
 
 template <typename T, int D, int G, bool SPARSE>
-__global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(const AttnLaunch a) {
+__global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch a) {
   using S = AttnShape<T, D>;
   constexpr int UNROLL = AttnUnroll<S::CPL, G>::value;
   constexpr int STEP = 16 * UNROLL;  // rows per CTA iteration
-  constexpr int PW = D + 2;          // partial record: m, l, o[D]
+  constexpr int PW = D + 4;          // partial record: m, l, 2 pad, o[D] (16-byte aligned)
+  static_assert(D <= ATTN_THREADS && D % 64 == 0, "merge maps one thread per output element");
   extern __shared__ int sh_prefix[];  // [units + 1]
   __shared__ int sh_idx[SPARSE ? ATTN_IDX_STAGE : 1];
   __shared__ float sm_m[4][G], sm_l[4][G];
   __shared__ float sm_o[4][G][D];
   __shared__ int sh_wsum[ATTN_THREADS / 32];
+  __shared__ float sh_red[ATTN_THREADS / 32];
+  __shared__ float sh_w[ATTN_THREADS];
   __shared__ int sh_last;
 
   pdl_wait();
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(const AttnLaunch a) 
     }
   }
   if (total == 0) return;
-  const int per = (total + C - 1) / C;
+  const int per = max((total + C - 1) / C, max(a.min_rows, 1));
   const int lo = c * per, hi = min(total, lo + per);
   if (lo >= hi) return;
 
@@ -338,7 +342,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(const AttnLaunch a) 
         }
       }
       float* rec = a.partials + ((long long)(c + u) * G + g) * PW;
-      rec[2 + e] = O;
+      rec[4 + e] = O;
       if (e == 0) {
         rec[0] = M;
         rec[1] = L;
@@ -350,22 +354,72 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(const AttnLaunch a) 
     __syncthreads();
     if (!sh_last) continue;
     __threadfence();
-    for (int x = tid; x < G * D; x += ATTN_THREADS) {
-      const int g = x / D, e = x % D;
-      float M = -INFINITY;
-      for (int cs = cf; cs <= cl; cs++)
-        M = fmaxf(M, __ldcg(a.partials + ((long long)(cs + u) * G + g) * PW));
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-        for (int cs = cf; cs <= cl; cs++) {
-          const float* rec = a.partials + ((long long)(cs + u) * G + g) * PW;
-          const float cw = exp2f(__ldcg(rec) - M);
-          L += cw * __ldcg(rec + 1);
-          O += cw * __ldcg(rec + 2 + e);
+    // Merge the ncov partial records of this unit with the whole block: one
+    // parallel pass for the largest max, then per chunk of ATTN_THREADS
+    // records the weights 2^(m_i - M) in shared memory and, warp by warp,
+    // the weighted rows o_i (each lane a 16-byte slice, the loads of a warp
+    // independent of one another).
+    const int ncov = cl - cf + 1;
+    constexpr int EPL = D / 32;  // output elements per lane
+    for (int g = 0; g < G; g++) {
+      const float* rec0 = a.partials + ((long long)(cf + u) * G + g) * PW;
+      const long long RS = (long long)G * PW;  // floats between consecutive records
+      float mx = -INFINITY;
+      for (int i = tid; i < ncov; i += ATTN_THREADS) mx = fmaxf(mx, __ldcg(rec0 + i * RS));
+      mx = warp_max(mx);
+      if (lane == 0) sh_red[warp] = mx;
+      __syncthreads();
+      float M = sh_red[0];
+#pragma unroll
+      for (int w = 1; w < ATTN_THREADS / 32; w++) M = fmaxf(M, sh_red[w]);
+      float Lp = 0.f;
+      float acc[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; e++) acc[e] = 0.f;
+      for (int i0 = 0; i0 < ncov; i0 += ATTN_THREADS) {
+        const int nb = min(ATTN_THREADS, ncov - i0);
+        __syncthreads();  // sh_w and sh_red of the previous round consumed
+        if (tid < nb) {
+          const float* r = rec0 + (i0 + tid) * RS;
+          const float wgt = M == -INFINITY ? 0.f : exp2f(__ldcg(r) - M);
+          sh_w[tid] = wgt;
+          Lp += wgt * __ldcg(r + 1);
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int i = warp; i < nb; i += ATTN_THREADS / 32) {
+          const float wgt = sh_w[i];
+          const float* o = rec0 + (i0 + i) * RS + 4 + lane * EPL;
+          if constexpr (EPL == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
+            acc[0] = fmaf(wgt, v.x, acc[0]);
+            acc[1] = fmaf(wgt, v.y, acc[1]);
+            acc[2] = fmaf(wgt, v.z, acc[2]);
+            acc[3] = fmaf(wgt, v.w, acc[3]);
+          } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
+            acc[0] = fmaf(wgt, v.x, acc[0]);
+            acc[1] = fmaf(wgt, v.y, acc[1]);
+          }
         }
       }
-      a.out[(long long)(qh0 + g) * D + e] = L > 0.f ? O / L : 0.f;
-      if (e == 0) a.lse[qh0 + g] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+      Lp = warp_sum(Lp);
+      __syncthreads();  // every warp done with sh_w and sh_red
+      if (lane == 0) sh_red[warp] = Lp;
+#pragma unroll
+      for (int e = 0; e < EPL; e++) sm_o[warp][0][lane * EPL + e] = acc[e];
+      __syncthreads();
+      if (tid < D) {
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < ATTN_THREADS / 32; w++) {
+          L += sh_red[w];
+          O += sm_o[w][0][tid];
+        }
+        a.out[(long long)(qh0 + g) * D + tid] = L > 0.f ? O / L : 0.f;
+        if (tid == 0) a.lse[qh0 + g] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+      }
+      __syncthreads();  // sm_o and sh_red free for the next query head or unit
     }
     if (tid == 0) a.counters[u] = 0u;
   }
@@ -377,7 +431,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(const AttnLaunch a) 
 int attn_units(const KVView& kv, bool sparse) { (void)sparse; return kv.B * kv.Hq; }
 
 size_t attn_partial_floats(const KVView& kv, bool sparse, int ctas) {
-  return ((size_t)ctas + attn_units(kv, sparse)) * (kv.d + 2);
+  return ((size_t)ctas + attn_units(kv, sparse)) * (kv.d + 4);
 }
 
 template <typename T, int D, int G, bool SPARSE>

@@ -68,6 +68,11 @@ struct CisLaunch {
   uint8_t* reuse;
 };
 
+// A CTA of the attention kernels takes at least this many rows: below it the
+// fixed per-CTA cost (prefix, index staging, partial record, merge) outweighs
+// the extra parallelism.
+constexpr int ATTN_MIN_ROWS = 64;
+
 struct AttnLaunch {
   KVView kv;
   const void* q;
@@ -79,9 +84,10 @@ struct AttnLaunch {
   int cap;
   float* out;
   float* lse;
-  float* partials;       // [ctas + units][G][d + 2]
+  float* partials;       // [ctas + units][G][d + 4]
   unsigned* counters;    // [units], zero on entry, left zero
   int ctas;              // CTAs sharing the rows of all units
+  int min_rows;          // fewest rows a CTA takes (fewer CTAs join small batches)
 };
 
 // Units of the attention split (query heads when sparse, KV heads when dense)

@@ -60,6 +60,8 @@ extern "C" prhs_status prhs_sparse_attn_noalloc(const prhs_kv* kv, const void* q
   if (!q || !idx || !n_sel || !out || !lse)
     return abi_fail(PRHS_EINVAL, "sparse_attn_noalloc: null pointer argument");
   if (cap <= 0) return abi_fail(PRHS_EINVAL, "sparse_attn_noalloc: cap must be positive");
+  if ((long long)kv->B * kv->Hq * cap >= (1ll << 30))
+    return abi_fail(PRHS_EUNSUPPORTED, "sparse_attn_noalloc: B * Hq * cap above 2^30 rows");
   unsigned* err = nullptr;
   int sms = 0;
   if ((s = abi_device(&err, &sms)) != PRHS_OK) return s;
@@ -95,6 +97,7 @@ extern "C" prhs_status prhs_sparse_attn_noalloc(const prhs_kv* kv, const void* q
   a.counters = static_cast<unsigned*>(scratch);
   a.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + tickets);
   a.ctas = ctas;
+  a.min_rows = ATTN_MIN_ROWS;
   e = launch_attn(a, true, stream);
   if (e != cudaSuccess) return abi_fail(PRHS_ECUDA, cudaGetErrorString(e));
   return PRHS_OK;

@@ -23,7 +23,7 @@
  *    skipped, nothing faults. prhs_last_error() synchronises the device,
  *    reads and clears that word.
  *  - Layouts (row-major, innermost last):
- *      q, q_anchor   [B][Hq][d]      same element type as the cache
+ *      q, q_anchor   [B][Hq][d]      same element type as the cache, 16-byte aligned
  *      K, V          contiguous [B][Hkv][t_max][d]
  *                    or paged   [num_blocks][Hkv][block_size][d]
  *      idx           [B][Hq][cap]    int32, ascending, n_sel valid entries

@@ -290,6 +290,7 @@ prhs_status check_select_args(const prhs_kv& kv, const void* q, int N, const int
                               void* q_anchor) {
   if (q == nullptr || idx == nullptr || n_sel == nullptr || delta == nullptr)
     return fail(PRHS_EINVAL, "q, idx, n_sel and delta must be non-null");
+  if (!aligned16(q) || !aligned16(q_anchor)) return fail(PRHS_EINVAL, "q and q_anchor must be 16-byte aligned");
   if (n_budget == nullptr && N <= 0) return fail(PRHS_EINVAL, "N must be positive (got %d)", N);
   if (cap <= 0) return fail(PRHS_EINVAL, "cap must be positive");
   const int tmax = t_max_of(kv);
@@ -306,7 +307,8 @@ prhs_status check_select_args(const prhs_kv& kv, const void* q, int N, const int
 prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws, const void* q,
                     float scale, const int32_t* idx, const int32_t* n_sel, int cap, float* out,
                     float* lse, bool sparse, cudaStream_t st, const uint8_t* unit_mask = nullptr,
-                    int mask_want = 0, bool second_region = false, int max_ctas = 0) {
+                    int mask_want = 0, bool second_region = false, int max_ctas = 0,
+                    int min_rows = ATTN_MIN_ROWS) {
   // the kernels index the concatenated rows of all units with 32-bit integers
   if ((long long)kv.B * kv.Hq * (sparse ? cap : t_max_of(kv)) >= (1ll << 30))
     return fail(PRHS_EUNSUPPORTED, "B * Hq * %s = %lld rows above 2^30", sparse ? "cap" : "t_max",
@@ -325,7 +327,7 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
   a.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + (second_region ? L.partials2 : L.partials));
   a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.counters);
   a.ctas = attn_ctas(kv, sparse, cap, di->sms);
-  a.min_rows = ATTN_MIN_ROWS;
+  a.min_rows = min_rows;
   if (max_ctas > 0 && a.ctas > max_ctas) a.ctas = max_ctas;
   return launch_result(launch_attn(a, sparse, st), sparse ? "sparse attention" : "dense attention");
 }
@@ -419,6 +421,7 @@ prhs_status prhs_score(const prhs_kv* kv, const void* q, float scale, const uint
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
   if (q == nullptr) return fail(PRHS_EINVAL, "q must be non-null");
+  if (!aligned16(q)) return fail(PRHS_EINVAL, "q must be 16-byte aligned");
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
   Layout L;
@@ -449,6 +452,8 @@ prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx, const 
                             uint8_t* reuse, cudaStream_t stream) {
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
+  if ((q && !aligned16(q)) || (q_anchor && !aligned16(q_anchor)))
+    return fail(PRHS_EINVAL, "q and q_anchor must be 16-byte aligned");
   if (!anchor_idx || !anchor_n || !q || !q_anchor || !idx || !n_sel || !reuse)
     return fail(PRHS_EINVAL, "cis: null pointer argument");
   if (w < 0) return fail(PRHS_EINVAL, "w must be >= 0 (got %d)", w);
@@ -469,6 +474,7 @@ prhs_status prhs_sparse_attn(const prhs_kv* kv, const void* q, float scale, cons
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
   if (!q || !idx || !n_sel || !out || !lse) return fail(PRHS_EINVAL, "sparse: null pointer argument");
+  if (!aligned16(q)) return fail(PRHS_EINVAL, "q must be 16-byte aligned");
   if (cap <= 0) return fail(PRHS_EINVAL, "cap must be positive");
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
@@ -482,6 +488,7 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
   if (!q || !out || !lse) return fail(PRHS_EINVAL, "dense: null pointer argument");
+  if (!aligned16(q)) return fail(PRHS_EINVAL, "q must be 16-byte aligned");
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
   Layout L;
@@ -511,6 +518,7 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if (s != PRHS_OK) return s;
   if (!q || !anchor_idx || !anchor_n || !q_anchor || !idx || !n_sel || !reuse || !delta || !out || !lse)
     return fail(PRHS_EINVAL, "decode: null pointer argument");
+  if (!aligned16(q) || !aligned16(q_anchor)) return fail(PRHS_EINVAL, "q and q_anchor must be 16-byte aligned");
   if (n_budget == nullptr && N <= 0) return fail(PRHS_EINVAL, "N must be positive (got %d)", N);
   if (w < 0) return fail(PRHS_EINVAL, "w must be >= 0 (got %d)", w);
   if (max_run < 0) return fail(PRHS_EINVAL, "max_run must be >= 0 (got %d)", max_run);
@@ -536,7 +544,7 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if (e == cudaSuccess) e = cudaStreamWaitEvent(di->side, di->fork, 0);
   if (e != cudaSuccess) return cuda_fail(e, "decode: fork");
   if ((s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, di->side, reuse, 1,
-                   true)) != PRHS_OK)
+                   true, 0, ATTN_SIDE_MIN_ROWS)) != PRHS_OK)
     return s;
   if ((s = do_score_select(*kv, di, L, ws, q, scale, N, n_budget, reuse, idx, n_sel, cap, delta,
                            anchor_idx, anchor_n, anchor_cap, q_anchor, stream)) != PRHS_OK)

@@ -29,6 +29,14 @@ namespace prhs {
 
 constexpr int ATTN_THREADS = 128;
 constexpr int ATTN_IDX_STAGE = 2048;
+constexpr int MERGE_CH = 32;  // partial records merged per shared-memory pass
+constexpr int ATTN_ALIGN_UNITS = 2048;  // most units for the unit-aligned split
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  return v;
+}
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -62,13 +70,16 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
   constexpr int STEP = 16 * UNROLL;  // rows per CTA iteration
   constexpr int PW = D + 4;          // partial record: m, l, 2 pad, o[D] (16-byte aligned)
   static_assert(D <= ATTN_THREADS && D % 64 == 0, "merge maps one thread per output element");
-  extern __shared__ int sh_prefix[];  // [units + 1]
-  __shared__ int sh_idx[SPARSE ? ATTN_IDX_STAGE : 1];
+  // one buffer: the row numbers of a segment, or a chunk of partial records
+  // while a unit is merged
+  constexpr int BUF_FLOATS = (SPARSE && ATTN_IDX_STAGE > MERGE_CH * PW) ? ATTN_IDX_STAGE : MERGE_CH * PW;
+  // [units + 1] row prefix, then (aligned split) [units + 1] CTA prefix
+  extern __shared__ int sh_prefix[];
+  __shared__ __align__(16) float sh_buf[BUF_FLOATS];
+  int* const sh_idx = reinterpret_cast<int*>(sh_buf);
   __shared__ float sm_m[4][G], sm_l[4][G];
   __shared__ float sm_o[4][G][D];
-  __shared__ int sh_wsum[ATTN_THREADS / 32];
-  __shared__ float sh_red[ATTN_THREADS / 32];
-  __shared__ float sh_w[ATTN_THREADS];
+  __shared__ int sh_wsum[ATTN_THREADS / 32], sh_wact[ATTN_THREADS / 32];
   __shared__ int sh_last;
 
   pdl_wait();
@@ -83,11 +94,44 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
   const int C = gridDim.x, c = blockIdx.x;
   const int group = kv.Hq / kv.Hkv;
 
+  // Exclusive prefix over units of per-unit counts: thread tid owns units
+  // [u0, u0 + per_t), whose counts are in arr[] on entry; also returns the
+  // number of units with a non-zero count. Ends with a barrier.
+  const int per_t = (U + ATTN_THREADS - 1) / ATTN_THREADS;
+  const int u0 = tid * per_t;
+  auto block_scan = [&](int* arr, int loc, int act) -> int {
+    int v = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, v, o);
+      if (lane >= o) v += y;
+    }
+    act = warp_sum_int(act);
+    if (lane == 31) sh_wsum[warp] = v;
+    if (lane == 0) sh_wact[warp] = act;
+    __syncthreads();
+    int before = 0, nact = 0;
+    for (int w = 0; w < ATTN_THREADS / 32; w++) {
+      if (w < warp) before += sh_wsum[w];
+      nact += sh_wact[w];
+    }
+    int run = before + v - loc;
+    for (int k = 0; k < per_t; k++) {
+      const int u = u0 + k;
+      if (u >= U) break;
+      const int r = arr[u];
+      arr[u] = run;
+      run += r;
+    }
+    if (tid == ATTN_THREADS - 1) arr[U] = run;
+    __syncthreads();
+    return nact;
+  };
+
   // ---- rows per unit and their prefix sums (every CTA computes the same) ----
+  int nact;
   {
-    const int per_t = (U + ATTN_THREADS - 1) / ATTN_THREADS;
-    const int u0 = tid * per_t;
-    int loc = 0;
+    int loc = 0, act = 0;
     for (int k = 0; k < per_t; k++) {
       const int u = u0 + k;
       if (u >= U) break;
@@ -105,27 +149,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
       }
       sh_prefix[u] = r;  // temporarily the count
       loc += r;
+      act += r > 0;
     }
-    int v = loc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(FULL_MASK, v, o);
-      if (lane >= o) v += y;
-    }
-    if (lane == 31) sh_wsum[warp] = v;
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp; w++) before += sh_wsum[w];
-    int run = before + v - loc;
-    for (int k = 0; k < per_t; k++) {
-      const int u = u0 + k;
-      if (u >= U) break;
-      const int r = sh_prefix[u];
-      sh_prefix[u] = run;
-      run += r;
-    }
-    if (tid == ATTN_THREADS - 1) sh_prefix[U] = run;
-    __syncthreads();
+    nact = block_scan(sh_prefix, loc, act);
   }
   const int total = sh_prefix[U];
 
@@ -140,25 +166,38 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
     }
   }
   if (total == 0) return;
-  const int per = max((total + C - 1) / C, max(a.min_rows, 1));
-  const int lo = c * per, hi = min(total, lo + per);
-  if (lo >= hi) return;
 
-  // first unit with rows overlapping [lo, hi): largest u with P[u] <= lo
-  int ulo = 0, uhi = U - 1;
-  while (ulo < uhi) {
-    const int mid = (ulo + uhi + 1) >> 1;
-    if (sh_prefix[mid] <= lo) ulo = mid; else uhi = mid - 1;
+  // ---- the split ----
+  // Aligned (few active units): every CTA takes rows of one unit only, unit u
+  // getting ceil(rows_u / per) CTAs with its rows shared evenly; with per =
+  // ceil(total / (C - nact)) those counts add up to at most C. Otherwise the
+  // concatenated rows are cut into C equal ranges, and a CTA may cover the
+  // end of one unit and the start of the next.
+  const int min_rows = max(a.min_rows, 1);
+  const bool aligned = U <= ATTN_ALIGN_UNITS && 2 * nact <= C;
+  int per;
+  int* const sh_cpre = sh_prefix + (U + 1);
+  if (aligned) {
+    per = max(min_rows, (total + (C - nact) - 1) / (C - nact));
+    int loc = 0;
+    for (int k = 0; k < per_t; k++) {
+      const int u = u0 + k;
+      if (u >= U) break;
+      const int n = (sh_prefix[u + 1] - sh_prefix[u] + per - 1) / per;
+      sh_cpre[u] = n;
+      loc += n;
+    }
+    block_scan(sh_cpre, loc, 0);
+  } else {
+    per = max((total + C - 1) / C, min_rows);
   }
 
   const char* kbase = static_cast<const char*>(kv.k);
   const char* vbase = static_cast<const char*>(kv.v);
   const float qscale = a.scale * LOG2E;
 
-  for (int u = ulo; u < U && sh_prefix[u] < hi; u++) {
-    const int P0 = sh_prefix[u], P1 = sh_prefix[u + 1];
-    const int r0 = max(lo, P0) - P0, r1 = min(hi, P1) - P0;
-    if (r0 >= r1) continue;
+  // Rows [r0, r1) of unit u, one of the CTAs cf..cl that cover it.
+  auto process = [&](const int u, const int r0, const int r1, const int cf, const int cl) {
     int b, kvh, qh0;
     if (PER_QUERY) {
       b = u / kv.Hq;
@@ -171,15 +210,31 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
     }
     const int t = seq_len(kv, b);
 
-    float qf[G][S::EL];
+    // the query's 16-byte pieces and the first segment's row numbers are
+    // requested together
+    uint4 qraw[G][S::CPL];
 #pragma unroll
     for (int g = 0; g < G; g++)
 #pragma unroll
       for (int cc = 0; cc < S::CPL; cc++)
+        qraw[g][cc] = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.q) +
+                                                           ((long long)(qh0 + g) * D) * sizeof(T)) +
+                            cc * 8 + j);
+    const int32_t* rows = SPARSE ? a.idx + (long long)u * a.cap : nullptr;
+    if (SPARSE) {
+      __syncthreads();  // earlier readers of the buffer are done
+      const int se0 = min(r1, r0 + ATTN_IDX_STAGE);
+      for (int x = tid; x < se0 - r0; x += ATTN_THREADS) sh_idx[x] = rows[r0 + x];
+      __syncthreads();
+    }
+    float qf[G][S::EL];
 #pragma unroll
-        for (int e = 0; e < S::EPC; e++)
-          qf[g][cc * S::EPC + e] =
-              Elem<T>::load1(a.q, (long long)(qh0 + g) * D + (cc * 8 + j) * S::EPC + e) * qscale;
+    for (int g = 0; g < G; g++) {
+#pragma unroll
+      for (int cc = 0; cc < S::CPL; cc++) Elem<T>::unpack(qraw[g][cc], qf[g] + cc * S::EPC);
+#pragma unroll
+      for (int e = 0; e < S::EL; e++) qf[g][e] *= qscale;
+    }
     float m[G], l[G], o[G][S::EL];
 #pragma unroll
     for (int g = 0; g < G; g++) {
@@ -189,10 +244,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
       for (int e = 0; e < S::EL; e++) o[g][e] = 0.f;
     }
 
-    const int32_t* rows = SPARSE ? a.idx + (long long)u * a.cap : nullptr;
     for (int sb = r0; sb < r1; sb += (SPARSE ? ATTN_IDX_STAGE : (r1 - r0))) {
       const int se = SPARSE ? min(r1, sb + ATTN_IDX_STAGE) : r1;
-      if (SPARSE) {
+      if (SPARSE && sb != r0) {
         __syncthreads();
         for (int x = tid; x < se - sb; x += ATTN_THREADS) sh_idx[x] = rows[sb + x];
         __syncthreads();
@@ -305,7 +359,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
     }
     __syncthreads();
 
-    const int cf = P0 / per, cl = (P1 - 1) / per;  // CTAs covering this unit
     if (cf == cl) {
       // the whole unit is in this CTA: final result
       for (int x = tid; x < G * D; x += ATTN_THREADS) {
@@ -325,7 +378,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
         a.out[(long long)(qh0 + g) * D + e] = L > 0.f ? O / L : 0.f;
         if (e == 0) a.lse[qh0 + g] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
       }
-      continue;
+      return;
     }
     for (int x = tid; x < G * D; x += ATTN_THREADS) {
       const int g = x / D, e = x % D;
@@ -352,76 +405,73 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
     __syncthreads();
     if (tid == 0) sh_last = atomicAdd(&a.counters[u], 1u) == (unsigned)(cl - cf);
     __syncthreads();
-    if (!sh_last) continue;
+    if (!sh_last) return;
     __threadfence();
-    // Merge the ncov partial records of this unit with the whole block: one
-    // parallel pass for the largest max, then per chunk of ATTN_THREADS
-    // records the weights 2^(m_i - M) in shared memory and, warp by warp,
-    // the weighted rows o_i (each lane a 16-byte slice, the loads of a warp
-    // independent of one another).
+    // Merge the ncov partial records of this unit: chunks of MERGE_CH records
+    // are copied to shared memory by the whole block in one pass (16-byte
+    // loads, all independent), then folded into a running (M, L, O) state,
+    // thread e owning output element e.
     const int ncov = cl - cf + 1;
-    constexpr int EPL = D / 32;  // output elements per lane
+    constexpr int V4 = PW / 4;  // 16-byte pieces per record
     for (int g = 0; g < G; g++) {
       const float* rec0 = a.partials + ((long long)(cf + u) * G + g) * PW;
       const long long RS = (long long)G * PW;  // floats between consecutive records
-      float mx = -INFINITY;
-      for (int i = tid; i < ncov; i += ATTN_THREADS) mx = fmaxf(mx, __ldcg(rec0 + i * RS));
-      mx = warp_max(mx);
-      if (lane == 0) sh_red[warp] = mx;
-      __syncthreads();
-      float M = sh_red[0];
-#pragma unroll
-      for (int w = 1; w < ATTN_THREADS / 32; w++) M = fmaxf(M, sh_red[w]);
-      float Lp = 0.f;
-      float acc[EPL];
-#pragma unroll
-      for (int e = 0; e < EPL; e++) acc[e] = 0.f;
-      for (int i0 = 0; i0 < ncov; i0 += ATTN_THREADS) {
-        const int nb = min(ATTN_THREADS, ncov - i0);
-        __syncthreads();  // sh_w and sh_red of the previous round consumed
-        if (tid < nb) {
-          const float* r = rec0 + (i0 + tid) * RS;
-          const float wgt = M == -INFINITY ? 0.f : exp2f(__ldcg(r) - M);
-          sh_w[tid] = wgt;
-          Lp += wgt * __ldcg(r + 1);
+      float M = -INFINITY, L = 0.f, O = 0.f;
+      for (int i0 = 0; i0 < ncov; i0 += MERGE_CH) {
+        const int nb = min(MERGE_CH, ncov - i0);
+        __syncthreads();  // the buffer is free
+        for (int x = tid; x < nb * V4; x += ATTN_THREADS) {
+          const int i = x / V4, k = x % V4;
+          reinterpret_cast<float4*>(sh_buf)[x] =
+              __ldcg(reinterpret_cast<const float4*>(rec0 + (i0 + i) * RS) + k);
         }
         __syncthreads();
-#pragma unroll 4
-        for (int i = warp; i < nb; i += ATTN_THREADS / 32) {
-          const float wgt = sh_w[i];
-          const float* o = rec0 + (i0 + i) * RS + 4 + lane * EPL;
-          if constexpr (EPL == 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
-            acc[0] = fmaf(wgt, v.x, acc[0]);
-            acc[1] = fmaf(wgt, v.y, acc[1]);
-            acc[2] = fmaf(wgt, v.z, acc[2]);
-            acc[3] = fmaf(wgt, v.w, acc[3]);
-          } else {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
-            acc[0] = fmaf(wgt, v.x, acc[0]);
-            acc[1] = fmaf(wgt, v.y, acc[1]);
+        float mc = M;
+        for (int i = 0; i < nb; i++) mc = fmaxf(mc, sh_buf[i * PW]);
+        if (mc != -INFINITY) {
+          const float r = exp2f(M - mc);  // 0 while M is still -inf
+          L *= r;
+          O *= r;
+          for (int i = 0; i < nb; i++) {
+            const float wgt = exp2f(sh_buf[i * PW] - mc);
+            L = fmaf(wgt, sh_buf[i * PW + 1], L);
+            if (tid < D) O = fmaf(wgt, sh_buf[i * PW + 4 + tid], O);
           }
+          M = mc;
         }
       }
-      Lp = warp_sum(Lp);
-      __syncthreads();  // every warp done with sh_w and sh_red
-      if (lane == 0) sh_red[warp] = Lp;
-#pragma unroll
-      for (int e = 0; e < EPL; e++) sm_o[warp][0][lane * EPL + e] = acc[e];
-      __syncthreads();
       if (tid < D) {
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < ATTN_THREADS / 32; w++) {
-          L += sh_red[w];
-          O += sm_o[w][0][tid];
-        }
         a.out[(long long)(qh0 + g) * D + tid] = L > 0.f ? O / L : 0.f;
         if (tid == 0) a.lse[qh0 + g] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
       }
-      __syncthreads();  // sm_o and sh_red free for the next query head or unit
     }
     if (tid == 0) a.counters[u] = 0u;
+  };
+
+  if (aligned) {
+    if (c >= sh_cpre[U]) return;  // more CTAs than the split needs
+    int ulo = 0, uhi = U - 1;     // the unit: largest u with CP[u] <= c
+    while (ulo < uhi) {
+      const int mid = (ulo + uhi + 1) >> 1;
+      if (sh_cpre[mid] <= c) ulo = mid; else uhi = mid - 1;
+    }
+    const int cf = sh_cpre[ulo], n = sh_cpre[ulo + 1] - cf, k = c - cf;
+    const int ru = sh_prefix[ulo + 1] - sh_prefix[ulo];
+    process(ulo, (int)((long long)k * ru / n), (int)((long long)(k + 1) * ru / n), cf, cf + n - 1);
+    return;
+  }
+  const int lo = c * per, hi = min(total, lo + per);
+  if (lo >= hi) return;
+  // first unit with rows overlapping [lo, hi): largest u with P[u] <= lo
+  int ulo = 0, uhi = U - 1;
+  while (ulo < uhi) {
+    const int mid = (ulo + uhi + 1) >> 1;
+    if (sh_prefix[mid] <= lo) ulo = mid; else uhi = mid - 1;
+  }
+  for (int u = ulo; u < U && sh_prefix[u] < hi; u++) {
+    const int P0 = sh_prefix[u], P1 = sh_prefix[u + 1];
+    const int r0 = max(lo, P0) - P0, r1 = min(hi, P1) - P0;
+    if (r0 < r1) process(u, r0, r1, P0 / per, (P1 - 1) / per);
   }
 }
 
@@ -436,7 +486,8 @@ size_t attn_partial_floats(const KVView& kv, bool sparse, int ctas) {
 
 template <typename T, int D, int G, bool SPARSE>
 static cudaError_t attn_go(const AttnLaunch& a, cudaStream_t st) {
-  const size_t smem = ((size_t)attn_units(a.kv, SPARSE) + 1) * sizeof(int);
+  const size_t units = (size_t)attn_units(a.kv, SPARSE);
+  const size_t smem = (units + 1) * sizeof(int) * (units <= (size_t)ATTN_ALIGN_UNITS ? 2 : 1);
   auto k = attn_kernel<T, D, G, SPARSE>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -72,6 +72,10 @@ struct CisLaunch {
 // fixed per-CTA cost (prefix, index staging, partial record, merge) outweighs
 // the extra parallelism.
 constexpr int ATTN_MIN_ROWS = 64;
+// The same floor for the reusing heads' branch of a decode step, which runs
+// beside the retrieving heads' scoring and selection: when the reused sets
+// are small, fewer and fuller CTAs leave room on the SMs for those kernels.
+constexpr int ATTN_SIDE_MIN_ROWS = 192;
 
 struct AttnLaunch {
   KVView kv;

@@ -59,6 +59,8 @@ extern "C" prhs_status prhs_sparse_attn_noalloc(const prhs_kv* kv, const void* q
   if (s != PRHS_OK) return s;
   if (!q || !idx || !n_sel || !out || !lse)
     return abi_fail(PRHS_EINVAL, "sparse_attn_noalloc: null pointer argument");
+  if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0)
+    return abi_fail(PRHS_EINVAL, "sparse_attn_noalloc: q must be 16-byte aligned");
   if (cap <= 0) return abi_fail(PRHS_EINVAL, "sparse_attn_noalloc: cap must be positive");
   if ((long long)kv->B * kv->Hq * cap >= (1ll << 30))
     return abi_fail(PRHS_EUNSUPPORTED, "sparse_attn_noalloc: B * Hq * cap above 2^30 rows");

@@ -108,6 +108,52 @@ def test_sparse_attn_on_oracle_sets(name):
         assert abs(l[b, h] - rl) <= LSE_TOL, (b, h)
 
 
+@pytest.mark.parametrize("B,Hq,t,live,nmax", [
+    (2, 4, 1500, 1, 1400),     # one head with rows: each CTA takes part of that head
+    (2, 4, 1500, 8, 1400),     # every head, long sets: CTAs aligned to heads
+    (8, 32, 300, 256, 40),     # many heads with short sets: CTAs straddle heads
+    (65, 32, 64, 2080, 20),    # more heads than the head-aligned split handles
+])
+def test_sparse_attn_split_modes(B, Hq, t, live, nmax):
+    """Both ways of cutting the rows over CTAs, and the merge of split heads."""
+    import sparse_kv_selection_gb300 as S
+    from workloads.torch_io import upload
+    wl = make_workload("split", dtype="bf16", B=B, Hq=Hq, Hkv=Hq, d=128, t=t, n_clusters=2,
+                       steps=1, N=8, w=1, seed=3)
+    dev = upload(wl)
+    kv = S.KVCache(dev["k"], dev["v"], dev["seq_lens"], wl.Hq)
+    rng = np.random.default_rng(11)
+    cap = nmax
+    idx = np.zeros((B, Hq, cap), np.int32)
+    n = np.zeros((B, Hq), np.int32)
+    sets = {}
+    for u in range(B * Hq):
+        b, h = divmod(u, Hq)
+        if u >= live:
+            continue
+        k = int(rng.integers(1, min(nmax, t) + 1))
+        Sx = np.sort(rng.choice(t, size=k, replace=False))
+        sets[(b, h)] = Sx
+        idx[b, h, :k] = Sx
+        n[b, h] = k
+    out = torch.full((B, Hq, wl.d), 7.0, device="cuda")
+    lse = torch.full((B, Hq), 7.0, device="cuda")
+    ws = S.make_workspace(kv, cap)
+    for rep in range(2):  # tickets must be back at zero for the second call
+        S.sparse_attn(kv, dev["q"][0], wl.scale, torch.from_numpy(idx).cuda(),
+                      torch.from_numpy(n).cuda(), out, lse, ws)
+        o, l = out.cpu().numpy(), lse.cpu().numpy()
+        for u in range(B * Hq):
+            b, h = divmod(u, Hq)
+            if (b, h) not in sets:
+                assert (o[b, h] == 0).all() and l[b, h] == -math.inf, (b, h)
+                continue
+            K, V = kv_rows64(wl, b, h)
+            ro, rl = P.attention(q64(wl, 0, b, h), K, V, sets[(b, h)], wl.scale)
+            assert np.abs(o[b, h] - ro).max() <= OUT_TOL, (rep, b, h)
+            assert abs(l[b, h] - rl) <= LSE_TOL, (rep, b, h)
+
+
 def test_sparse_attn_edge_sets():
     """Empty set, single key, every key, last key, repeated calls."""
     S, wl, dev, kv = _setup("mha_bf16_ragged")

@@ -172,6 +172,22 @@ int attn_ctas(const prhs_kv& kv, bool sparse, int cap, int sms) {
   return c < 1 ? 1 : (int)c;
 }
 
+// CTAs per query head of the cluster attention kernel, or 0 for the balanced
+// kernel. Clusters pay off when the whole launch is small (at most 256 rows
+// per CTA slot, rows_hint rows per head at most) and the heads are few enough
+// that each can have at least two CTAs within ATTN_CTAS_PER_SM CTAs per SM;
+// then as many CTAs per head (a power of two up to ATTN_CLUSTER_MAX) as fit,
+// each with at least 64 of rows_hint rows. Large launches keep the balanced
+// kernel, which fills every SM whatever the number of heads.
+int attn_cluster_size(const prhs_kv& kv, int rows_hint, int sms) {
+  const long long units = (long long)kv.B * kv.Hq;
+  const long long slots = (long long)ATTN_CTAS_PER_SM * sms;
+  if (units * 2 > slots || units * rows_hint > slots * 256) return 0;
+  int cl = 1;
+  while (cl * 2 <= ATTN_CLUSTER_MAX && units * cl * 2 <= slots && rows_hint >= 64ll * cl * 2) cl *= 2;
+  return cl;
+}
+
 struct Layout {
   size_t counters, partials, partials2, scores, total;
 };
@@ -308,7 +324,7 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
                     float scale, const int32_t* idx, const int32_t* n_sel, int cap, float* out,
                     float* lse, bool sparse, cudaStream_t st, const uint8_t* unit_mask = nullptr,
                     int mask_want = 0, bool second_region = false, int max_ctas = 0,
-                    int min_rows = ATTN_MIN_ROWS) {
+                    int min_rows = ATTN_MIN_ROWS, int rows_hint = 0) {
   // the kernels index the concatenated rows of all units with 32-bit integers
   if ((long long)kv.B * kv.Hq * (sparse ? cap : t_max_of(kv)) >= (1ll << 30))
     return fail(PRHS_EUNSUPPORTED, "B * Hq * %s = %lld rows above 2^30", sparse ? "cap" : "t_max",
@@ -328,6 +344,7 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
   a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.counters);
   a.ctas = attn_ctas(kv, sparse, cap, di->sms);
   a.min_rows = min_rows;
+  a.cluster = sparse ? attn_cluster_size(kv, rows_hint > 0 ? rows_hint : cap, di->sms) : 0;
   if (max_ctas > 0 && a.ctas > max_ctas) a.ctas = max_ctas;
   return launch_result(launch_attn(a, sparse, st), sparse ? "sparse attention" : "dense attention");
 }
@@ -549,8 +566,9 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if ((s = do_score_select(*kv, di, L, ws, q, scale, N, n_budget, reuse, idx, n_sel, cap, delta,
                            anchor_idx, anchor_n, anchor_cap, q_anchor, stream)) != PRHS_OK)
     return s;
+  // the retrieving heads' sets hold at most anchor_cap rows
   if ((s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, stream, reuse, 0,
-                   false)) != PRHS_OK)
+                   false, 0, ATTN_MIN_ROWS, anchor_cap)) != PRHS_OK)
     return s;
   e = cudaEventRecord(di->join, di->side);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, di->join, 0);

@@ -503,6 +503,7 @@ static cudaError_t attn_dispatch(const AttnLaunch& a, bool sparse, cudaStream_t 
 }
 
 cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t st) {
+  if (sparse && a.cluster > 0) return launch_attn_cluster(a, st);
   if (a.kv.dtype == PRHS_BF16) {
     if (a.kv.d == 128) return attn_dispatch<__nv_bfloat16, 128>(a, sparse, st);
     if (a.kv.d == 64) return attn_dispatch<__nv_bfloat16, 64>(a, sparse, st);

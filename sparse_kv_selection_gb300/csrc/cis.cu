@@ -40,19 +40,20 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   const int d = kv.d;
   constexpr int CHUNK = CIS_THREADS * CIS_PER;
 
-  // every input of the first chunk is requested before any result is used
+  // every input of the first chunk is requested before any result is used:
+  // the anchor row is read up to its capacity, whatever anchor_n turns out
+  // to be, and the entries past anchor_n are ignored below
   int n = a.anchor_n[qh];
   const int age = a.anchor_age != nullptr ? a.anchor_age[qh] : 0;
   const int t = seq_len(kv, b);
   const int32_t* anc = a.anchor_idx + (long long)qh * a.anchor_cap;
-  const int ncap = min(n, a.anchor_cap);
   int x[CIS_PER];
   int prev0;
   {
     const int j0 = tid * CIS_PER;
 #pragma unroll
-    for (int k = 0; k < CIS_PER; k++) x[k] = j0 + k < ncap ? anc[j0 + k] : 0;
-    prev0 = j0 > 0 && j0 - 1 < ncap ? anc[j0 - 1] : -1;
+    for (int k = 0; k < CIS_PER; k++) x[k] = j0 + k < a.anchor_cap ? anc[j0 + k] : 0;
+    prev0 = j0 > 0 && j0 - 1 < a.anchor_cap ? anc[j0 - 1] : -1;
   }
   double dot = 0.0, nq = 0.0, na = 0.0;
   for (int i = tid; i < d; i += CIS_THREADS) {

@@ -92,6 +92,7 @@ struct AttnLaunch {
   unsigned* counters;    // [units], zero on entry, left zero
   int ctas;              // CTAs sharing the rows of all units
   int min_rows;          // fewest rows a CTA takes (fewer CTAs join small batches)
+  int cluster = 0;       // sparse only: > 0 runs the cluster kernel with this many CTAs per head
 };
 
 // Units of the attention split (query heads when sparse, KV heads when dense)
@@ -104,6 +105,10 @@ cudaError_t launch_select(const SelectLaunch& a, cudaStream_t s);
 cudaError_t launch_select_global(const SelectLaunch& a, cudaStream_t s);
 cudaError_t launch_cis(const CisLaunch& a, cudaStream_t s);
 cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t s);
+// Sparse attention with one thread-block cluster of a.cluster CTAs per query
+// head (batches with few heads; no workspace).
+constexpr int ATTN_CLUSTER_MAX = 8;
+cudaError_t launch_attn_cluster(const AttnLaunch& a, cudaStream_t s);
 
 // Hooks into the C ABI layer for the library's other entry-point files:
 // descriptor checks, per-device facts (error word, SM count), the failure

@@ -122,7 +122,9 @@ prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* 
                         void* q_anchor, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Critical-index-set reuse with dilation (Fig. 2, Fig. 4, Fig. 8, Table VIII).
- * Per query head: c = <q, q_anchor> / (|q| |q_anchor|) evaluated in float64;
+ * Per query head: c = <q, q_anchor> / (|q| |q_anchor|); the decision is the
+ * one of that formula in float64 (an fp32 estimate decides when it is more
+ * than 1e-4 away from tau, its error being below 2e-6; float64 otherwise);
  * reuse = anchor_n > 0 and |q| |q_anchor| > 0 and c >= tau, and, when
  * max_run > 0, anchor_age < max_run - 1: the CIS block size s of Tables IV,
  * V and VIII read as the most consecutive queries one retrieval serves.

@@ -10,10 +10,10 @@
 // set size ignored) in one round trip. The gather is the one of the balanced
 // kernel: eight lanes per row, 16-byte streaming loads, fp32 online softmax
 // in base 2. Each CTA folds its four warps into one partial state (m, l, o)
-// in shared memory; after a cluster barrier CTA 0 reads the CL partial states
-// through distributed shared memory and writes out and lse, and a second
-// barrier keeps every CTA's shared memory alive until it has. No workspace
-// and no global-memory round trip take part in the merge.
+// and stores it into CTA 0's shared memory through distributed shared
+// memory; after one cluster barrier CTA 0 merges the CL states from its own
+// shared memory and writes out and lse. No workspace and no global-memory
+// round trip take part in the merge.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(ACL_THREADS, 4) attn_cluster_kernel(const Attn
   __shared__ int sh_idx[ACL_STAGE];
   __shared__ float sm_m[4], sm_l[4];
   __shared__ float sm_o[4][D];
-  __shared__ float part[D + 2];  // this CTA's state: m, l, o[D]
+  __shared__ float part[ATTN_CLUSTER_MAX][D + 2];  // CTA 0: every CTA's state m, l, o[D]
 
   pdl_wait();
   pdl_trigger();
@@ -206,34 +206,35 @@ __global__ void __launch_bounds__(ACL_THREADS, 4) attn_cluster_kernel(const Attn
       a.out[(long long)u * D + tid] = L > 0.f ? O / L : 0.f;
       if (tid == 0) a.lse[u] = L > 0.f ? (M + log2f(L)) * ACL_LN2 : -INFINITY;
     } else {
-      part[2 + tid] = O;
+      // this CTA's state into row `rank` of CTA 0's table
+      cg::cluster_group cluster = cg::this_cluster();
+      float* dst = cluster.map_shared_rank(&part[0][0], 0) + rank * (D + 2);
+      dst[2 + tid] = O;
       if (tid == 0) {
-        part[0] = M;
-        part[1] = L;
+        dst[0] = M;
+        dst[1] = L;
       }
     }
   }
   if (CL == 1) return;
 
-  // ---- merge of the cluster's states through distributed shared memory ----
+  // ---- CTA 0 merges the cluster's states from its own shared memory ----
   cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();
+  cluster.sync();  // every CTA's stores into CTA 0 are visible
   if (rank == 0 && tid < D) {
     float M = -INFINITY;
-    for (int r = 0; r < CL; r++) M = fmaxf(M, cluster.map_shared_rank(part, r)[0]);
+    for (int r = 0; r < CL; r++) M = fmaxf(M, part[r][0]);
     float L = 0.f, O = 0.f;
     if (M != -INFINITY) {
       for (int r = 0; r < CL; r++) {
-        const float* pr = cluster.map_shared_rank(part, r);
-        const float cw = exp2f(pr[0] - M);
-        L += cw * pr[1];
-        O += cw * pr[2 + tid];
+        const float cw = exp2f(part[r][0] - M);
+        L += cw * part[r][1];
+        O += cw * part[r][2 + tid];
       }
     }
     a.out[(long long)u * D + tid] = L > 0.f ? O / L : 0.f;
     if (tid == 0) a.lse[u] = L > 0.f ? (M + log2f(L)) * ACL_LN2 : -INFINITY;
   }
-  cluster.sync();  // CTA 0 has read every CTA's state
 }
 
 template <typename T, int D>

@@ -5,8 +5,14 @@
 // Table VIII (the shared set is dilated; radius r), and the CIS block size s
 // of Tables IV, V and VIII read as a bound on consecutive reuses.
 //
-// One CTA per query head. The gate is evaluated in float64 so that it takes
-// the same decision as a float64 reference. The dilated set
+// One CTA per query head. The gate takes the decision of the float64 formula
+// c = <q, q_a> / (sqrt(|q|^2) sqrt(|q_a|^2)) >= tau. Its first warp forms the
+// three sums in fp32 (bf16 products are exact in fp32; tree sums of d <= 128
+// terms stay within 8 roundings, so the fp32 cosine is within about 2e-6 of
+// the exact one) and decides from them when that cosine lies farther than
+// CIS_MARGIN = 1e-4 from tau; otherwise, or when a sum is not finite or a norm
+// is tiny, the same warp recomputes the sums and the ratio in float64. fp64 is
+// slow on this part, so the common case avoids it. The dilated set
 //   union_{a in anchor} [a - w, a + w] clipped to [0, t_b)
 // is produced without sorting: the anchor row is ascending, so interval j
 // contributes the positions after max(lo_j, hi_{j-1} + 1); a block-wide
@@ -25,10 +31,10 @@ __device__ __forceinline__ double warp_sum_f64(double v) {
 }
 
 constexpr int CIS_PER = 4;  // anchor entries per thread per chunk
+constexpr float CIS_MARGIN = 1e-4f;
 
 template <typename T>
 __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
-  __shared__ double red[3][CIS_THREADS / 32];
   __shared__ int sh_reuse;
   __shared__ int warp_tot[CIS_THREADS / 32];
   pdl_wait();
@@ -55,38 +61,46 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
     for (int k = 0; k < CIS_PER; k++) x[k] = j0 + k < a.anchor_cap ? anc[j0 + k] : 0;
     prev0 = j0 > 0 && j0 - 1 < a.anchor_cap ? anc[j0 - 1] : -1;
   }
-  double dot = 0.0, nq = 0.0, na = 0.0;
-  for (int i = tid; i < d; i += CIS_THREADS) {
-    const double u = (double)Elem<T>::load1(a.q, (long long)qh * d + i);
-    const double v = (double)Elem<T>::load1(a.q_anchor, (long long)qh * d + i);
-    dot = fma(u, v, dot);
-    nq = fma(u, u, nq);
-    na = fma(v, v, na);
-  }
-  if (warp * 32 < d) {  // only the warps that hold elements take part
-    dot = warp_sum_f64(dot);
-    nq = warp_sum_f64(nq);
-    na = warp_sum_f64(na);
+  if (warp == 0) {
+    float df = 0.f, qq = 0.f, aa = 0.f;
+    for (int i = lane; i < d; i += 32) {
+      const float u = Elem<T>::load1(a.q, (long long)qh * d + i);
+      const float v = Elem<T>::load1(a.q_anchor, (long long)qh * d + i);
+      df = fmaf(u, v, df);
+      qq = fmaf(u, u, qq);
+      aa = fmaf(v, v, aa);
+    }
+    df = warp_sum(df);
+    qq = warp_sum(qq);
+    aa = warp_sum(aa);
+    int pass = -1;  // -1: not decided in fp32
+    if (isfinite(df) && isfinite(qq) && isfinite(aa) && qq > 1e-30f && aa > 1e-30f) {
+      const float c = df * rsqrtf(qq) * rsqrtf(aa);
+      const float tf = (float)a.tau;
+      if (fabsf(c - tf) > CIS_MARGIN) pass = c > tf;
+    }
+    pass = __shfl_sync(FULL_MASK, pass, 0);  // one decision for the warp
+    if (pass < 0) {  // near the threshold: the float64 formula
+      double dot = 0.0, nq = 0.0, na = 0.0;
+      for (int i = lane; i < d; i += 32) {
+        const double u = (double)Elem<T>::load1(a.q, (long long)qh * d + i);
+        const double v = (double)Elem<T>::load1(a.q_anchor, (long long)qh * d + i);
+        dot = fma(u, v, dot);
+        nq = fma(u, u, nq);
+        na = fma(v, v, na);
+      }
+      dot = warp_sum_f64(dot);
+      nq = warp_sum_f64(nq);
+      na = warp_sum_f64(na);
+      const double den = sqrt(nq) * sqrt(na);
+      pass = den > 0.0 && dot / den >= a.tau;
+    }
     if (lane == 0) {
-      red[0][warp] = dot;
-      red[1][warp] = nq;
-      red[2][warp] = na;
+      const int reuse = n > 0 && pass && (a.max_run <= 0 || age < a.max_run - 1);
+      sh_reuse = reuse;
+      a.reuse[qh] = (uint8_t)reuse;
+      if (a.anchor_age != nullptr) a.anchor_age[qh] = reuse ? age + 1 : 0;
     }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    double D = 0, Q = 0, A = 0;
-    for (int w = 0; w * 32 < d && w < CIS_THREADS / 32; w++) {
-      D += red[0][w];
-      Q += red[1][w];
-      A += red[2][w];
-    }
-    const double den = sqrt(Q) * sqrt(A);
-    const int reuse = n > 0 && den > 0.0 && (D / den) >= a.tau &&
-                      (a.max_run <= 0 || age < a.max_run - 1);
-    sh_reuse = reuse;
-    a.reuse[qh] = (uint8_t)reuse;
-    if (a.anchor_age != nullptr) a.anchor_age[qh] = reuse ? age + 1 : 0;
   }
   __syncthreads();
   if (!sh_reuse) return;

@@ -375,6 +375,41 @@ def test_cis_dilate(dtype, d):
                 assert gn[b, h] == -4 and (gi[b, h] == -4).all()
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+@pytest.mark.parametrize("gap", [1e-3, 2e-4, 5e-5, 1e-6, 1e-9, 1e-11])
+def test_cis_gate_near_threshold(dtype, d, gap):
+    """tau placed `gap` below or above each head's float64 cosine: gaps past
+    1e-4 are decided from the fp32 sums, nearer ones by the float64 formula;
+    every decision must be the oracle's."""
+    import sparse_kv_selection_gb300 as S
+    from workloads import bf16_bits_from_f32
+    from workloads.torch_io import tensor_of
+    rng = np.random.default_rng(17)
+    B, H, t, acap, w = 1, 16, 64, 4, 1
+    k = torch.zeros(B, H, t, d, dtype=torch.bfloat16 if dtype == "bf16" else torch.float32,
+                    device="cuda")
+    kv = S.KVCache(k, k, torch.full((B,), t, dtype=torch.int32, device="cuda"), H)
+    store = (lambda x: x.astype(np.float32)) if dtype == "f32" else bf16_bits_from_f32
+    q = rng.normal(size=(B, H, d)).astype(np.float32)
+    qa = (q + 0.6 * rng.normal(size=(B, H, d))).astype(np.float32)
+    qs, qas = store(q), store(qa)
+    cos = np.array([[P.cosine(P.widen(qs[0, h], dtype), P.widen(qas[0, h], dtype))
+                     for h in range(H)]])
+    an = np.full((B, H), acap, np.int32)
+    aidx = np.tile(np.arange(0, 4 * acap, 4, dtype=np.int32), (B, H, 1))
+    for sign in (-1.0, 1.0):
+        for h in range(H):
+            tau = float(cos[0, h] + sign * gap)
+            reuse = torch.full((B, H), 9, dtype=torch.uint8, device="cuda")
+            idx = torch.zeros((B, H, t), dtype=torch.int32, device="cuda")
+            n_sel = torch.zeros((B, H), dtype=torch.int32, device="cuda")
+            S.cis_dilate(kv, torch.from_numpy(aidx).cuda(), torch.from_numpy(an).cuda(),
+                         tensor_of(qs, dtype, "cuda"), tensor_of(qas, dtype, "cuda"), w, tau, idx,
+                         n_sel, reuse)
+            c, want = P.cis_gate(P.widen(qs[0, h], dtype), P.widen(qas[0, h], dtype), tau)
+            assert bool(reuse[0, h].item()) == want == (sign < 0), (h, sign, c, tau)
+
+
 # --------------------------------------------------------------------------- #
 # whole decode loop
 # --------------------------------------------------------------------------- #

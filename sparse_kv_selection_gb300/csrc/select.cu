@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
     vmax = fmaxf(vmax, s);
   }
   for (int i = tid; i < 2048; i += SEL_THREADS) sh.hist[i] = 0;
-  if (rank == 0)
+  if (!ONE && rank == 0)  // a single CTA finds its bins in its own histogram
     for (int i = tid; i < 2 * 2048; i += SEL_THREADS) (&sh.histg[0][0])[i] = 0;
   if (tid == 0) {
     sh.ncand = 0;
@@ -201,22 +201,26 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
     sh.scan[warp] = __float_as_uint(vmax);
   }
   __syncthreads();
-  if (tid == 0) {
-    float mn = INFINITY, mx = -INFINITY;
-    for (int w = 0; w < SEL_WARPS; w++) {
-      mn = fminf(mn, sh.red[w]);
-      mx = fmaxf(mx, __uint_as_float(sh.scan[w]));
-    }
-    sh.lmin = mn;
-    sh.lmax = mx;
+  float smin = INFINITY, smax = -INFINITY;  // every thread reads the warp results
+#pragma unroll
+  for (int w = 0; w < SEL_WARPS; w++) {
+    smin = fminf(smin, sh.red[w]);
+    smax = fmaxf(smax, __uint_as_float(sh.scan[w]));
   }
-  __syncthreads();
-  head_sync<ONE>(cluster);  // ranges published; rank 0's accumulators are zero
-  float smin = INFINITY, smax = -INFINITY;
-  for (int r = 0; r < CL; r++) {
-    const SelClusterShared* rs = rank_shared<ONE>(cluster, sh, r);
-    smin = fminf(smin, rs->lmin);
-    smax = fmaxf(smax, rs->lmax);
+  if (!ONE) {
+    if (tid == 0) {
+      sh.lmin = smin;
+      sh.lmax = smax;
+    }
+    __syncthreads();
+    head_sync<ONE>(cluster);  // ranges published; rank 0's accumulators are zero
+    smin = INFINITY;
+    smax = -INFINITY;
+    for (int r = 0; r < CL; r++) {
+      const SelClusterShared* rs = rank_shared<ONE>(cluster, sh, r);
+      smin = fminf(smin, rs->lmin);
+      smax = fmaxf(smax, rs->lmax);
+    }
   }
   SelClusterShared* root = rank_shared<ONE>(cluster, sh, 0);
   const bool flat = !(smax > smin);
@@ -226,12 +230,14 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   // ---- pass 1: value histogram over [smin, smax] ----
   if (!flat) {
     for (int i = tid; i < cnt; i += SEL_THREADS) atomicAdd(&sh.hist[vbin(cache[i], smin, inv1)], 1u);
-    __syncthreads();
-    for (int i = tid; i < 2048; i += SEL_THREADS)
-      if (sh.hist[i]) atomicAdd(&root->histg[0][i], sh.hist[i]);
+    if (!ONE) {
+      __syncthreads();
+      for (int i = tid; i < 2048; i += SEL_THREADS)
+        if (sh.hist[i]) atomicAdd(&root->histg[0][i], sh.hist[i]);
+    }
   }
   __syncthreads();
-  head_sync<ONE>(cluster);
+  if (!ONE) head_sync<ONE>(cluster);
 
   // ---- threshold: the key of the N-th largest logit, and how many ties to keep ----
   unsigned thr = 0, keq = 0, cta_gt = 0, cta_eq = 0;
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
     keq = (unsigned)Nb;
     cta_eq = (unsigned)cnt;
   } else {
-    find_bin(root->histg[0], 2048, (unsigned)Nb, sh);
+    find_bin(ONE ? sh.hist : root->histg[0], 2048, (unsigned)Nb, sh);
     const int b1 = (int)sh.digit;
     unsigned krem = sh.krem;
     const float lo1 = smin + (float)b1 * w1;
@@ -256,11 +262,13 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
         if (vbin(s, smin, inv1) == b1) atomicAdd(&sh.hist[vbin(s, lo1, inv2)], 1u);
       }
       __syncthreads();
-      for (int i = tid; i < 2048; i += SEL_THREADS)
-        if (sh.hist[i]) atomicAdd(&root->histg[1][i], sh.hist[i]);
-      __syncthreads();
-      head_sync<ONE>(cluster);
-      find_bin(root->histg[1], 2048, krem, sh);
+      if (!ONE) {
+        for (int i = tid; i < 2048; i += SEL_THREADS)
+          if (sh.hist[i]) atomicAdd(&root->histg[1][i], sh.hist[i]);
+        __syncthreads();
+        head_sync<ONE>(cluster);
+      }
+      find_bin(ONE ? sh.hist : root->histg[1], 2048, krem, sh);
       b2 = (int)sh.digit;
       krem = sh.krem;
     }
@@ -286,19 +294,24 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
           const unsigned u = order_key(s);
           const unsigned slot = atomicAdd(&root->ncand, 1u);
           if (slot < SEL_CANDS) root->cand[slot] = u;
-          const unsigned ls = atomicAdd(&sh.nlcand, 1u);
-          if (ls < SEL_CANDS) sh.lcand[ls] = u;
+          if (!ONE) {
+            const unsigned ls = atomicAdd(&sh.nlcand, 1u);
+            if (ls < SEL_CANDS) sh.lcand[ls] = u;
+          }
         }
       }
-      unsigned dgt_cta;
-      scan_block(dgt, sh.scan, dgt_cta);
+      // a single CTA needs no count of its own: nothing follows it
+      unsigned dgt_cta = 0;
+      if (!ONE) scan_block(dgt, sh.scan, dgt_cta);
       head_sync<ONE>(cluster);
       const unsigned nc = min(root->ncand, (unsigned)SEL_CANDS);
       unsigned myc = 0;
       if (tid < (int)nc) myc = root->cand[tid];
-      __syncthreads();
-      if (tid < (int)nc) sh.cand[tid] = myc;
-      __syncthreads();
+      if (!ONE) {
+        __syncthreads();
+        if (tid < (int)nc) sh.cand[tid] = myc;
+        __syncthreads();
+      }
       if (tid < (int)nc) {  // exact rank of each candidate among all candidates
         unsigned g = 0, e = 0;
         for (unsigned jj = 0; jj < nc; jj++) {
@@ -313,11 +326,13 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
       __syncthreads();
       thr = sh.thr;
       keq = sh.keq;
-      const unsigned nl = min(sh.nlcand, (unsigned)SEL_CANDS);
-      cta_gt = dgt_cta;
-      for (unsigned jj = 0; jj < nl; jj++) {
-        cta_gt += sh.lcand[jj] > thr;
-        cta_eq += sh.lcand[jj] == thr;
+      if (!ONE) {
+        const unsigned nl = min(sh.nlcand, (unsigned)SEL_CANDS);
+        cta_gt = dgt_cta;
+        for (unsigned jj = 0; jj < nl; jj++) {
+          cta_gt += sh.lcand[jj] > thr;
+          cta_eq += sh.lcand[jj] == thr;
+        }
       }
     } else {
       fallback = true;  // heavy ties or a very dense spot: exact radix over all logits
@@ -359,17 +374,19 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
     scan_block(lgt, sh.scan, cta_gt);
     scan_block(leq, sh.scan, cta_eq);
   }
-  if (tid == 0) {
-    sh.cnt_gt = cta_gt;
-    sh.cnt_eq = cta_eq;
-  }
-  __syncthreads();
-  head_sync<ONE>(cluster);
-  unsigned carry_gt = 0, carry_eq = 0;
-  for (int r = 0; r < rank; r++) {
-    const SelClusterShared* rs = rank_shared<ONE>(cluster, sh, r);
-    carry_gt += rs->cnt_gt;
-    carry_eq += rs->cnt_eq;
+  unsigned carry_gt = 0, carry_eq = 0;  // counts in the lower ranks' slices
+  if (!ONE) {
+    if (tid == 0) {
+      sh.cnt_gt = cta_gt;
+      sh.cnt_eq = cta_eq;
+    }
+    __syncthreads();
+    head_sync<ONE>(cluster);
+    for (int r = 0; r < rank; r++) {
+      const SelClusterShared* rs = rank_shared<ONE>(cluster, sh, r);
+      carry_gt += rs->cnt_gt;
+      carry_eq += rs->cnt_eq;
+    }
   }
 
   // ---- index-ordered compaction; dropped weight of the rest ----
@@ -442,8 +459,10 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
     sh.dsum = s;
     sh.Zp = s + s2;
   }
-  __syncthreads();
-  head_sync<ONE>(cluster);
+  if (!ONE) {
+    __syncthreads();
+    head_sync<ONE>(cluster);
+  }
   if (rank == 0) {
     if (tid == 0) {
       float s = 0.f, Z = 0.f;
@@ -458,7 +477,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
     }
     if (a.q_anchor) mirror_query<T>(a, qh);
   }
-  head_sync<ONE>(cluster);  // shared memory stays valid until every remote read is done
+  if (!ONE) head_sync<ONE>(cluster);  // shared memory stays valid until every remote read is done
 }
 
 // Cluster size and slice length: one CTA holds up to SELECT_SLICE_ONE logits;

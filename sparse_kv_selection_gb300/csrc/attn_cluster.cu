@@ -22,23 +22,24 @@ namespace cg = cooperative_groups;
 
 namespace prhs {
 
-constexpr int ACL_THREADS = 128;
+constexpr int ACL_THREADS = 256;  // 8 warps: 32 rows per step in flight per CTA
+constexpr int ACL_WARPS = ACL_THREADS / 32;
 constexpr int ACL_STAGE = 2048;  // row numbers staged in shared memory at a time
 constexpr float ACL_LOG2E = 1.4426950408889634f;
 constexpr float ACL_LN2 = 0.6931471805599453f;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(ACL_THREADS, 4) attn_cluster_kernel(const AttnLaunch a) {
+__global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const AttnLaunch a) {
   constexpr int RB = D * (int)sizeof(T);  // bytes per row
   constexpr int CPL = RB / 16 / 8;        // 16-byte chunks per lane
   constexpr int EPC = 16 / (int)sizeof(T);
   constexpr int EL = CPL * EPC;           // elements per lane
   constexpr int UNROLL = CPL >= 4 ? 2 : 4;
-  constexpr int STEP = 16 * UNROLL;       // rows per CTA iteration
+  constexpr int STEP = 4 * ACL_WARPS * UNROLL;  // rows per CTA iteration
   static_assert(RB % 128 == 0 && D <= ACL_THREADS, "row of whole 128-byte lines, one thread per output");
   __shared__ int sh_idx[ACL_STAGE];
-  __shared__ float sm_m[4], sm_l[4];
-  __shared__ float sm_o[4][D];
+  __shared__ float sm_m[ACL_WARPS], sm_l[ACL_WARPS];
+  __shared__ float sm_o[ACL_WARPS][D];
   __shared__ float part[ATTN_CLUSTER_MAX][D + 2];  // CTA 0: every CTA's state m, l, o[D]
 
   pdl_wait();
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(ACL_THREADS, 4) attn_cluster_kernel(const Attn
       long long row[UNROLL];
 #pragma unroll
       for (int uu = 0; uu < UNROLL; uu++) {
-        const int r = base + uu * 16 + warp * 4 + sg;
+        const int r = base + uu * 4 * ACL_WARPS + warp * 4 + sg;
         row[uu] = -1;
         if (r < se) {
           const int key = sh_idx[r - sb];
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(ACL_THREADS, 4) attn_cluster_kernel(const Attn
     }
   }
 
-  // ---- this CTA's state: the 4 row groups of each warp, then the 4 warps ----
+  // ---- this CTA's state: the 4 row groups of each warp, then the warps ----
 #pragma unroll
   for (int off = 8; off <= 16; off <<= 1) {
     const float m2 = __shfl_xor_sync(FULL_MASK, m, off);
@@ -192,11 +193,13 @@ __global__ void __launch_bounds__(ACL_THREADS, 4) attn_cluster_kernel(const Attn
   }
   __syncthreads();
   if (tid < D) {
-    float M = fmaxf(fmaxf(sm_m[0], sm_m[1]), fmaxf(sm_m[2], sm_m[3]));
+    float M = sm_m[0];
+#pragma unroll
+    for (int w = 1; w < ACL_WARPS; w++) M = fmaxf(M, sm_m[w]);
     float L = 0.f, O = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < 4; w++) {
+      for (int w = 0; w < ACL_WARPS; w++) {
         const float cw = exp2f(sm_m[w] - M);
         L += cw * sm_l[w];
         O += cw * sm_o[w][tid];

@@ -23,7 +23,10 @@ namespace prhs {
 constexpr int SEL_THREADS = 512;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 
-constexpr int SEL_CANDS = 256;  // candidates ranked exactly after the two bin passes
+// Candidates ranked exactly after the bin passes. The ranking costs
+// candidates^2 / threads steps, so a bin holding more runs the second, finer
+// bin pass first.
+constexpr int SEL_CANDS = 64;
 
 struct SelClusterShared {
   unsigned hist[2048];        // this CTA's histogram of the current bin pass
@@ -178,11 +181,23 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   // ---- load this CTA's slice; its logit range ----
   const float* src = a.scores + (long long)qh * kv.t_max + lo;
   float vmin = INFINITY, vmax = -INFINITY;
-  for (int i = tid; i < cnt; i += SEL_THREADS) {
-    const float s = src[i];
-    cache[i] = s;
-    vmin = fminf(vmin, s);
-    vmax = fmaxf(vmax, s);
+  constexpr int PRE = 8;  // loads in flight per thread before the first is used
+  for (int i0 = 0; i0 < cnt; i0 += SEL_THREADS * PRE) {
+    float v[PRE];
+#pragma unroll
+    for (int k = 0; k < PRE; k++) {
+      const int i = i0 + k * SEL_THREADS + tid;
+      v[k] = i < cnt ? src[i] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < PRE; k++) {
+      const int i = i0 + k * SEL_THREADS + tid;
+      if (i < cnt) {
+        cache[i] = v[k];
+        vmin = fminf(vmin, v[k]);
+        vmax = fmaxf(vmax, v[k]);
+      }
+    }
   }
   for (int i = tid; i < 2048; i += SEL_THREADS) sh.hist[i] = 0;
   if (!ONE && rank == 0)  // a single CTA finds its bins in its own histogram
@@ -390,7 +405,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   }
 
   // ---- index-ordered compaction; dropped weight of the rest ----
-  constexpr int E = 4;
+  constexpr int E = 8;  // consecutive logits per thread: 4096 per block-wide scan
   constexpr int TILE = SEL_THREADS * E;
   float dsum = 0.f, ssum = 0.f;  // weights exp(s - max) of dropped / kept logits
   for (int base = 0; base < cnt; base += TILE) {

@@ -439,6 +439,59 @@ def test_decode_matches_oracle(name):
 # --------------------------------------------------------------------------- #
 # the split entry points and graph capture of the decode step
 # --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_step_ties_flat_and_budgets(dtype):
+    """First decode step (every head retrieves) on caches whose logits tie
+    heavily (keys drawn from 7 rows), are all equal, or are fewer than the
+    budget, and with a zero budget: the set must be the oracle's exactly,
+    ties going to the lowest index."""
+    import sparse_kv_selection_gb300 as S
+    from workloads import bf16_bits_from_f32
+    from workloads.torch_io import tensor_of
+    rng = np.random.default_rng(23)
+    B, H, d, tmax = 4, 2, 128, 1500
+    lens = np.array([1500, 300, 1000, 800], np.int32)
+    budget = np.array([100, 400, 0, 257], np.int32)
+    store = (lambda x: x.astype(np.float32)) if dtype == "f32" else bf16_bits_from_f32
+    base = rng.normal(size=(H, 7, d)).astype(np.float32)
+    K = np.zeros((B, H, tmax, d), np.float32)
+    K[0] = base[:, np.arange(tmax) % 7]                  # 7 distinct logits per head
+    K[1] = rng.normal(size=(H, 1, d)).astype(np.float32)  # budget above the length
+    K[2] = rng.normal(size=(H, tmax, d))                  # zero budget
+    K[3] = base[:, :1]                                    # one logit value: flat
+    V = rng.normal(size=(B, H, tmax, d)).astype(np.float32)
+    q = rng.normal(size=(B, H, d)).astype(np.float32)
+    Ks, Vs, qs = store(K), store(V), store(q)
+    kv = S.KVCache(tensor_of(Ks, dtype, "cuda"), tensor_of(Vs, dtype, "cuda"),
+                   torch.from_numpy(lens).cuda(), H)
+    scale = d ** -0.5
+    dec = S.SparseDecoder(kv, n_budget=torch.from_numpy(budget), w=1, tau=0.8, scale=scale)
+    o, l, dl, r, n = dec.alloc_outputs(1)
+    dec.step(tensor_of(qs, dtype, "cuda"), o[0], l[0], dl[0], r[0], n[0])
+    gi = dec.idx.cpu().numpy()
+    o, l, dl, n = o[0].cpu().numpy(), l[0].cpu().numpy(), dl[0].cpu().numpy(), n[0].cpu().numpy()
+    ai, an = dec.anchor_idx.cpu().numpy(), dec.anchor_n.cpu().numpy()
+    assert S.last_error() == 0
+    for b in range(B):
+        for h in range(H):
+            t = int(lens[b])
+            Kb = P.widen(Ks[b, h, :t], dtype)
+            Vb = P.widen(Vs[b, h, :t], dtype)
+            qv = P.widen(qs[b, h], dtype)
+            if budget[b] == 0:
+                assert n[b, h] == 0 and an[b, h] == 0 and dl[b, h] == 1.0
+                assert (o[b, h] == 0).all() and l[b, h] == -math.inf
+                continue
+            sc = P.scores(qv, Kb, scale)
+            Sx = P.top_n(sc, int(budget[b]))
+            assert n[b, h] == len(Sx) == an[b, h], (b, h)
+            assert gi[b, h, :len(Sx)].tolist() == Sx.tolist(), (b, h)
+            assert ai[b, h, :len(Sx)].tolist() == Sx.tolist(), (b, h)
+            assert abs(dl[b, h] - P.dropped_mass(sc, Sx)) <= DELTA_TOL, (b, h)
+            ro, rl = P.attention(qv, Kb, Vb, Sx, scale)
+            assert np.abs(o[b, h] - ro).max() <= OUT_TOL and abs(l[b, h] - rl) <= LSE_TOL, (b, h)
+
+
 def test_score_then_select_equals_score_select():
     S, wl, dev, kv = _setup("gqa4_bf16")
     N = int(wl.budget[0])

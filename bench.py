@@ -189,6 +189,22 @@ def measured_peak_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def gathered_rows(idx_host, n_host, G):
+    """K/V rows the query heads of each KV head gather, each row counted once
+    per KV head: the compulsory HBM reads of a sparse attention launch (query
+    heads of one group that select the same row read it once; with G = 1 this
+    is the sum of the set sizes)."""
+    if G == 1:
+        return int(n_host.sum())
+    B, Hq = n_host.shape
+    tot = 0
+    for b in range(B):
+        for k in range(Hq // G):
+            sets = [idx_host[b, k * G + g, :n_host[b, k * G + g]] for g in range(G)]
+            tot += len(np.unique(np.concatenate(sets)))
+    return tot
+
+
 def profiled_traffic():
     """Per-launch DRAM bytes of each kernel from the committed ncu summary."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -366,7 +382,8 @@ def run_ours(args):
         score_bytes += float((fresh_groups * tlen[:, None]).sum() * d * es)
         score_bytes += float((~r_h[s]).sum() * d * es)                # q rows
     score_bytes /= Sq
-    attn_bytes = float((n_h * (2 * d * es + 4)).sum() + Sq * B * Hq * (d * es + 4 * d + 4)) / Sq
+    rows = sum(gathered_rows(idx[s].cpu().numpy() if G > 1 else None, n_h[s], G) for s in range(Sq))
+    attn_bytes = float(rows * 2 * d * es + 4 * n_h.sum() + Sq * B * Hq * (d * es + 4 * d + 4)) / Sq
     kb = {"score": score_bytes, "sparse_attn": attn_bytes}
     peak, peak_kind = measured_peak_gbs()
     traffic = profiled_traffic()
@@ -509,9 +526,9 @@ def run_kernels(args):
         "select": (lambda kv: S.binding.select(kv, q, N, idx, n_sel, delta, ws, n_budget=nb),
                    float(B * Hq * tl.mean() * 4)),
         "sparse_attn_topN": (lambda kv: S.sparse_attn(kv, q, wl.scale, idx, n_sel, out, lse, ws),
-                             float(n_h.sum() * 2 * d * es)),
+                             float(gathered_rows(idx.cpu().numpy(), n_h, wl.G) * 2 * d * es)),
         "sparse_attn_dilated": (lambda kv: S.sparse_attn(kv, q, wl.scale, didx, dn, out, lse, ws),
-                                float(dn_h.sum() * 2 * d * es)),
+                                float(gathered_rows(didx.cpu().numpy(), dn_h, wl.G) * 2 * d * es)),
     }
     peak, peak_kind = measured_peak_gbs()
     stream = torch.cuda.Stream()

@@ -205,6 +205,49 @@ def gathered_rows(idx_host, n_host, G):
     return tot
 
 
+def decode_diagnostics(S, kvs, q, scale, N, nb, idx, n_sel, reuse, delta, ws):
+    """Untimed diagnostics of a decode sequence, per (query, head) that reused
+    its anchor: the dropped mass of the attended (dilated) set under the
+    current query, the dropped mass of that query's own top-N set, and the
+    share of that top-N set the attended set covers. Retrieving queries
+    contribute their own dropped mass."""
+    import torch
+    Sq, B, Hq = reuse.shape
+    R = len(kvs)
+    acap = max(1, min(int(nb.max()) if nb is not None else N, kvs[0].t_max))
+    i32 = dict(device="cuda", dtype=torch.int32)
+    used = torch.empty(B, Hq, device="cuda")
+    tidx = torch.zeros(B, Hq, acap, **i32)
+    tn = torch.zeros(B, Hq, **i32)
+    tdel = torch.empty(B, Hq, device="cuda")
+    r_h = reuse.cpu().numpy().astype(bool)
+    d_used, d_top, cover = [], [], []
+    for s in range(Sq):
+        if not r_h[s].any():
+            continue
+        kv = kvs[s % R]
+        S.set_mass(kv, q[s], scale, idx[s], n_sel[s], used, ws)
+        S.score_select(kv, q[s], scale, N, tidx, tn, tdel, ws, n_budget=nb)
+        du, dt = used.cpu().numpy(), tdel.cpu().numpy()
+        gi, gn = idx[s].cpu().numpy(), n_sel[s].cpu().numpy()
+        ti, tnn = tidx.cpu().numpy(), tn.cpu().numpy()
+        for b, h in zip(*np.nonzero(r_h[s])):
+            d_used.append(float(du[b, h]))
+            d_top.append(float(dt[b, h]))
+            top = ti[b, h, :tnn[b, h]]
+            if top.size:
+                cover.append(len(np.intersect1d(gi[b, h, :gn[b, h]], top)) / top.size)
+    dl = delta.cpu().numpy()
+    fresh = dl[~r_h]
+    mean = lambda x: float(np.mean(x)) if len(x) else None
+    return {"reuse_delta_of_attended_set": mean(d_used),
+            "reuse_delta_of_own_topN": mean(d_top),
+            "reuse_topN_covered": mean(cover),
+            "retrieve_delta": mean(fresh[np.isfinite(fresh)]),
+            "reuse_pairs": len(d_used),
+            "untimed": True}
+
+
 def profiled_traffic():
     """Per-launch DRAM bytes of each kernel from the committed ncu summary."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -436,6 +479,10 @@ def run_ours(args):
     e2e_ms = max_over_ranks(te0.elapsed_time(te1), world, "cuda")
     e2e_value = units / (e2e_ms / 1e3)
 
+    # ---------------- untimed diagnostics (reuse steps) ----------------
+    diag = decode_diagnostics(S, kvs, q, scale, N, nb, idx, n_sel, reuse, delta, ws)
+    assert S.last_error() == 0
+
     # ---------------- CPU oracle on a bounded sample ----------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -465,6 +512,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
+            "diagnostics": diag,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -141,6 +141,18 @@ prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx,
                             int32_t* anchor_age, int32_t* idx, int32_t* n_sel, int cap,
                             uint8_t* reuse, cudaStream_t stream);
 
+/* Dropped attention mass of given index sets under the current query (a
+ * diagnostic for reuse steps, whose set was not selected under this query;
+ * abstract: the attention mass of discarded entries; Table I: delta(.)).
+ * Per query head with n = n_sel entries of idx (ascending, inside [0, t_b)):
+ *   s_i = scale * <q, k_i>, i < t_b;  delta = sum_{i < t_b, i not in idx} softmax(s)_i.
+ * n = 0 gives 1 (0 when t_b = 0). Scores every head through the workspace
+ * (ws from prhs_workspace_size(kv, 0)); entries out of range or not
+ * ascending are flagged in the device error word and skipped. */
+prhs_status prhs_set_mass(const prhs_kv* kv, const void* q, float scale, const int32_t* idx,
+                          const int32_t* n_sel, int cap, float* delta, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
 /* Sparse attention over the selected rows (Table V caption: sparse-attention
  * kernel over the selected KV): per query head with n = n_sel entries of idx,
  *   lse = log sum_{i in S} exp(s_i),  out = sum_{i in S} exp(s_i - lse) v_i,

@@ -22,7 +22,7 @@ DEV_TIMEOUT, DEV_BAD_INDEX, DEV_BAD_LEN, DEV_BAD_BLOCK, DEV_CAPACITY = 1, 2, 4, 
 # Entry points declared in include/prhs.h, in declaration order.
 EXPORTS = ["prhs_workspace_size", "prhs_workspace_init", "prhs_score_select", "prhs_score",
            "prhs_select", "prhs_cis_dilate",
-           "prhs_sparse_attn", "prhs_sparse_attn_noalloc", "prhs_dense_attn", "prhs_decode_step", "prhs_last_error",
+           "prhs_sparse_attn", "prhs_sparse_attn_noalloc", "prhs_set_mass", "prhs_dense_attn", "prhs_decode_step", "prhs_last_error",
            "prhs_device_error_bits", "prhs_status_str", "prhs_last_message", "prhs_num_sms"]
 
 
@@ -63,6 +63,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "prhs_cis_dilate": (I, [KV, P, P, I, P, P, I, D, I, P, P, P, I, P, P]),
         "prhs_sparse_attn": (I, [KV, P, F, P, P, I, P, P, P, Z, P]),
         "prhs_sparse_attn_noalloc": (I, [KV, P, F, P, P, I, P, P, P]),
+        "prhs_set_mass": (I, [KV, P, F, P, P, I, P, P, Z, P]),
         "prhs_dense_attn": (I, [KV, P, F, P, P, P, Z, P]),
         "prhs_decode_step": (I, [KV, P, F, I, P, I, D, I, P, P, P, I, P, P, P, I, P, P, P, P, P, Z, P]),
         "prhs_last_error": (I, []),
@@ -202,6 +203,13 @@ def cis_dilate(kv, anchor_idx, anchor_n, q, q_anchor, w, tau, idx, n_sel, reuse,
                                   _ptr(q), _ptr(q_anchor), int(w), float(tau), int(max_run),
                                   _ptr(anchor_age), _ptr(idx), _ptr(n_sel), idx.shape[-1],
                                   _ptr(reuse), _stream(stream)), "cis_dilate")
+
+
+def set_mass(kv, q, scale, idx, n_sel, delta, ws, stream=None) -> None:
+    """Dropped attention mass of the given sets under q (prhs_set_mass)."""
+    _check(load().prhs_set_mass(kv.ref(), _ptr(q), float(scale), _ptr(idx), _ptr(n_sel),
+                                idx.shape[-1], _ptr(delta), _ptr(ws), ws.numel(), _stream(stream)),
+           "set_mass")
 
 
 def sparse_attn(kv, q, scale, idx, n_sel, out, lse, ws, stream=None) -> None:

@@ -446,6 +446,29 @@ prhs_status prhs_score(const prhs_kv* kv, const void* q, float scale, const uint
   return do_score(*kv, di, L, ws, q, scale, head_skip, stream);
 }
 
+prhs_status prhs_set_mass(const prhs_kv* kv, const void* q, float scale, const int32_t* idx,
+                          const int32_t* n_sel, int cap, float* delta, void* ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if (!q || !idx || !n_sel || !delta) return fail(PRHS_EINVAL, "set_mass: null pointer argument");
+  if (!aligned16(q)) return fail(PRHS_EINVAL, "q must be 16-byte aligned");
+  if (cap <= 0) return fail(PRHS_EINVAL, "cap must be positive");
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  Layout L;
+  if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
+  if ((s = do_score(*kv, di, L, ws, q, scale, nullptr, stream)) != PRHS_OK) return s;
+  MassLaunch m;
+  m.kv = view_of(*kv, di->err);
+  m.scores = reinterpret_cast<const float*>(static_cast<const char*>(ws) + L.scores);
+  m.idx = idx;
+  m.n_sel = n_sel;
+  m.cap = cap;
+  m.delta = delta;
+  return launch_result(launch_mass(m, stream), "set mass kernel");
+}
+
 prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* n_budget,
                         const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
                         float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,

@@ -95,6 +95,17 @@ struct AttnLaunch {
   int cluster = 0;       // sparse only: > 0 runs the cluster kernel with this many CTAs per head
 };
 
+// Dropped mass of given sets over the logits in `scores` ([B][Hq][t_max]).
+struct MassLaunch {
+  KVView kv;
+  const float* scores;
+  const int32_t* idx;
+  const int32_t* n_sel;
+  int cap;
+  float* delta;
+};
+cudaError_t launch_mass(const MassLaunch& a, cudaStream_t s);
+
 // Units of the attention split (query heads when sparse, KV heads when dense)
 // and the floats of partial records the kernel may write for `ctas` CTAs.
 int attn_units(const KVView& kv, bool sparse);

@@ -94,3 +94,59 @@ def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0):
                 break
             assert n[s, b, h] == len(rec.S), (b, h, s)
     return compared, r
+
+
+def compare_decode_forced(wl, dev, kv, heads, steps=None, max_run=0):
+    """Teacher-forced decode: before every query the sampled heads get the
+    oracle's anchor state (its undilated set, the anchor query, the reuse
+    count), so a near-tie at one query cannot carry over to the next and
+    every (head, query) pair is compared. A retrieving set that differs from
+    the oracle's only at near-ties is accepted; the attention is then checked
+    against the oracle on the GPU's own set. Returns the pairs compared."""
+    import torch
+
+    import sparse_kv_selection_gb300 as S
+    steps = wl.steps if steps is None else steps
+    nb = dev["budget"] if len(set(wl.budget.tolist())) > 1 else None
+    dec = S.SparseDecoder(kv, N=int(wl.budget[0]) if nb is None else None, n_budget=nb, w=wl.w,
+                          tau=wl.tau, scale=wl.scale, max_run=max_run)
+    ref = P.decode_workload(wl, heads=heads, steps=steps, keep_scores=True, max_run=max_run)
+    o, l, dl, r, n = dec.alloc_outputs(1)
+    compared = 0
+    for s in range(steps):
+        for (b, h), recs in ref.items():
+            if s == 0:
+                dec.anchor_n[b, h] = 0
+                dec.anchor_age[b, h] = 0
+                continue
+            A = recs[s - 1].anchor_S
+            last = max(j for j in range(s) if not recs[j].reuse)  # the anchor's query
+            dec.anchor_idx[b, h, :len(A)] = torch.from_numpy(A.astype(np.int32)).cuda()
+            dec.anchor_n[b, h] = len(A)
+            dec.anchor_age[b, h] = s - 1 - last
+            dec.q_anchor[b, h] = dev["q"][last, b, h]
+        dl.fill_(float("nan"))
+        dec.step(dev["q"][s], o[0], l[0], dl[0], r[0], n[0])
+        oo, ll, dd, rr, nn = [x[0].cpu().numpy() for x in (o, l, dl, r, n)]
+        gidx = dec.idx.cpu().numpy()
+        for (b, h), recs in ref.items():
+            rec = recs[s]
+            if rec.cos is not None and abs(rec.cos - wl.tau) < GATE_GAP:
+                continue
+            assert bool(rr[b, h]) == rec.reuse, (b, h, s)
+            gset = gidx[b, h, :nn[b, h]]
+            if rec.reuse:
+                assert gset.tolist() == rec.S.tolist(), ("dilated set differs", b, h, s)
+                want_o, want_l = rec.out, rec.lse
+            else:
+                assert abs(dd[b, h] - rec.delta) <= DELTA_TOL, (b, h, s)
+                if gset.size == rec.S.size and (gset == rec.S).all():
+                    want_o, want_l = rec.out, rec.lse
+                else:
+                    check_topn(gset, rec.scores, int(wl.budget[b]))
+                    K, V = kv_rows64(wl, b, h // wl.G)
+                    want_o, want_l = P.attention(q64(wl, s, b, h), K, V, gset, wl.scale)
+            assert np.abs(oo[b, h] - want_o).max() <= OUT_TOL, (b, h, s)
+            assert abs(ll[b, h] - want_l) <= LSE_TOL, (b, h, s)
+            compared += 1
+    return compared

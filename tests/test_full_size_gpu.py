@@ -4,7 +4,7 @@ own grids), on sampled heads the fp64 oracle decodes one by one."""
 import numpy as np
 import pytest
 
-from parity_util import DELTA_TOL, LSE_TOL, OUT_TOL, compare_decode, kv_rows64, q64
+from parity_util import LSE_TOL, OUT_TOL, compare_decode, compare_decode_forced, kv_rows64, q64
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -40,6 +40,13 @@ def test_full_size_decode(name):
     assert S.last_error() == 0
     print(f"{name}: compared {compared} (head, step) pairs of {len(heads) * wl.steps}; "
           f"reuse fraction {r.mean():.3f}")
+
+
+@pytest.mark.parametrize("name", list(SAMPLES))
+def test_full_size_decode_teacher_forced(name):
+    S, wl, dev, kv, heads = _load(name)
+    compared = compare_decode_forced(wl, dev, kv, heads)
+    assert compared >= len(heads) * wl.steps - 2, compared
 
 
 @pytest.mark.parametrize("name", ["llama2_7b_mha", "mistral_7b_gqa", "paged_serving"])

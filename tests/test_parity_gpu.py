@@ -8,7 +8,7 @@ import pytest
 
 import oracle.prhs as P
 from parity_util import (DELTA_TOL, GATE_GAP, LSE_TOL, OUT_TOL, TIE_GAP, check_topn,
-                         compare_decode, kv_rows64, q64)
+                         compare_decode, compare_decode_forced, kv_rows64, q64)
 from workloads import make_workload
 
 torch = pytest.importorskip("torch")
@@ -490,6 +490,53 @@ def test_decode_step_ties_flat_and_budgets(dtype):
             assert abs(dl[b, h] - P.dropped_mass(sc, Sx)) <= DELTA_TOL, (b, h)
             ro, rl = P.attention(qv, Kb, Vb, Sx, scale)
             assert np.abs(o[b, h] - ro).max() <= OUT_TOL and abs(l[b, h] - rl) <= LSE_TOL, (b, h)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("max_run", [0, 3])
+def test_decode_teacher_forced(name, max_run):
+    S, wl, dev, kv = _setup(name)
+    compared = compare_decode_forced(wl, dev, kv, _heads(wl), max_run=max_run)
+    assert compared >= len(_heads(wl)) * wl.steps - 2, compared
+
+
+@pytest.mark.parametrize("name", ["mha_bf16_ragged", "gqa4_bf16", "paged_bf16", "f32_d64_gqa2"])
+def test_set_mass_matches_oracle(name):
+    """Dropped mass of given sets (the reuse-step diagnostic): top-N sets,
+    their dilations, random sets, the empty set and the whole cache."""
+    S, wl, dev, kv = _setup(name)
+    rng = np.random.default_rng(29)
+    cap = wl.t_max
+    idx = np.zeros((wl.B, wl.Hq, cap), np.int32)
+    n = np.zeros((wl.B, wl.Hq), np.int32)
+    sets = {}
+    for b, h in _heads(wl):
+        K, _ = kv_rows64(wl, b, h // wl.G)
+        t = K.shape[0]
+        sc = P.scores(q64(wl, 2, b, h), K, wl.scale)
+        kind = (b * wl.Hq + h) % 5
+        if kind == 0:
+            Sx = P.top_n(sc, int(wl.budget[b]))
+        elif kind == 1:
+            Sx = P.dilate(P.top_n(sc, int(wl.budget[b])), wl.w, t)
+        elif kind == 2:
+            Sx = np.sort(rng.choice(t, size=int(rng.integers(1, t)), replace=False))
+        elif kind == 3:
+            Sx = np.zeros(0, np.int64)
+        else:
+            Sx = np.arange(t)
+        sets[(b, h)] = Sx
+        idx[b, h, :len(Sx)] = Sx
+        n[b, h] = len(Sx)
+    delta = torch.full((wl.B, wl.Hq), -1.0, device="cuda")
+    ws = S.make_workspace(kv, cap)
+    S.set_mass(kv, dev["q"][2], wl.scale, torch.from_numpy(idx).cuda(), torch.from_numpy(n).cuda(),
+               delta, ws)
+    dl = delta.cpu().numpy()
+    for b, h in _heads(wl):
+        K, _ = kv_rows64(wl, b, h // wl.G)
+        want = P.dropped_mass(P.scores(q64(wl, 2, b, h), K, wl.scale), sets[(b, h)])
+        assert abs(dl[b, h] - want) <= DELTA_TOL, (b, h, dl[b, h], want)
 
 
 def test_score_then_select_equals_score_select():

@@ -34,8 +34,8 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
   constexpr int CPL = RB / 16 / 8;        // 16-byte chunks per lane
   constexpr int EPC = 16 / (int)sizeof(T);
   constexpr int EL = CPL * EPC;           // elements per lane
-  constexpr int UNROLL = CPL >= 4 ? 2 : 4;
-  constexpr int STEP = 4 * ACL_WARPS * UNROLL;  // rows per CTA iteration
+  constexpr int UP = CPL >= 4 ? 1 : 2;          // rows per 8-lane group per batch
+  constexpr int STEP = 4 * ACL_WARPS * UP;       // rows per batch per CTA
   static_assert(RB % 128 == 0 && D <= ACL_THREADS, "row of whole 128-byte lines, one thread per output");
   __shared__ int sh_idx[ACL_STAGE];
   __shared__ float sm_m[ACL_WARPS], sm_l[ACL_WARPS];
@@ -100,10 +100,14 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
       for (int x = tid; x < se - sb; x += ACL_THREADS) sh_idx[x] = rows[rank + (long long)CL * (sb + x)];
       __syncthreads();
     }
-    for (int base = sb; base < se; base += STEP) {
-      long long row[UNROLL];
+    // Two batches of UP rows per 8-lane group in flight: the loads of the
+    // next batch are issued before the current one is consumed, so a CTA
+    // never waits a full memory round trip between batches.
+    long long rowA[UP], rowB[UP];
+    uint4 kA[UP][CPL], vA[UP][CPL], kB[UP][CPL], vB[UP][CPL];
+    auto issue = [&](int base, long long (&row)[UP], uint4 (&kc)[UP][CPL], uint4 (&vc)[UP][CPL]) {
 #pragma unroll
-      for (int uu = 0; uu < UNROLL; uu++) {
+      for (int uu = 0; uu < UP; uu++) {
         const int r = base + uu * 4 * ACL_WARPS + warp * 4 + sg;
         row[uu] = -1;
         if (r < se) {
@@ -116,9 +120,8 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
           }
         }
       }
-      uint4 kc[UNROLL][CPL], vc[UNROLL][CPL];
 #pragma unroll
-      for (int uu = 0; uu < UNROLL; uu++)
+      for (int uu = 0; uu < UP; uu++)
 #pragma unroll
         for (int cc = 0; cc < CPL; cc++) {
           if (row[uu] >= 0) {
@@ -129,9 +132,12 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
             vc[uu][cc] = make_uint4(0, 0, 0, 0);
           }
         }
-      float s[UNROLL];
+    };
+    auto consume = [&](const long long (&row)[UP], const uint4 (&kc)[UP][CPL],
+                       const uint4 (&vc)[UP][CPL]) {
+      float s[UP];
 #pragma unroll
-      for (int uu = 0; uu < UNROLL; uu++) {
+      for (int uu = 0; uu < UP; uu++) {
         float kf[EL];
 #pragma unroll
         for (int cc = 0; cc < CPL; cc++) Elem<T>::unpack(kc[uu][cc], kf + cc * EPC);
@@ -145,14 +151,14 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
       }
       float mx = m;
 #pragma unroll
-      for (int uu = 0; uu < UNROLL; uu++) mx = fmaxf(mx, s[uu]);
-      if (mx == -INFINITY) continue;
+      for (int uu = 0; uu < UP; uu++) mx = fmaxf(mx, s[uu]);
+      if (mx == -INFINITY) return;
       const float corr = exp2f(m - mx);
       l *= corr;
 #pragma unroll
       for (int e = 0; e < EL; e++) o[e] *= corr;
 #pragma unroll
-      for (int uu = 0; uu < UNROLL; uu++) {
+      for (int uu = 0; uu < UP; uu++) {
         float vf[EL];
 #pragma unroll
         for (int cc = 0; cc < CPL; cc++) Elem<T>::unpack(vc[uu][cc], vf + cc * EPC);
@@ -162,6 +168,15 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
         for (int e = 0; e < EL; e++) o[e] = fmaf(p, vf[e], o[e]);
       }
       m = mx;
+    };
+    issue(sb, rowA, kA, vA);
+    for (int base = sb; base < se; base += 2 * STEP) {  // uniform over the CTA
+      const bool more = base + STEP < se;
+      if (more) issue(base + STEP, rowB, kB, vB);
+      consume(rowA, kA, vA);
+      if (!more) break;
+      if (base + 2 * STEP < se) issue(base + 2 * STEP, rowA, kA, vA);
+      consume(rowB, kB, vB);
     }
   }
 

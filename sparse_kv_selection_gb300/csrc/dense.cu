@@ -3,11 +3,14 @@
 // head, for all G query heads that read it.
 //
 // K and V tiles of one KV head stream through a TMA -> shared-memory ring
-// (128-byte swizzle, mbarrier-paced, one producer warp); the consumer warps
-// compute the G logits of each key as the scoring kernel does (8 lanes per
-// key, transposed shuffle reduction), keep a warp-uniform online softmax per
-// query head in base 2, and accumulate p * v from the same shared-memory V
-// tile, so each K and V byte leaves HBM once for the whole group. CTAs take
+// (128-byte swizzle, mbarrier-paced, one producer warp). The consumer warps
+// form two groups of four, each holding GH = G / 2 query heads of the KV
+// head: both groups read the same shared-memory tiles,
+// computes its heads' logits as the scoring kernel does (8 lanes per key,
+// transposed shuffle reduction), keeps a warp-uniform online softmax per head
+// in base 2 and accumulates p * v from the same V tile. Each K and V byte
+// leaves HBM once for the whole group, and the SM runs 8 consumer warps
+// instead of 4 with the registers of G / 2 heads each. CTAs take
 // equal shares of the key tiles of all KV heads; a KV head split over several
 // CTAs is merged by the last one to finish (atomic ticket, no waiting).
 #include "kernels.h"
@@ -75,20 +78,31 @@ __device__ __forceinline__ bool in_range(long long i, long long n, unsigned* err
   return false;
 }
 
+// Query heads per consumer group and consumer warps of the dense kernel.
+// Two consumer groups of G / 2 heads (one group when G = 1): 9 warps per SM,
+// at most 3 per scheduler, whose 16K registers then allow 168 per thread.
+template <int G> struct DenseGroups {
+  static constexpr int GH = G >= 2 ? G / 2 : 1;
+  static constexpr int NGR = G / GH;
+  static constexpr int REGS = 168;
+};
+
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(32 * (DenseShape<T, D>::NW + 1))
+__global__ void __maxnreg__(DenseGroups<G>::REGS)
     dense_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                  const DenseLaunch a) {
   using S = DenseShape<T, D>;
   constexpr int PW = D + 2;
-  constexpr int NC = S::NW * 32;  // consumer threads
+  constexpr int GH = DenseGroups<G>::GH;     // query heads per consumer group
+  constexpr int NCW = S::NW * DenseGroups<G>::NGR;  // consumer warps
+  constexpr int NC = NCW * 32;                // consumer threads
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::STAGES * S::STAGE);
   uint64_t* empty = full + S::STAGES;
   int* tprefix = reinterpret_cast<int*>(empty + S::STAGES);  // [units + 1]
-  __shared__ int sh_wsum[8];
+  __shared__ int sh_wsum[32];
   __shared__ float sm_m[S::NW][G], sm_l[S::NW][G];
   __shared__ float sm_o[S::NW][G][D];
   __shared__ int sh_last;
@@ -167,13 +181,13 @@ __global__ void __launch_bounds__(32 * (DenseShape<T, D>::NW + 1))
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::STAGES; s++) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], S::NW);
+      mbar_init(&empty[s], NCW);
     }
     fence_barrier_init();
   }
   __syncthreads();
 
-  if (warp == S::NW) {
+  if (warp == NCW) {
     // ------- producer warp: K and V tiles of each stage -------
     if (lane == 0) {
       prefetch_tmap(&kmap);
@@ -222,31 +236,33 @@ __global__ void __launch_bounds__(32 * (DenseShape<T, D>::NW + 1))
   // ---------------- consumers ----------------
   const int r = lane >> 3;  // key slot (8 keys)
   const int j = lane & 7;   // 16-byte chunk of each 128-byte segment: this lane's d-slice
+  const int wl = warp % S::NW;       // this warp's 32 keys of each stage
+  const int hg = (warp / S::NW) * GH;  // this warp's first query head in the group
   const float qscale = a.scale * D_LOG2E;
-  float qf[G][S::EL], o[G][S::EL], m[G], l[G];
+  float qf[GH][S::EL], o[GH][S::EL], m[GH], l[GH];
   int cur_u = -1, k1 = 0, qh0 = 0;
   bool dead = false;  // a wait timed out: keep step with the other warps, compute nothing
 
   // merge this CTA's state for unit u into out/lse (or a partial + ticket)
   auto finalize = [&](int u) {
 #pragma unroll
-    for (int g = 0; g < G; g++) {
+    for (int gg = 0; gg < GH; gg++) {
 #pragma unroll
       for (int e = 0; e < S::EL; e++) {  // the warp's m is uniform: slots add up
-        o[g][e] += __shfl_xor_sync(FULL_MASK, o[g][e], 8);
-        o[g][e] += __shfl_xor_sync(FULL_MASK, o[g][e], 16);
+        o[gg][e] += __shfl_xor_sync(FULL_MASK, o[gg][e], 8);
+        o[gg][e] += __shfl_xor_sync(FULL_MASK, o[gg][e], 16);
       }
-      const float L = warp_sum(l[g]);
+      const float L = warp_sum(l[gg]);
       if (lane == 0) {
-        sm_m[warp][g] = m[g];
-        sm_l[warp][g] = L;
+        sm_m[wl][hg + gg] = m[gg];
+        sm_l[wl][hg + gg] = L;
       }
       if (lane < 8) {
 #pragma unroll
         for (int h = 0; h < S::NH; h++)
 #pragma unroll
           for (int e = 0; e < S::EPC; e++)
-            sm_o[warp][g][h * (128 / (int)sizeof(T)) + j * S::EPC + e] = o[g][h * S::EPC + e];
+            sm_o[wl][hg + gg][h * (128 / (int)sizeof(T)) + j * S::EPC + e] = o[gg][h * S::EPC + e];
       }
     }
     consumer_bar(NC);
@@ -328,16 +344,17 @@ __global__ void __launch_bounds__(32 * (DenseShape<T, D>::NW + 1))
       qh0 = b * kv.Hq + kvh * G;
       k1 = seq_len(kv, b);
 #pragma unroll
-      for (int g = 0; g < G; g++) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
+      for (int gg = 0; gg < GH; gg++) {
+        m[gg] = -INFINITY;
+        l[gg] = 0.f;
 #pragma unroll
         for (int h = 0; h < S::NH; h++)
 #pragma unroll
           for (int e = 0; e < S::EPC; e++) {
-            const long long qi = (long long)(qh0 + g) * D + h * (128 / (int)sizeof(T)) + j * S::EPC + e;
-            qf[g][h * S::EPC + e] = in_range(qi, n_out, kv.err) ? Elem<T>::load1(a.q, qi) * qscale : 0.f;
-            o[g][h * S::EPC + e] = 0.f;
+            const long long qi =
+                (long long)(qh0 + hg + gg) * D + h * (128 / (int)sizeof(T)) + j * S::EPC + e;
+            qf[gg][h * S::EPC + e] = in_range(qi, n_out, kv.err) ? Elem<T>::load1(a.q, qi) * qscale : 0.f;
+            o[gg][h * S::EPC + e] = 0.f;
           }
       }
     }
@@ -348,14 +365,14 @@ __global__ void __launch_bounds__(32 * (DenseShape<T, D>::NW + 1))
     }
     const uint8_t* kt = smem + s * S::STAGE;
     const uint8_t* vt = kt + S::TILE;
-    float acc[G][8];
+    float acc[GH][8];
 #pragma unroll
-    for (int g = 0; g < G; g++)
+    for (int gg = 0; gg < GH; gg++)
 #pragma unroll
-      for (int p = 0; p < 8; p++) acc[g][p] = 0.f;
+      for (int p = 0; p < 8; p++) acc[gg][p] = 0.f;
 #pragma unroll
     for (int p = 0; p < 8; p++) {
-      const int key = warp * 32 + r * 8 + p;
+      const int key = wl * 32 + r * 8 + p;
 #pragma unroll
       for (int h = 0; h < S::NH; h++) {
         const int line = key * S::NH + h;
@@ -363,29 +380,29 @@ __global__ void __launch_bounds__(32 * (DenseShape<T, D>::NW + 1))
         float f[S::EPC];
         Elem<T>::unpack(cw, f);
 #pragma unroll
-        for (int g = 0; g < G; g++)
+        for (int gg = 0; gg < GH; gg++)
 #pragma unroll
-          for (int e = 0; e < S::EPC; e++) acc[g][p] = fmaf(qf[g][h * S::EPC + e], f[e], acc[g][p]);
+          for (int e = 0; e < S::EPC; e++) acc[gg][p] = fmaf(qf[gg][h * S::EPC + e], f[e], acc[gg][p]);
       }
     }
-    const bool valid = tile0 + warp * 32 + lane < k1;
-    float pr[G];
+    const bool valid = tile0 + wl * 32 + lane < k1;
+    float pr[GH];
 #pragma unroll
-    for (int g = 0; g < G; g++) {
-      const float red = transpose_reduce8_d(acc[g], j);  // every lane takes part
+    for (int gg = 0; gg < GH; gg++) {
+      const float red = transpose_reduce8_d(acc[gg], j);  // every lane takes part
       const float sc = valid ? red : -INFINITY;
-      const float mx = fmaxf(m[g], warp_max(sc));
-      const float corr = m[g] == -INFINITY ? 0.f : exp2f(m[g] - mx);
-      pr[g] = mx == -INFINITY ? 0.f : exp2f(sc - mx);
-      l[g] = l[g] * corr + pr[g];
+      const float mx = fmaxf(m[gg], warp_max(sc));
+      const float corr = m[gg] == -INFINITY ? 0.f : exp2f(m[gg] - mx);
+      pr[gg] = mx == -INFINITY ? 0.f : exp2f(sc - mx);
+      l[gg] = l[gg] * corr + pr[gg];
 #pragma unroll
-      for (int e = 0; e < S::EL; e++) o[g][e] *= corr;
-      m[g] = mx;
+      for (int e = 0; e < S::EL; e++) o[gg][e] *= corr;
+      m[gg] = mx;
     }
     // p * v: lane (r, j) adds the keys of slot r into its d-slice j
 #pragma unroll
     for (int p = 0; p < 8; p++) {
-      const int key = warp * 32 + r * 8 + p;
+      const int key = wl * 32 + r * 8 + p;
       float vf[S::EL];
 #pragma unroll
       for (int h = 0; h < S::NH; h++) {
@@ -394,10 +411,10 @@ __global__ void __launch_bounds__(32 * (DenseShape<T, D>::NW + 1))
         Elem<T>::unpack(cw, vf + h * S::EPC);
       }
 #pragma unroll
-      for (int g = 0; g < G; g++) {
-        const float pk = __shfl_sync(FULL_MASK, pr[g], r * 8 + p);
+      for (int gg = 0; gg < GH; gg++) {
+        const float pk = __shfl_sync(FULL_MASK, pr[gg], r * 8 + p);
 #pragma unroll
-        for (int e = 0; e < S::EL; e++) o[g][e] = fmaf(pk, vf[e], o[g][e]);
+        for (int e = 0; e < S::EL; e++) o[gg][e] = fmaf(pk, vf[e], o[gg][e]);
       }
     }
     __syncwarp();
@@ -414,7 +431,7 @@ static cudaError_t dense_go(const DenseLaunch& a, const CUtensorMap* km, const C
   const size_t smem = S::SMEM + ((size_t)a.kv.B * a.kv.Hkv + 1) * sizeof(int);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(a.ctas), dim3(32 * (S::NW + 1)), smem, st, *km, *vm, a);
+  return launch_pdl(k, dim3(a.ctas), dim3(32 * (S::NW * DenseGroups<G>::NGR + 1)), smem, st, *km, *vm, a);
 }
 
 template <typename T, int D>

@@ -228,3 +228,70 @@ def decode_workload(wl, heads=None, steps=None, keep_scores=False, max_run=0):
         res[(b, hq)] = decode_head(qs, K, V, int(wl.budget[b]), wl.w, wl.tau, wl.scale,
                                    keep_scores=keep_scores, max_run=max_run)
     return res
+
+
+# --------------------------------------------------------------------------- #
+# growing cache with forced sinks and local window (Fig. 11)
+# --------------------------------------------------------------------------- #
+def forced_set(t: int, n_sink: int, window: int) -> np.ndarray:
+    """Keys every query attends whatever its scores: the first n_sink keys
+    (attention sinks) and the last `window` keys (the local window), clipped
+    to [0, t), ascending without repeats.
+
+    Reading of Fig. 11 (sink and recent positions carry attention mass for
+    every query) as a deterministic set added to the selected one.
+    """
+    keep = np.zeros(t, bool)
+    keep[:min(max(n_sink, 0), t)] = True
+    keep[max(0, t - max(window, 0)):] = True
+    return np.nonzero(keep)[0].astype(np.int64)
+
+
+def top_n_between(s: np.ndarray, N: int, n_sink: int, window: int) -> np.ndarray:
+    """The N largest logits among the keys outside the forced set (lowest
+    index on ties), ascending: top_n over the middle range [n_sink, t - window)."""
+    t = np.asarray(s).shape[0]
+    lo, hi = min(max(n_sink, 0), t), max(min(max(n_sink, 0), t), t - max(window, 0))
+    return lo + top_n(np.asarray(s)[lo:hi], N)
+
+
+def decode_head_grow(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, t0: int, N: int, w: int,
+                     tau: float, scale: float, n_sink: int, window: int,
+                     keep_scores: bool = False, max_run: int = 0) -> list[HeadStep]:
+    """decode_head on a cache that gains one key per query, with a forced set.
+
+    Query s sees the first t_s = t0 + s + 1 rows of K and V (the current
+    token's key and value are appended before it attends). A retrieving
+    query attends forced_set(t_s) together with top_n_between(N); its anchor
+    is the top-N part. A reusing query attends forced_set(t_s) together with
+    the anchor's set dilated by +/- w and clipped to [0, t_s). delta is the
+    dropped mass of the attended set on retrieving queries. With n_sink =
+    window = 0 and a fixed cache this is decode_head.
+    """
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    anchor_S = anchor_q = None
+    rec = []
+    age = 0
+    for step, q in enumerate(np.asarray(q_steps, np.float64)):
+        t = t0 + step + 1
+        Kt, Vt = K[:t], V[:t]
+        c, reuse = (None, False) if anchor_S is None else cis_gate(q, anchor_q, tau)
+        if max_run > 0 and age >= max_run - 1:
+            reuse = False
+        age = age + 1 if reuse else 0
+        s = scores(q, Kt, scale)
+        F = forced_set(t, n_sink, window)
+        delta = s_nth = None
+        if reuse:
+            S = np.union1d(F, dilate(anchor_S, w, t)).astype(np.int64)
+        else:
+            T = top_n_between(s, N, n_sink, window)
+            S = np.union1d(F, T).astype(np.int64)
+            delta = dropped_mass(s, S)
+            anchor_S, anchor_q = T, q
+        out, lse = attention(q, Kt, Vt, S, scale)
+        rec.append(HeadStep(reuse=reuse, cos=c, S=S, anchor_S=anchor_S, delta=delta,
+                            delta_used=dropped_mass(s, S), s_nth=s_nth, out=out, lse=lse,
+                            scores=s if keep_scores else None))
+    return rec

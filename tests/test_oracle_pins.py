@@ -252,6 +252,80 @@ def check_widen():
     assert P.widen(np.array([0.1], np.float32), "f32")[0] == float(np.float32(0.1))
 
 
+def check_forced_set():
+    """Sinks and window clipped to [0, t): hand cases."""
+    assert P.forced_set(10, 2, 3).tolist() == [0, 1, 7, 8, 9]
+    assert P.forced_set(3, 2, 3).tolist() == [0, 1, 2]
+    assert P.forced_set(10, 0, 0).tolist() == []
+    assert P.forced_set(10, 12, 0).tolist() == list(range(10))
+    assert P.forced_set(10, 0, 1).tolist() == [9]
+    assert P.forced_set(0, 2, 3).tolist() == []
+
+
+def check_top_n_between(rng):
+    """The N best keys outside the forced set: brute force over subsets of
+    the middle keys (the lowest-index subset among the optimal ones)."""
+    for t in (5, 8, 11):
+        for n_sink, window in ((0, 0), (1, 2), (2, 3), (4, 4)):
+            s = rng.normal(size=t) * 2
+            s[rng.integers(0, t)] = s[rng.integers(0, t)]  # a tie
+            mid = [i for i in range(t) if i >= n_sink and i < t - window]
+            for N in range(1, len(mid) + 2):
+                got = P.top_n_between(s, N, n_sink, window).tolist()
+                if N >= len(mid):
+                    assert got == mid
+                    continue
+                best = None
+                for sub in itertools.combinations(mid, N):
+                    key = (-np.exp(s[list(sub)]).sum(), sub)
+                    if best is None or key < best:
+                        best = key
+                # equal sums only at exact ties: compare the kept mass
+                assert abs(np.exp(s[got]).sum() + best[0]) < 1e-12, (t, n_sink, window, N)
+                assert set(got).isdisjoint(P.forced_set(t, n_sink, window).tolist())
+
+
+def check_decode_grow(rng):
+    """Growing-cache decode: the forced keys are always attended, retrieving
+    steps keep |F| + min(N, |middle|) keys and no N-subset of the middle
+    drops less mass, reuse steps attend F with the dilated anchor, the
+    anchor never holds forced keys; the first step with no forced keys is
+    decode_head's on the visible rows; a budget covering the cache is dense."""
+    d, t0, steps, w = 8, 9, 6, 1
+    K = rng.normal(size=(t0 + steps, d))
+    V = rng.normal(size=(t0 + steps, d))
+    qs = rng.normal(size=(steps, d))
+    qs[1:] = qs[0] + 0.05 * rng.normal(size=(steps - 1, d))    # reuse after step 0
+    qs[3] = -qs[0]                                              # then retrieve again
+    for n_sink, window, N in ((2, 2, 3), (1, 3, 2), (0, 0, 4)):
+        rec = P.decode_head_grow(qs, K, V, t0, N, w, 0.8, d ** -0.5, n_sink, window,
+                                 keep_scores=True)
+        assert [r.reuse for r in rec][:4] == [False, True, True, False]
+        for st, r in enumerate(rec):
+            t = t0 + st + 1
+            F = P.forced_set(t, n_sink, window)
+            assert np.all(np.diff(r.S) > 0) and r.S.min() >= 0 and r.S.max() < t
+            assert set(F.tolist()) <= set(r.S.tolist())
+            assert set(r.anchor_S.tolist()).isdisjoint(F.tolist()) or (n_sink == 0 and window == 0)
+            if r.reuse:
+                want = np.union1d(F, P.dilate(r.anchor_S, w, t))
+                assert r.S.tolist() == want.tolist()
+            else:
+                mid = [i for i in range(t) if i >= n_sink and i < t - window]
+                assert len(r.S) == len(F) + min(N, len(mid))
+                for sub in itertools.combinations(mid, min(N, len(mid))):
+                    alt = np.union1d(F, list(sub)).astype(np.int64)
+                    assert r.delta <= P.dropped_mass(r.scores, alt) + 1e-12
+        if n_sink == 0 and window == 0:
+            first = P.decode_head(qs[:1], K[:t0 + 1], V[:t0 + 1], N, w, 0.8, d ** -0.5)[0]
+            assert rec[0].S.tolist() == first.S.tolist()
+            assert np.allclose(rec[0].out, first.out, atol=1e-14) and abs(rec[0].lse - first.lse) < 1e-14
+    big = P.decode_head_grow(qs[:1], K, V, t0, 100, w, 0.8, d ** -0.5, 2, 2)[0]
+    do, dl = P.dense_attention(qs[0], K[:t0 + 1], V[:t0 + 1], d ** -0.5)
+    assert big.S.tolist() == list(range(t0 + 1)) and big.delta == 0.0
+    assert np.allclose(big.out, do, atol=1e-14) and abs(big.lse - dl) < 1e-14
+
+
 # --------------------------------------------------------------------------- #
 # tests
 # --------------------------------------------------------------------------- #
@@ -404,3 +478,33 @@ def test_mutation_gate_sign(monkeypatch):
     good = P.cosine
     monkeypatch.setattr(P, "cosine", lambda q, qa: None if good(q, qa) is None else -good(q, qa))
     assert _caught(check_cosine_gate, np.random.default_rng(0))
+
+
+def test_forced_set():
+    check_forced_set()
+
+
+def test_top_n_between(rng):
+    check_top_n_between(rng)
+
+
+def test_decode_grow(rng):
+    check_decode_grow(rng)
+
+
+def test_mutation_window_off_by_one(monkeypatch, rng):
+    orig = P.forced_set
+    monkeypatch.setattr(P, "forced_set", lambda t, n, wdw: orig(t, n, wdw + 1))
+    assert _caught(check_forced_set)
+
+
+def test_mutation_forced_keys_ranked(monkeypatch, rng):
+    monkeypatch.setattr(P, "top_n_between", lambda s, N, n, wdw: P.top_n(s, N))
+    assert _caught(check_top_n_between, rng)
+
+
+def test_mutation_anchor_holds_forced(monkeypatch, rng):
+    orig = P.top_n_between
+    monkeypatch.setattr(P, "top_n_between",
+                        lambda s, N, n, wdw: np.union1d(orig(s, N, n, wdw), P.forced_set(len(s), n, wdw)))
+    assert _caught(check_decode_grow, rng)

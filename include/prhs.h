@@ -101,12 +101,20 @@ prhs_status prhs_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
  * untouched (their idx, n_sel and delta rows are not written).
  * anchor_idx / anchor_n / q_anchor (all nullable together): also copy each
  * written set, its size and the query into these anchor buffers (the CIS
- * anchor, row capacity anchor_cap). */
+ * anchor, row capacity anchor_cap).
+ * Forced keys (Fig. 11: attention sinks and the recent window), n_sink >= 0
+ * and window >= 0, 0 and 0 for none: the first n_sink and the last `window`
+ * keys of each cache are left out of the ranking; the N largest are taken
+ * among the keys between them, and the written set is the forced keys, those
+ * N and nothing else (ascending); delta is its dropped mass; the anchor row
+ * gets only the N ranked keys. Forced keys need the anchor buffers and a
+ * t_max of at most 131072; cap >= N + n_sink + window. */
 prhs_status prhs_score_select(const prhs_kv* kv, const void* q, float scale, int N,
-                              const int32_t* n_budget, const uint8_t* head_skip,
-                              int32_t* idx, int32_t* n_sel, int cap, float* delta,
-                              int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
-                              void* q_anchor, void* ws, size_t ws_bytes, cudaStream_t stream);
+                              const int32_t* n_budget, int n_sink, int window,
+                              const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
+                              float* delta, int32_t* anchor_idx, int32_t* anchor_n,
+                              int anchor_cap, void* q_anchor, void* ws, size_t ws_bytes,
+                              cudaStream_t stream);
 
 /* The two halves of prhs_score_select, for callers that time or reuse them
  * separately. prhs_score writes the logits s_i = scale * <q, k_i> of every
@@ -117,9 +125,10 @@ prhs_status prhs_score_select(const prhs_kv* kv, const void* q, float scale, int
 prhs_status prhs_score(const prhs_kv* kv, const void* q, float scale, const uint8_t* head_skip,
                        void* ws, size_t ws_bytes, cudaStream_t stream);
 prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* n_budget,
-                        const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
-                        float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
-                        void* q_anchor, void* ws, size_t ws_bytes, cudaStream_t stream);
+                        int n_sink, int window, const uint8_t* head_skip, int32_t* idx,
+                        int32_t* n_sel, int cap, float* delta, int32_t* anchor_idx,
+                        int32_t* anchor_n, int anchor_cap, void* q_anchor, void* ws,
+                        size_t ws_bytes, cudaStream_t stream);
 
 /* Critical-index-set reuse with dilation (Fig. 2, Fig. 4, Fig. 8, Table VIII).
  * Per query head: c = <q, q_anchor> / (|q| |q_anchor|); the decision is the
@@ -134,12 +143,15 @@ prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* 
  * When reuse: idx = union over anchor entries a of [a - w, a + w] clipped to
  * [0, t_b), ascending without repeats, n_sel its size (<= cap required).
  * When not: idx and n_sel rows are left untouched. reuse [B][Hq] is always
- * written. anchor_idx rows must be ascending and inside [0, t_b). */
+ * written. anchor_idx rows must be ascending and inside [0, t_b).
+ * Forced keys (n_sink, window as in prhs_score_select): the dilated set is
+ * united with [0, n_sink) and [t_b - window, t_b) (clipped), still ascending
+ * without repeats; cap >= min(t_max, anchor_cap * (2w + 1) + n_sink + window). */
 prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx,
                             const int32_t* anchor_n, int anchor_cap, const void* q,
-                            const void* q_anchor, int w, double tau, int max_run,
-                            int32_t* anchor_age, int32_t* idx, int32_t* n_sel, int cap,
-                            uint8_t* reuse, cudaStream_t stream);
+                            const void* q_anchor, int w, int n_sink, int window, double tau,
+                            int max_run, int32_t* anchor_age, int32_t* idx, int32_t* n_sel,
+                            int cap, uint8_t* reuse, cudaStream_t stream);
 
 /* Dropped attention mass of given index sets under the current query (a
  * diagnostic for reuse steps, whose set was not selected under this query;
@@ -199,14 +211,24 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
  * Heads that reuse attend the dilated anchor set; the others retrieve a fresh
  * top-N set, attend it and make it (with q) the new anchor. delta is written
  * for retrieving heads only. Start a sequence with anchor_n (and anchor_age)
- * all zero; max_run and anchor_age as in prhs_cis_dilate. */
+ * all zero; max_run and anchor_age as in prhs_cis_dilate; n_sink and window
+ * (forced keys) as in prhs_score_select and prhs_cis_dilate. */
 prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int N,
-                             const int32_t* n_budget, int w, double tau, int max_run,
-                             int32_t* anchor_age, int32_t* anchor_idx, int32_t* anchor_n,
-                             int anchor_cap,
-                             void* q_anchor, int32_t* idx, int32_t* n_sel, int cap,
-                             uint8_t* reuse, float* delta, float* out, float* lse,
-                             void* ws, size_t ws_bytes, cudaStream_t stream);
+                             const int32_t* n_budget, int n_sink, int window, int w, double tau,
+                             int max_run, int32_t* anchor_age, int32_t* anchor_idx,
+                             int32_t* anchor_n, int anchor_cap, void* q_anchor, int32_t* idx,
+                             int32_t* n_sel, int cap, uint8_t* reuse, float* delta, float* out,
+                             float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Grow the cache by one key per sequence (decoding appends the current
+ * token's key and value before it attends): for every sequence b and KV head
+ * h, k_new[b][h][:] and v_new[b][h][:] (device, [B][Hkv][d], the cache's
+ * element type) are written at position seq_lens[b] of the cache, then
+ * seq_lens[b] (the descriptor's device array) is advanced by one. A paged
+ * cache must already map that position to a page. A sequence whose length
+ * is already t_max is left as it is and flagged (PRHS_DEV_CAPACITY). */
+prhs_status prhs_append_kv(const prhs_kv* kv, const void* k_new, const void* v_new,
+                           cudaStream_t stream);
 
 /* Synchronise the current device, read and clear the device error word.
  * PRHS_OK when it was zero, PRHS_EDEVICE otherwise, PRHS_ECUDA when the

@@ -22,7 +22,8 @@ DEV_TIMEOUT, DEV_BAD_INDEX, DEV_BAD_LEN, DEV_BAD_BLOCK, DEV_CAPACITY = 1, 2, 4, 
 # Entry points declared in include/prhs.h, in declaration order.
 EXPORTS = ["prhs_workspace_size", "prhs_workspace_init", "prhs_score_select", "prhs_score",
            "prhs_select", "prhs_cis_dilate",
-           "prhs_sparse_attn", "prhs_sparse_attn_noalloc", "prhs_set_mass", "prhs_dense_attn", "prhs_decode_step", "prhs_last_error",
+           "prhs_sparse_attn", "prhs_sparse_attn_noalloc", "prhs_set_mass", "prhs_dense_attn",
+           "prhs_decode_step", "prhs_append_kv", "prhs_last_error",
            "prhs_device_error_bits", "prhs_status_str", "prhs_last_message", "prhs_num_sms"]
 
 
@@ -57,15 +58,17 @@ def load(path: str | None = None) -> ctypes.CDLL:
     sig = {
         "prhs_workspace_size": (Z, [KV, I]),
         "prhs_workspace_init": (I, [P, Z, P]),
-        "prhs_score_select": (I, [KV, P, F, I, P, P, P, P, I, P, P, P, I, P, P, Z, P]),
+        "prhs_score_select": (I, [KV, P, F, I, P, I, I, P, P, P, I, P, P, P, I, P, P, Z, P]),
         "prhs_score": (I, [KV, P, F, P, P, Z, P]),
-        "prhs_select": (I, [KV, P, I, P, P, P, P, I, P, P, P, I, P, P, Z, P]),
-        "prhs_cis_dilate": (I, [KV, P, P, I, P, P, I, D, I, P, P, P, I, P, P]),
+        "prhs_select": (I, [KV, P, I, P, I, I, P, P, P, I, P, P, P, I, P, P, Z, P]),
+        "prhs_cis_dilate": (I, [KV, P, P, I, P, P, I, I, I, D, I, P, P, P, I, P, P]),
         "prhs_sparse_attn": (I, [KV, P, F, P, P, I, P, P, P, Z, P]),
         "prhs_sparse_attn_noalloc": (I, [KV, P, F, P, P, I, P, P, P]),
         "prhs_set_mass": (I, [KV, P, F, P, P, I, P, P, Z, P]),
         "prhs_dense_attn": (I, [KV, P, F, P, P, P, Z, P]),
-        "prhs_decode_step": (I, [KV, P, F, I, P, I, D, I, P, P, P, I, P, P, P, I, P, P, P, P, P, Z, P]),
+        "prhs_decode_step": (I, [KV, P, F, I, P, I, I, I, D, I, P, P, P, I, P, P, P, I, P, P, P, P, P, Z,
+                                 P]),
+        "prhs_append_kv": (I, [KV, P, P, P]),
         "prhs_last_error": (I, []),
         "prhs_device_error_bits": (ctypes.c_uint, []),
         "prhs_status_str": (ctypes.c_char_p, [I]),
@@ -173,10 +176,12 @@ def make_workspace(kv: KVCache, cap: int = 0, stream=None):
 
 
 def score_select(kv, q, scale, N, idx, n_sel, delta, ws, *, n_budget=None, head_skip=None,
-                 anchor_idx=None, anchor_n=None, q_anchor=None, stream=None) -> None:
+                 anchor_idx=None, anchor_n=None, q_anchor=None, n_sink=0, window=0,
+                 stream=None) -> None:
     cap = idx.shape[-1]
     acap = anchor_idx.shape[-1] if anchor_idx is not None else 0
     _check(load().prhs_score_select(kv.ref(), _ptr(q), float(scale), int(N), _ptr(n_budget),
+                                    int(n_sink), int(window),
                                     _ptr(head_skip), _ptr(idx), _ptr(n_sel), cap, _ptr(delta),
                                     _ptr(anchor_idx), _ptr(anchor_n), acap, _ptr(q_anchor),
                                     _ptr(ws), ws.numel(), _stream(stream)), "score_select")
@@ -188,19 +193,21 @@ def score(kv, q, scale, ws, *, head_skip=None, stream=None) -> None:
 
 
 def select(kv, q, N, idx, n_sel, delta, ws, *, n_budget=None, head_skip=None, anchor_idx=None,
-           anchor_n=None, q_anchor=None, stream=None) -> None:
+           anchor_n=None, q_anchor=None, n_sink=0, window=0, stream=None) -> None:
     cap = idx.shape[-1]
     acap = anchor_idx.shape[-1] if anchor_idx is not None else 0
-    _check(load().prhs_select(kv.ref(), _ptr(q), int(N), _ptr(n_budget), _ptr(head_skip),
+    _check(load().prhs_select(kv.ref(), _ptr(q), int(N), _ptr(n_budget), int(n_sink), int(window),
+                              _ptr(head_skip),
                               _ptr(idx), _ptr(n_sel), cap, _ptr(delta), _ptr(anchor_idx),
                               _ptr(anchor_n), acap, _ptr(q_anchor), _ptr(ws), ws.numel(),
                               _stream(stream)), "select")
 
 
 def cis_dilate(kv, anchor_idx, anchor_n, q, q_anchor, w, tau, idx, n_sel, reuse, *, max_run=0,
-               anchor_age=None, stream=None) -> None:
+               anchor_age=None, n_sink=0, window=0, stream=None) -> None:
     _check(load().prhs_cis_dilate(kv.ref(), _ptr(anchor_idx), _ptr(anchor_n), anchor_idx.shape[-1],
-                                  _ptr(q), _ptr(q_anchor), int(w), float(tau), int(max_run),
+                                  _ptr(q), _ptr(q_anchor), int(w), int(n_sink), int(window),
+                                  float(tau), int(max_run),
                                   _ptr(anchor_age), _ptr(idx), _ptr(n_sel), idx.shape[-1],
                                   _ptr(reuse), _stream(stream)), "cis_dilate")
 
@@ -231,13 +238,21 @@ def dense_attn(kv, q, scale, out, lse, ws, stream=None) -> None:
 
 
 def decode_step(kv, q, scale, N, w, tau, anchor_idx, anchor_n, q_anchor, idx, n_sel, reuse, delta,
-                out, lse, ws, *, n_budget=None, max_run=0, anchor_age=None, stream=None) -> None:
-    _check(load().prhs_decode_step(kv.ref(), _ptr(q), float(scale), int(N), _ptr(n_budget), int(w),
+                out, lse, ws, *, n_budget=None, max_run=0, anchor_age=None, n_sink=0, window=0,
+                stream=None) -> None:
+    _check(load().prhs_decode_step(kv.ref(), _ptr(q), float(scale), int(N), _ptr(n_budget),
+                                   int(n_sink), int(window), int(w),
                                    float(tau), int(max_run), _ptr(anchor_age), _ptr(anchor_idx),
                                    _ptr(anchor_n),
                                    anchor_idx.shape[-1], _ptr(q_anchor), _ptr(idx), _ptr(n_sel),
                                    idx.shape[-1], _ptr(reuse), _ptr(delta), _ptr(out), _ptr(lse),
                                    _ptr(ws), ws.numel(), _stream(stream)), "decode_step")
+
+
+def append_kv(kv, k_new, v_new, stream=None) -> None:
+    """Write one key and value row per (sequence, KV head) at each
+    sequence's current length and advance kv.seq_lens (prhs_append_kv)."""
+    _check(load().prhs_append_kv(kv.ref(), _ptr(k_new), _ptr(v_new), _stream(stream)), "append_kv")
 
 
 def last_error() -> int:

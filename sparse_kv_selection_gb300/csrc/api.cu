@@ -267,7 +267,8 @@ prhs_status do_score(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* w
 }
 
 prhs_status do_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws,
-                      const void* q, int N, const int32_t* n_budget, const uint8_t* head_skip,
+                      const void* q, int N, const int32_t* n_budget, int n_sink, int window,
+                      const uint8_t* head_skip,
                       int32_t* idx, int32_t* n_sel, int cap, float* delta, int32_t* anchor_idx,
                       int32_t* anchor_n, int anchor_cap, void* q_anchor, cudaStream_t st) {
   SelectLaunch se;
@@ -285,18 +286,20 @@ prhs_status do_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* 
   se.anchor_cap = anchor_cap;
   se.q = q;
   se.q_anchor = q_anchor;
+  se.n_sink = n_sink;
+  se.window = window;
   return launch_result(launch_select(se, st), "select kernel");
 }
 
 prhs_status do_score_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws,
                             const void* q, float scale, int N, const int32_t* n_budget,
-                            const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
+                            int n_sink, int window, const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
                             float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
                             void* q_anchor, cudaStream_t st) {
   prhs_status s = do_score(kv, di, L, ws, q, scale, head_skip, st);
   if (s != PRHS_OK) return s;
-  return do_select(kv, di, L, ws, q, N, n_budget, head_skip, idx, n_sel, cap, delta, anchor_idx,
-                   anchor_n, anchor_cap, q_anchor, st);
+  return do_select(kv, di, L, ws, q, N, n_budget, n_sink, window, head_skip, idx, n_sel, cap, delta,
+                   anchor_idx, anchor_n, anchor_cap, q_anchor, st);
 }
 
 // Host checks shared by the selection entry points.
@@ -351,8 +354,8 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
 
 prhs_status do_cis(const prhs_kv& kv, DeviceInfo* di, const int32_t* anchor_idx,
                    const int32_t* anchor_n, int anchor_cap, const void* q, const void* q_anchor,
-                   int w, double tau, int max_run, int32_t* anchor_age, int32_t* idx,
-                   int32_t* n_sel, int cap, uint8_t* reuse, cudaStream_t st) {
+                   int w, int n_sink, int window, double tau, int max_run, int32_t* anchor_age,
+                   int32_t* idx, int32_t* n_sel, int cap, uint8_t* reuse, cudaStream_t st) {
   CisLaunch c;
   c.kv = view_of(kv, di->err);
   c.anchor_idx = anchor_idx;
@@ -368,13 +371,56 @@ prhs_status do_cis(const prhs_kv& kv, DeviceInfo* di, const int32_t* anchor_idx,
   c.n_sel = n_sel;
   c.cap = cap;
   c.reuse = reuse;
+  c.n_sink = n_sink;
+  c.window = window;
   return launch_result(launch_cis(c, st), "cis kernel");
 }
 
-bool dilated_fits(long long anchor_cap, int w, int tmax, int cap) {
-  long long need = anchor_cap * (2ll * w + 1);
+bool dilated_fits(long long anchor_cap, int w, int tmax, int cap, int forced = 0) {
+  long long need = anchor_cap * (2ll * w + 1) + forced;
   if (need > tmax) need = tmax;
   return need <= cap;
+}
+
+// Forced keys (sinks and window): non-negative, and selection with forced
+// keys runs only where a head's logits fit one CTA or a cluster.
+prhs_status check_forced(const prhs_kv& kv, int n_sink, int window) {
+  if (n_sink < 0 || window < 0)
+    return fail(PRHS_EINVAL, "n_sink and window must be >= 0 (got %d, %d)", n_sink, window);
+  if ((n_sink > 0 || window > 0) && (long long)t_max_of(kv) > 8ll * SELECT_SLICE_MAX)
+    return fail(PRHS_EUNSUPPORTED, "forced keys with t_max above %d", 8 * SELECT_SLICE_MAX);
+  return PRHS_OK;
+}
+
+// After a selection with forced keys: the attended set (sinks, the middle
+// top-N kept in the anchor rows, window) into idx / n_sel, and its dropped
+// mass over the logits still in the workspace into delta.
+prhs_status forced_finish(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws,
+                          const uint8_t* head_skip, const int32_t* anchor_idx,
+                          const int32_t* anchor_n, int anchor_cap, int32_t* idx, int32_t* n_sel,
+                          int cap, float* delta, int n_sink, int window, cudaStream_t st) {
+  ComposeLaunch c;
+  c.kv = view_of(kv, di->err);
+  c.head_skip = head_skip;
+  c.anchor_idx = anchor_idx;
+  c.anchor_n = anchor_n;
+  c.anchor_cap = anchor_cap;
+  c.idx = idx;
+  c.n_sel = n_sel;
+  c.cap = cap;
+  c.n_sink = n_sink;
+  c.window = window;
+  prhs_status s = launch_result(launch_compose(c, st), "compose kernel");
+  if (s != PRHS_OK) return s;
+  MassLaunch m;
+  m.kv = view_of(kv, di->err);
+  m.scores = reinterpret_cast<const float*>(static_cast<const char*>(ws) + L.scores);
+  m.idx = idx;
+  m.n_sel = n_sel;
+  m.cap = cap;
+  m.delta = delta;
+  m.head_skip = head_skip;
+  return launch_result(launch_mass(m, st), "set mass kernel");
 }
 
 }  // namespace
@@ -416,21 +462,29 @@ prhs_status prhs_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) 
 }
 
 prhs_status prhs_score_select(const prhs_kv* kv, const void* q, float scale, int N,
-                              const int32_t* n_budget, const uint8_t* head_skip, int32_t* idx,
-                              int32_t* n_sel, int cap, float* delta, int32_t* anchor_idx,
-                              int32_t* anchor_n, int anchor_cap, void* q_anchor, void* ws,
-                              size_t ws_bytes, cudaStream_t stream) {
+                              const int32_t* n_budget, int n_sink, int window,
+                              const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
+                              float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
+                              void* q_anchor, void* ws, size_t ws_bytes, cudaStream_t stream) {
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
   if ((s = check_select_args(*kv, q, N, n_budget, idx, n_sel, cap, delta, anchor_idx, anchor_n,
                              anchor_cap, q_anchor)) != PRHS_OK)
     return s;
+  if ((s = check_forced(*kv, n_sink, window)) != PRHS_OK) return s;
+  const bool forced = n_sink > 0 || window > 0;
+  if (forced && anchor_idx == nullptr) return fail(PRHS_EINVAL, "forced keys need the anchor buffers");
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
   Layout L;
   if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
-  return do_score_select(*kv, di, L, ws, q, scale, N, n_budget, head_skip, idx, n_sel, cap, delta,
-                         anchor_idx, anchor_n, anchor_cap, q_anchor, stream);
+  if ((s = do_score_select(*kv, di, L, ws, q, scale, N, n_budget, n_sink, window, head_skip, idx,
+                           n_sel, cap, delta, anchor_idx, anchor_n, anchor_cap, q_anchor,
+                           stream)) != PRHS_OK)
+    return s;
+  if (!forced) return PRHS_OK;
+  return forced_finish(*kv, di, L, ws, head_skip, anchor_idx, anchor_n, anchor_cap, idx, n_sel, cap,
+                       delta, n_sink, window, stream);
 }
 
 prhs_status prhs_score(const prhs_kv* kv, const void* q, float scale, const uint8_t* head_skip,
@@ -470,26 +524,34 @@ prhs_status prhs_set_mass(const prhs_kv* kv, const void* q, float scale, const i
 }
 
 prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* n_budget,
-                        const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
-                        float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
-                        void* q_anchor, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                        int n_sink, int window, const uint8_t* head_skip, int32_t* idx,
+                        int32_t* n_sel, int cap, float* delta, int32_t* anchor_idx,
+                        int32_t* anchor_n, int anchor_cap, void* q_anchor, void* ws,
+                        size_t ws_bytes, cudaStream_t stream) {
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
   if ((s = check_select_args(*kv, q, N, n_budget, idx, n_sel, cap, delta, anchor_idx, anchor_n,
                              anchor_cap, q_anchor)) != PRHS_OK)
     return s;
+  if ((s = check_forced(*kv, n_sink, window)) != PRHS_OK) return s;
+  const bool forced = n_sink > 0 || window > 0;
+  if (forced && anchor_idx == nullptr) return fail(PRHS_EINVAL, "forced keys need the anchor buffers");
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
   Layout L;
   if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
-  return do_select(*kv, di, L, ws, q, N, n_budget, head_skip, idx, n_sel, cap, delta, anchor_idx,
-                   anchor_n, anchor_cap, q_anchor, stream);
+  if ((s = do_select(*kv, di, L, ws, q, N, n_budget, n_sink, window, head_skip, idx, n_sel, cap,
+                     delta, anchor_idx, anchor_n, anchor_cap, q_anchor, stream)) != PRHS_OK)
+    return s;
+  if (!forced) return PRHS_OK;
+  return forced_finish(*kv, di, L, ws, head_skip, anchor_idx, anchor_n, anchor_cap, idx, n_sel, cap,
+                       delta, n_sink, window, stream);
 }
 
 prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx, const int32_t* anchor_n,
-                            int anchor_cap, const void* q, const void* q_anchor, int w, double tau,
-                            int max_run, int32_t* anchor_age, int32_t* idx, int32_t* n_sel, int cap,
-                            uint8_t* reuse, cudaStream_t stream) {
+                            int anchor_cap, const void* q, const void* q_anchor, int w, int n_sink,
+                            int window, double tau, int max_run, int32_t* anchor_age, int32_t* idx,
+                            int32_t* n_sel, int cap, uint8_t* reuse, cudaStream_t stream) {
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
   if ((q && !aligned16(q)) || (q_anchor && !aligned16(q_anchor)))
@@ -500,12 +562,14 @@ prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx, const 
   if (max_run < 0) return fail(PRHS_EINVAL, "max_run must be >= 0 (got %d)", max_run);
   if (max_run > 0 && anchor_age == nullptr) return fail(PRHS_EINVAL, "max_run > 0 needs anchor_age");
   if (anchor_cap <= 0 || cap <= 0) return fail(PRHS_EINVAL, "capacities must be positive");
-  if (!dilated_fits(anchor_cap, w, t_max_of(*kv), cap))
-    return fail(PRHS_EINVAL, "cap %d < min(t_max, anchor_cap * (2w + 1))", cap);
+  if (n_sink < 0 || window < 0)
+    return fail(PRHS_EINVAL, "n_sink and window must be >= 0 (got %d, %d)", n_sink, window);
+  if (!dilated_fits(anchor_cap, w, t_max_of(*kv), cap, n_sink + window))
+    return fail(PRHS_EINVAL, "cap %d < min(t_max, anchor_cap * (2w + 1) + n_sink + window)", cap);
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
-  return do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, tau, max_run,
-                anchor_age, idx, n_sel, cap, reuse, stream);
+  return do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, n_sink, window, tau,
+                max_run, anchor_age, idx, n_sel, cap, reuse, stream);
 }
 
 prhs_status prhs_sparse_attn(const prhs_kv* kv, const void* q, float scale, const int32_t* idx,
@@ -549,7 +613,8 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
 }
 
 prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int N,
-                             const int32_t* n_budget, int w, double tau, int max_run,
+                             const int32_t* n_budget, int n_sink, int window, int w, double tau,
+                             int max_run,
                              int32_t* anchor_age, int32_t* anchor_idx,
                              int32_t* anchor_n, int anchor_cap, void* q_anchor, int32_t* idx,
                              int32_t* n_sel, int cap, uint8_t* reuse, float* delta, float* out,
@@ -567,14 +632,16 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if (anchor_cap <= 0 || cap <= 0) return fail(PRHS_EINVAL, "capacities must be positive");
   if (n_budget == nullptr && anchor_cap < (N < tmax ? N : tmax))
     return fail(PRHS_EINVAL, "anchor_cap %d < budget", anchor_cap);
-  if (!dilated_fits(anchor_cap, w, tmax, cap))
-    return fail(PRHS_EINVAL, "cap %d < min(t_max, anchor_cap * (2w + 1))", cap);
+  if ((s = check_forced(*kv, n_sink, window)) != PRHS_OK) return s;
+  const bool forced = n_sink > 0 || window > 0;
+  if (!dilated_fits(anchor_cap, w, tmax, cap, n_sink + window))
+    return fail(PRHS_EINVAL, "cap %d < min(t_max, anchor_cap * (2w + 1) + n_sink + window)", cap);
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
   Layout L;
   if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
-  if ((s = do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, tau, max_run,
-                  anchor_age, idx, n_sel, cap, reuse, stream)) != PRHS_OK)
+  if ((s = do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, n_sink, window, tau,
+                  max_run, anchor_age, idx, n_sel, cap, reuse, stream)) != PRHS_OK)
     return s;
   // Two branches after the gate: heads that reuse their anchor only need the
   // dilated sets and attend on the side stream, while the retrieving heads
@@ -586,16 +653,35 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if ((s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, di->side, reuse, 1,
                    true, 0, ATTN_SIDE_MIN_ROWS)) != PRHS_OK)
     return s;
-  if ((s = do_score_select(*kv, di, L, ws, q, scale, N, n_budget, reuse, idx, n_sel, cap, delta,
-                           anchor_idx, anchor_n, anchor_cap, q_anchor, stream)) != PRHS_OK)
+  if ((s = do_score_select(*kv, di, L, ws, q, scale, N, n_budget, n_sink, window, reuse, idx,
+                           n_sel, cap, delta, anchor_idx, anchor_n, anchor_cap, q_anchor,
+                           stream)) != PRHS_OK)
     return s;
-  // the retrieving heads' sets hold at most anchor_cap rows
+  if (forced && (s = forced_finish(*kv, di, L, ws, reuse, anchor_idx, anchor_n, anchor_cap, idx,
+                                   n_sel, cap, delta, n_sink, window, stream)) != PRHS_OK)
+    return s;
+  // the retrieving heads' sets hold at most anchor_cap (+ forced) rows
   if ((s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, stream, reuse, 0,
-                   false, 0, ATTN_MIN_ROWS, anchor_cap)) != PRHS_OK)
+                   false, 0, ATTN_MIN_ROWS, anchor_cap + n_sink + window)) != PRHS_OK)
     return s;
   e = cudaEventRecord(di->join, di->side);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, di->join, 0);
   return e == cudaSuccess ? PRHS_OK : cuda_fail(e, "decode: join");
+}
+
+prhs_status prhs_append_kv(const prhs_kv* kv, const void* k_new, const void* v_new,
+                           cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if (!k_new || !v_new) return fail(PRHS_EINVAL, "append: null pointer argument");
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  AppendLaunch a;
+  a.kv = view_of(*kv, di->err);
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.seq_lens = const_cast<int32_t*>(kv->seq_lens);
+  return launch_result(launch_append(a, stream), "append kernel");
 }
 
 prhs_status prhs_last_error(void) {

@@ -112,7 +112,13 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   }
   int32_t* out = a.idx + (long long)qh * a.cap;
   const int w = a.w;
-  int carry = 0;
+  // forced keys: sinks [0, ns) first, the window after the dilated entries
+  const int ns = min(max(a.n_sink, 0), t);
+  for (int i = tid; i < ns; i += CIS_THREADS) {
+    if (i < a.cap) out[i] = i;
+    else raise_error(kv.err, PRHS_DEV_CAPACITY);
+  }
+  int carry = ns;
   for (int base = 0; base < n; base += CHUNK) {
     const int j0 = base + tid * CIS_PER;
     if (base > 0) {
@@ -134,7 +140,7 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
         } else {
           const int lo = max(0, xv - w);
           const int hi = min(t - 1, xv + w);
-          const int prev_hi = j0 + k > 0 ? min(t - 1, prev + w) : -1;
+          const int prev_hi = max(ns - 1, j0 + k > 0 ? min(t - 1, prev + w) : -1);
           start[k] = max(lo, prev_hi + 1);
           cnt[k] = max(0, hi - start[k] + 1);
         }
@@ -173,6 +179,18 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
     carry += total;
     if (base + CHUNK < n) __syncthreads();  // warp_tot is reused by the next chunk
   }
+  // the window: past both the sinks and the last dilated interval
+  int last = ns - 1;
+  if (n > 0) {
+    const int xl = anc[n - 1];
+    if (xl >= 0 && xl < t) last = max(last, min(t - 1, xl + w));
+  }
+  const int wstart = max(max(ns, t - max(a.window, 0)), last + 1);
+  for (int i = tid; i < t - wstart; i += CIS_THREADS) {
+    if (carry + i < a.cap) out[carry + i] = wstart + i;
+    else raise_error(kv.err, PRHS_DEV_CAPACITY);
+  }
+  carry += max(0, t - wstart);
   if (tid == 0) a.n_sel[qh] = min(carry, a.cap);
 }
 

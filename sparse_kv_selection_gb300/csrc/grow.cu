@@ -1,0 +1,87 @@
+// Decode on a growing cache with forced keys.
+// "Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference":
+// Fig. 11 (attention sinks and the most recent positions take attention mass
+// for every query), read as a deterministic set that every query attends on
+// top of its selected or shared keys, while the cache gains one key per
+// decode query.
+//
+// compose_kernel: the attended set of a retrieving head = the first n_sink
+// keys, the head's middle top-N set (kept in its anchor row by selection,
+// which ranks only the keys between the forced ones), and the last `window`
+// keys; ascending because the three ranges are disjoint and ordered.
+// append_kernel: one CTA per sequence writes its new key and value rows for
+// every KV head at position seq_lens[b], then advances seq_lens[b].
+#include "kernels.h"
+
+namespace prhs {
+
+constexpr int GROW_THREADS = 128;
+
+__global__ void __launch_bounds__(GROW_THREADS) compose_kernel(const ComposeLaunch a) {
+  pdl_wait();
+  pdl_trigger();
+  const KVView& kv = a.kv;
+  const int qh = blockIdx.x, b = qh / kv.Hq;
+  if (a.head_skip != nullptr && a.head_skip[qh] != 0) return;
+  const int t = seq_len(kv, b);
+  const int ns = min(max(a.n_sink, 0), t);
+  const int we = max(ns, t - max(a.window, 0));
+  int nm = a.anchor_n[qh];
+  if (nm < 0 || nm > a.anchor_cap || nm > we - ns) {
+    if (threadIdx.x == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
+    nm = max(0, min(nm, min(a.anchor_cap, we - ns)));
+  }
+  const int total = ns + nm + (t - we);
+  if (total > a.cap && threadIdx.x == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
+  const int32_t* mid = a.anchor_idx + (long long)qh * a.anchor_cap;
+  int32_t* out = a.idx + (long long)qh * a.cap;
+  for (int p = threadIdx.x; p < min(total, a.cap); p += GROW_THREADS) {
+    int key;
+    if (p < ns) key = p;
+    else if (p < ns + nm) key = mid[p - ns];
+    else key = we + (p - ns - nm);
+    out[p] = key;
+  }
+  if (threadIdx.x == 0) a.n_sel[qh] = min(total, a.cap);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(GROW_THREADS) append_kernel(const AppendLaunch a) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int sh_pos;
+  const KVView& kv = a.kv;
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) sh_pos = a.seq_lens[b];
+  __syncthreads();
+  const int pos = sh_pos;
+  if (pos < 0 || pos >= kv.t_max) {  // no room: flagged, nothing written
+    if (threadIdx.x == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
+    return;
+  }
+  for (int x = threadIdx.x; x < kv.Hkv * kv.d; x += GROW_THREADS) {
+    const int h = x / kv.d, e = x % kv.d;
+    const long long row = kv_row(kv, b, h, pos);
+    if (row < 0) {
+      raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
+      continue;
+    }
+    const long long src = ((long long)b * kv.Hkv + h) * kv.d + e;
+    static_cast<T*>(const_cast<void*>(kv.k))[row * kv.d + e] = static_cast<const T*>(a.k_new)[src];
+    static_cast<T*>(const_cast<void*>(kv.v))[row * kv.d + e] = static_cast<const T*>(a.v_new)[src];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) a.seq_lens[b] = pos + 1;
+}
+
+cudaError_t launch_compose(const ComposeLaunch& a, cudaStream_t st) {
+  return launch_pdl(compose_kernel, dim3(a.kv.B * a.kv.Hq), dim3(GROW_THREADS), 0, st, a);
+}
+
+cudaError_t launch_append(const AppendLaunch& a, cudaStream_t st) {
+  if (a.kv.dtype == PRHS_BF16)
+    return launch_pdl(append_kernel<__nv_bfloat16>, dim3(a.kv.B), dim3(GROW_THREADS), 0, st, a);
+  return launch_pdl(append_kernel<float>, dim3(a.kv.B), dim3(GROW_THREADS), 0, st, a);
+}
+
+}  // namespace prhs

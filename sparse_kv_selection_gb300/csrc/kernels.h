@@ -49,6 +49,8 @@ struct SelectLaunch {
   int anchor_cap;
   const void* q;
   void* q_anchor;
+  int n_sink;  // forced keys are left out of the ranking (the caller adds them)
+  int window;
 };
 
 struct CisLaunch {
@@ -66,6 +68,8 @@ struct CisLaunch {
   int32_t* n_sel;
   int cap;
   uint8_t* reuse;
+  int n_sink;            // forced keys: the first n_sink and the last `window` of each cache
+  int window;
 };
 
 // A CTA of the attention kernels takes at least this many rows: below it the
@@ -103,8 +107,35 @@ struct MassLaunch {
   const int32_t* n_sel;
   int cap;
   float* delta;
+  const uint8_t* head_skip = nullptr;  // heads with a nonzero flag are left untouched
 };
 cudaError_t launch_mass(const MassLaunch& a, cudaStream_t s);
+
+// Attended set of a retrieving head with forced keys: the first n_sink keys,
+// the head's middle top-N set (its anchor row) and the last `window` keys.
+struct ComposeLaunch {
+  KVView kv;
+  const uint8_t* head_skip;
+  const int32_t* anchor_idx;
+  const int32_t* anchor_n;
+  int anchor_cap;
+  int32_t* idx;
+  int32_t* n_sel;
+  int cap;
+  int n_sink;
+  int window;
+};
+cudaError_t launch_compose(const ComposeLaunch& a, cudaStream_t s);
+
+// Appends one key and value row per (sequence, KV head) at position
+// seq_lens[b] and increments seq_lens[b].
+struct AppendLaunch {
+  KVView kv;
+  const void* k_new;  // [B][Hkv][d]
+  const void* v_new;
+  int32_t* seq_lens;
+};
+cudaError_t launch_append(const AppendLaunch& a, cudaStream_t s);
 
 // Units of the attention split (query heads when sparse, KV heads when dense)
 // and the floats of partial records the kernel may write for `ctas` CTAs.

@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(MASS_THREADS) mass_kernel(const MassLaunch a) 
   pdl_trigger();
   const KVView& kv = a.kv;
   const int qh = blockIdx.x, b = qh / kv.Hq;
+  if (a.head_skip != nullptr && a.head_skip[qh] != 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t = seq_len(kv, b);
   const float* s = a.scores + (long long)qh * kv.t_max;

@@ -160,17 +160,22 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   int32_t* out = a.idx + (long long)qh * a.cap;
   int32_t* aout = a.anchor_idx != nullptr ? a.anchor_idx + (long long)qh * a.anchor_cap : nullptr;
   const int lo = min(t, rank * chunk), hi = min(t, lo + chunk), cnt = hi - lo;
+  // forced keys [0, ns) and [we, t) are left out of the ranking: the set is
+  // the top Nb of the middle keys [ns, we), written from position 0
+  const int ns = min(max(a.n_sink, 0), t);
+  const int we = max(ns, t - max(a.window, 0));
+  const int tmid = we - ns;
 
-  if (Nb >= t || Nb == 0) {  // keep everything (delta = 0) or nothing (delta = 1)
-    const int n = Nb >= t ? t : 0;
-    for (int i = lo + tid; i < min(hi, n); i += SEL_THREADS) {
-      out[i] = i;
-      if (aout) aout[i] = i;
+  if (Nb >= tmid || Nb == 0) {  // keep every middle key (delta = 0 without forced keys) or none
+    const int n = Nb >= tmid ? tmid : 0;
+    for (int i = max(lo, ns) + tid; i < min(hi, ns + n); i += SEL_THREADS) {
+      out[i - ns] = i;
+      if (aout) aout[i - ns] = i;
     }
     if (rank == 0) {
       if (tid == 0) {
         a.n_sel[qh] = n;
-        a.delta[qh] = n == t ? 0.f : 1.f;
+        a.delta[qh] = n == t ? 0.f : 1.f;  // recomputed over the whole set when keys are forced
         if (a.anchor_n) a.anchor_n[qh] = n;
       }
       if (a.q_anchor) mirror_query<T>(a, qh);
@@ -193,9 +198,12 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
     for (int k = 0; k < PRE; k++) {
       const int i = i0 + k * SEL_THREADS + tid;
       if (i < cnt) {
-        cache[i] = v[k];
-        vmin = fminf(vmin, v[k]);
-        vmax = fmaxf(vmax, v[k]);
+        const bool forced = lo + i < ns || lo + i >= we;  // ranked below every middle key
+        cache[i] = forced ? -INFINITY : v[k];
+        if (!forced) {
+          vmin = fminf(vmin, v[k]);
+          vmax = fmaxf(vmax, v[k]);
+        }
       }
     }
   }

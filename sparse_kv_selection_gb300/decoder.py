@@ -5,8 +5,11 @@ device and calls ``prhs_decode_step`` once per decode query: heads whose
 query is similar enough to their anchor attend the anchor set dilated by
 +/- w, the others retrieve a fresh top-N set and become the new anchor
 ("Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference",
-Fig. 4 and Fig. 8). Buffers are allocated once; a step launches four
-kernels and never synchronises with the host.
+Fig. 4 and Fig. 8). With n_sink / window every query also attends the first
+and the last keys of its cache (Fig. 11), and ``append`` grows the cache by
+one key per sequence before the next query. Buffers are allocated once; a
+step launches the gate, scoring, selection and two attention kernels (two
+more with forced keys) and never synchronises with the host.
 """
 from __future__ import annotations
 
@@ -17,7 +20,8 @@ from . import binding as _b
 
 class SparseDecoder:
     def __init__(self, kv: _b.KVCache, *, N: int | None = None, n_budget=None, w: int = 2,
-                 tau: float = 0.8, scale: float | None = None, max_run: int = 0, stream=None):
+                 tau: float = 0.8, scale: float | None = None, max_run: int = 0, n_sink: int = 0,
+                 window: int = 0, stream=None):
         dev = kv.k.device
         self.kv, self.w, self.tau = kv, int(w), float(tau)
         self.scale = scale if scale is not None else kv.desc.d ** -0.5
@@ -26,7 +30,8 @@ class SparseDecoder:
         nmax = self.N if n_budget is None else int(n_budget.max())
         tmax = kv.t_max
         self.anchor_cap = max(1, min(nmax, tmax))
-        self.cap = max(1, min(tmax, self.anchor_cap * (2 * self.w + 1)))
+        self.n_sink, self.window = int(n_sink), int(window)
+        self.cap = max(1, min(tmax, self.anchor_cap * (2 * self.w + 1) + self.n_sink + self.window))
         B, Hq, d = kv.B, kv.Hq, kv.desc.d
         qdt = kv.k.dtype
         i32 = dict(device=dev, dtype=torch.int32)
@@ -61,7 +66,13 @@ class SparseDecoder:
                        self.out if out is None else out,
                        self.lse if lse is None else lse,
                        self.ws, n_budget=self.n_budget, max_run=self.max_run,
-                       anchor_age=self.anchor_age, stream=self.stream)
+                       anchor_age=self.anchor_age, n_sink=self.n_sink, window=self.window,
+                       stream=self.stream)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor) -> None:
+        """Grow the cache by one key per sequence ([B][Hkv][d] device rows,
+        the cache's element type) before the next query attends."""
+        _b.append_kv(self.kv, k_new, v_new, stream=self.stream)
 
     def run(self, q_steps: torch.Tensor, outs=None):
         """Decode a [S][B][Hq][d] device sequence; returns stacked per-step

@@ -78,26 +78,38 @@ def test_descriptor_rejected_on_host(lib, over, status):
 def test_null_arguments_rejected(lib):
     from sparse_kv_selection_gb300 import binding
     kv = _kv(binding)
-    assert lib.prhs_score_select(None, 64, 0.1, 8, None, None, 64, 64, 8, 64, None, None, 0,
+    assert lib.prhs_score_select(None, 64, 0.1, 8, None, 0, 0, None, 64, 64, 8, 64, None, None, 0,
                                  None, 256, 1 << 20, None) == binding.PRHS_EINVAL
     # N <= 0 without a per-sequence budget
-    assert lib.prhs_score_select(ctypes.byref(kv), 64, 0.1, 0, None, None, 64, 64, 8, 64, None,
+    assert lib.prhs_score_select(ctypes.byref(kv), 64, 0.1, 0, None, 0, 0, None, 64, 64, 8, 64, None,
                                  None, 0, None, 256, 1 << 20, None) == binding.PRHS_EINVAL
     # capacity below the budget
-    assert lib.prhs_score_select(ctypes.byref(kv), 64, 0.1, 16, None, None, 64, 64, 8, 64, None,
+    assert lib.prhs_score_select(ctypes.byref(kv), 64, 0.1, 16, None, 0, 0, None, 64, 64, 8, 64, None,
                                  None, 0, None, 256, 1 << 20, None) == binding.PRHS_EINVAL
     # anchor buffers must come together
-    assert lib.prhs_score_select(ctypes.byref(kv), 64, 0.1, 8, None, None, 64, 64, 8, 64, 64,
+    assert lib.prhs_score_select(ctypes.byref(kv), 64, 0.1, 8, None, 0, 0, None, 64, 64, 8, 64, 64,
                                  None, 8, None, 256, 1 << 20, None) == binding.PRHS_EINVAL
+    # forced keys: non-negative, with the anchor buffers, and t_max <= 131072
+    assert lib.prhs_score_select(ctypes.byref(kv), 64, 0.1, 8, None, -1, 0, None, 64, 64, 8, 64, 64,
+                                 64, 8, 64, 256, 1 << 20, None) == binding.PRHS_EINVAL
+    assert lib.prhs_score_select(ctypes.byref(kv), 64, 0.1, 8, None, 2, 2, None, 64, 64, 8, 64, None,
+                                 None, 0, None, 256, 1 << 20, None) == binding.PRHS_EINVAL
+    big = _kv(binding, t_max=1 << 18)
+    assert lib.prhs_score_select(ctypes.byref(big), 64, 0.1, 8, None, 0, 4, None, 64, 64, 8, 64, 64,
+                                 64, 8, 64, 256, 1 << 20, None) == binding.PRHS_EUNSUPPORTED
+    assert lib.prhs_append_kv(ctypes.byref(kv), None, 64, None) == binding.PRHS_EINVAL
     # dilation radius and dilated capacity
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, -1, 0.8, 0, None, 64, 64, 64,
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, -1, 0, 0, 0.8, 0, None, 64, 64, 64,
                                64, None) == binding.PRHS_EINVAL
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0.8, 0, None, 64, 64, 39,
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 0, 0.8, 0, None, 64, 64, 39,
+                               64, None) == binding.PRHS_EINVAL
+    # the dilated capacity must hold the forced keys too
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 2, 2, 0.8, 0, None, 64, 64, 40,
                                64, None) == binding.PRHS_EINVAL
     # a bounded reuse run needs the per-head age counters; a negative bound is invalid
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0.8, 4, None, 64, 64, 64,
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 0, 0.8, 4, None, 64, 64, 64,
                                64, None) == binding.PRHS_EINVAL
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0.8, -1, 64, 64, 64, 64,
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 0, 0.8, -1, 64, 64, 64, 64,
                                64, None) == binding.PRHS_EINVAL
     assert lib.prhs_dense_attn(ctypes.byref(kv), None, 0.1, 64, 64, 256, 1 << 20, None) == binding.PRHS_EINVAL
     assert lib.prhs_workspace_init(None, 0, None) == binding.PRHS_EWORKSPACE

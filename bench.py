@@ -49,6 +49,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="host time budget of the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--grow", action="store_true",
+                   help="decode on a growing cache: every query appends its key and value first "
+                        "and attends the forced sinks and window too (not the bench line)")
+    p.add_argument("--n-sink", type=int, default=4)
+    p.add_argument("--window", type=int, default=64)
     p.add_argument("--kernels", action="store_true",
                    help="time each kernel alone on the workload (all heads retrieving) instead")
     p.add_argument("--only", default=None,
@@ -519,6 +524,121 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_grow(args):
+    """Growing-cache decode: the workload's last `steps` keys of each sequence
+    arrive one per query through prhs_append_kv, and every query attends the
+    first n_sink and the last `window` keys besides its selected or shared
+    set. With several rotating KV copies (caches smaller than twice the L2)
+    each query appends to every copy, each with its own lengths."""
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    import __graft_entry__ as entry
+    entry.build()
+    import sparse_kv_selection_gb300 as S
+    from workloads import preset
+    from workloads.torch_io import tensor_of, upload
+
+    wl = preset(args.config, seed=rank)
+    dev = upload(wl)
+    Sq, B, Hq, Hkv, d = wl.steps, wl.B, wl.Hq, wl.Hkv, wl.d
+    t0 = (wl.seq_lens.astype(np.int64) - Sq).astype(np.int32)
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    R = max(1, math.ceil(2 * l2 / wl.kv_bytes()))
+    t0_dev = torch.from_numpy(t0).cuda()
+    kvs = []
+    for r in range(R):
+        k = dev["k"] if r == 0 else dev["k"].clone()
+        v = dev["v"] if r == 0 else dev["v"].clone()
+        kvs.append(S.KVCache(k, v, t0_dev.clone(), Hq, block_table=dev["block_table"]))
+    rows = lambda which: np.stack([np.stack([np.stack([wl.logical_rows(which, b, h)[int(t0[b]) + s]
+                                                        for h in range(Hkv)]) for b in range(B)])
+                                   for s in range(Sq)])
+    new_k, new_v = tensor_of(rows("K"), wl.dtype, "cuda"), tensor_of(rows("V"), wl.dtype, "cuda")
+    varied = len(set(wl.budget.tolist())) > 1
+    N = 0 if varied else int(wl.budget[0])
+    nb = dev["budget"] if varied else None
+    acap = max(1, min(int(wl.budget.max()), kvs[0].t_max))
+    cap = max(1, min(kvs[0].t_max, acap * (2 * wl.w + 1) + args.n_sink + args.window))
+    i32 = dict(device="cuda", dtype=torch.int32)
+    anchor_idx = torch.zeros(B, Hq, acap, **i32)
+    anchor_n = torch.zeros(B, Hq, **i32)
+    q_anchor = torch.zeros_like(dev["q"][0])
+    idx = torch.zeros(B, Hq, cap, **i32)
+    n_sel = torch.zeros(B, Hq, **i32)
+    reuse = torch.zeros(Sq, B, Hq, device="cuda", dtype=torch.uint8)
+    delta = torch.zeros(B, Hq, device="cuda")
+    out = torch.zeros(B, Hq, d, device="cuda")
+    lse = torch.zeros(B, Hq, device="cuda")
+    ws = S.make_workspace(kvs[0], cap)
+
+    def enqueue():
+        anchor_n.zero_()
+        for kvr in kvs:
+            kvr.seq_lens.copy_(t0_dev)
+        for s in range(Sq):
+            for kvr in kvs:
+                S.binding.append_kv(kvr, new_k[s], new_v[s])
+            S.decode_step(kvs[s % R], dev["q"][s], wl.scale, N, wl.w, wl.tau, anchor_idx, anchor_n,
+                          q_anchor, idx, n_sel, reuse[s], delta, out, lse, ws, n_budget=nb,
+                          n_sink=args.n_sink, window=args.window)
+
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        enqueue()
+    torch.cuda.synchronize()
+    assert S.last_error() == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        enqueue()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            t0e.record()
+            for _ in range(args.steps):
+                graph.replay()
+            t1e.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    elapsed_ms = max_over_ranks(t0e.elapsed_time(t1e), world, "cuda")
+    assert S.last_error() == 0
+    assert kvs[0].seq_lens.cpu().numpy().tolist() == wl.seq_lens.tolist()
+    value = B * Hq * Sq * args.steps * world / (elapsed_ms / 1e3)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded clustered-key generator, AR(1) correlated queries)",
+            "mode": "grow",
+            "config": {"workload": workload_label(wl),
+                       "step": f"one decode sequence of {Sq} queries x {B * Hq} heads, each query "
+                               f"appending one key per sequence first",
+                       "grow": {"t_first": int(t0.max()) + 1, "t_last": int(wl.seq_lens.max()),
+                                "n_sink": args.n_sink, "window": args.window},
+                       "l2": f"{R} rotating KV copies, every copy appended per query",
+                       "fresh_retrieval_fraction": float(1.0 - reuse.float().mean().item())},
+            "gpu_launches": Sq * args.steps * (R + 7),
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def run_kernels(args):
     """Each kernel alone, every head retrieving: dense attention, scoring,
     selection and sparse attention over the fresh top-N sets and over their
@@ -632,6 +752,8 @@ def main():
         run_reference(args)
     elif args.kernels:
         run_kernels(args)
+    elif args.grow:
+        run_grow(args)
     else:
         run_ours(args)
 

@@ -223,7 +223,7 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
 /* Grow the cache by one key per sequence (decoding appends the current
  * token's key and value before it attends): for every sequence b and KV head
  * h, k_new[b][h][:] and v_new[b][h][:] (device, [B][Hkv][d], the cache's
- * element type) are written at position seq_lens[b] of the cache, then
+ * element type, 16-byte aligned) are written at position seq_lens[b] of the cache, then
  * seq_lens[b] (the descriptor's device array) is advanced by one. A paged
  * cache must already map that position to a page. A sequence whose length
  * is already t_max is left as it is and flagged (PRHS_DEV_CAPACITY). */

@@ -674,6 +674,7 @@ prhs_status prhs_append_kv(const prhs_kv* kv, const void* k_new, const void* v_n
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
   if (!k_new || !v_new) return fail(PRHS_EINVAL, "append: null pointer argument");
+  if (!aligned16(k_new) || !aligned16(v_new)) return fail(PRHS_EINVAL, "k_new and v_new must be 16-byte aligned");
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
   AppendLaunch a;

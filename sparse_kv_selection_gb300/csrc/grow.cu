@@ -10,7 +10,8 @@
 // which ranks only the keys between the forced ones), and the last `window`
 // keys; ascending because the three ranges are disjoint and ordered.
 // append_kernel: one CTA per sequence writes its new key and value rows for
-// every KV head at position seq_lens[b], then advances seq_lens[b].
+// every KV head at position seq_lens[b] in 16-byte pieces (all loads of a
+// thread issued before its stores), then advances seq_lens[b].
 #include "kernels.h"
 
 namespace prhs {
@@ -45,8 +46,11 @@ __global__ void __launch_bounds__(GROW_THREADS) compose_kernel(const ComposeLaun
   if (threadIdx.x == 0) a.n_sel[qh] = min(total, a.cap);
 }
 
+constexpr int APPEND_THREADS = 256;
+constexpr int APPEND_PER = 4;  // 16-byte pieces per thread, loaded before any is stored
+
 template <typename T>
-__global__ void __launch_bounds__(GROW_THREADS) append_kernel(const AppendLaunch a) {
+__global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendLaunch a) {
   pdl_wait();
   pdl_trigger();
   __shared__ int sh_pos;
@@ -59,18 +63,38 @@ __global__ void __launch_bounds__(GROW_THREADS) append_kernel(const AppendLaunch
     if (threadIdx.x == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
     return;
   }
-  for (int x = threadIdx.x; x < kv.Hkv * kv.d; x += GROW_THREADS) {
-    const int h = x / kv.d, e = x % kv.d;
-    const long long row = kv_row(kv, b, h, pos);
-    if (row < 0) {
-      raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
-      continue;
+  const int cpr = kv.d * (int)sizeof(T) / 16;  // 16-byte pieces per row
+  const int pieces = kv.Hkv * cpr;
+  const uint4* kn = static_cast<const uint4*>(a.k_new) + (long long)b * pieces;
+  const uint4* vn = static_cast<const uint4*>(a.v_new) + (long long)b * pieces;
+  uint4* kc = static_cast<uint4*>(const_cast<void*>(kv.k));
+  uint4* vc = static_cast<uint4*>(const_cast<void*>(kv.v));
+  for (int x0 = 0; x0 < pieces; x0 += APPEND_THREADS * APPEND_PER) {
+    uint4 kk[APPEND_PER], vv[APPEND_PER];
+    long long dst[APPEND_PER];
+#pragma unroll
+    for (int u = 0; u < APPEND_PER; u++) {
+      const int x = x0 + u * APPEND_THREADS + threadIdx.x;
+      dst[u] = -1;
+      if (x < pieces) {
+        const long long row = kv_row(kv, b, x / cpr, pos);
+        if (row < 0) {
+          raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
+          continue;
+        }
+        dst[u] = row * cpr + x % cpr;
+        kk[u] = kn[x];
+        vv[u] = vn[x];
+      }
     }
-    const long long src = ((long long)b * kv.Hkv + h) * kv.d + e;
-    static_cast<T*>(const_cast<void*>(kv.k))[row * kv.d + e] = static_cast<const T*>(a.k_new)[src];
-    static_cast<T*>(const_cast<void*>(kv.v))[row * kv.d + e] = static_cast<const T*>(a.v_new)[src];
+#pragma unroll
+    for (int u = 0; u < APPEND_PER; u++)
+      if (dst[u] >= 0) {
+        kc[dst[u]] = kk[u];
+        vc[dst[u]] = vv[u];
+      }
   }
-  __syncthreads();
+  __syncthreads();  // every piece of this sequence is written before its length moves
   if (threadIdx.x == 0) a.seq_lens[b] = pos + 1;
 }
 
@@ -80,8 +104,8 @@ cudaError_t launch_compose(const ComposeLaunch& a, cudaStream_t st) {
 
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t st) {
   if (a.kv.dtype == PRHS_BF16)
-    return launch_pdl(append_kernel<__nv_bfloat16>, dim3(a.kv.B), dim3(GROW_THREADS), 0, st, a);
-  return launch_pdl(append_kernel<float>, dim3(a.kv.B), dim3(GROW_THREADS), 0, st, a);
+    return launch_pdl(append_kernel<__nv_bfloat16>, dim3(a.kv.B), dim3(APPEND_THREADS), 0, st, a);
+  return launch_pdl(append_kernel<float>, dim3(a.kv.B), dim3(APPEND_THREADS), 0, st, a);
 }
 
 }  // namespace prhs

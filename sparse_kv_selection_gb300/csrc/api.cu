@@ -420,6 +420,10 @@ prhs_status forced_finish(const prhs_kv& kv, DeviceInfo* di, const Layout& L, vo
   m.cap = cap;
   m.delta = delta;
   m.head_skip = head_skip;
+  // the retrieving heads' tickets and the first partial region: the reusing
+  // heads' attention, which may run beside this, uses the second region
+  m.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partials);
+  m.counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.counters);
   return launch_result(launch_mass(m, st), "set mass kernel");
 }
 
@@ -520,6 +524,8 @@ prhs_status prhs_set_mass(const prhs_kv* kv, const void* q, float scale, const i
   m.n_sel = n_sel;
   m.cap = cap;
   m.delta = delta;
+  m.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partials);
+  m.counters = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.counters);
   return launch_result(launch_mass(m, stream), "set mass kernel");
 }
 

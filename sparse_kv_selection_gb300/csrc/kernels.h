@@ -108,7 +108,15 @@ struct MassLaunch {
   int cap;
   float* delta;
   const uint8_t* head_skip = nullptr;  // heads with a nonzero flag are left untouched
+  float* partials = nullptr;   // [units][parts][4] when a head is split (workspace)
+  unsigned* counters = nullptr;  // [units], zero at rest
+  int chunk = 0;               // keys per part (set by launch_mass)
 };
+// A head's keys are split into parts of MASS_CHUNK keys, at most
+// MASS_PARTS_MAX (4 floats per part must fit a unit's attention partial record).
+constexpr int MASS_CHUNK = 8192;
+constexpr int MASS_PARTS_MAX = 16;
+int mass_parts(int t_max);
 cudaError_t launch_mass(const MassLaunch& a, cudaStream_t s);
 
 // Attended set of a retrieving head with forced keys: the first n_sink keys,

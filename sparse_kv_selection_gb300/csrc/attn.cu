@@ -475,9 +475,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
   }
 }
 
-// Both kernels split by query head: the dense one reads each K/V row once per
-// query head of the group, and the group's CTAs, running side by side, find
-// the rows their neighbours just brought into L2.
+// Units are query heads, sparse or dense (the dense path here serves one
+// query head per KV head; grouped heads go to the TMA dense kernel).
 int attn_units(const KVView& kv, bool sparse) { (void)sparse; return kv.B * kv.Hq; }
 
 size_t attn_partial_floats(const KVView& kv, bool sparse, int ctas) {

@@ -4,14 +4,18 @@
 // abstract (top-k oracle selection; the dropped mass delta) and Table I
 // (S_t, N, tau(.), delta(.)).
 //
-// The CL CTAs of a cluster each hold a contiguous slice of the head's logits
-// in shared memory (one read of the logits from L2/HBM). Softmax statistics
-// and three radix histograms (11, 11, 10 bits of an order-preserving key) are
-// built per CTA and summed across the cluster through distributed shared
-// memory; every CTA then takes the same digit decision. The index-ordered
-// compaction gets each CTA's output offset from the counts of the lower
-// ranks, so the set comes out ascending with ties resolved to the lowest
-// index, and the dropped mass is the cluster sum of the unselected weights.
+// The CL CTAs of a cluster (often one) each hold a contiguous slice of the
+// head's logits in shared memory (one read of the logits from L2/HBM). The
+// threshold is found on value bins: the logit range, a 2048-bin histogram over
+// it summed into CTA 0 through distributed shared memory, a second 2048 bins
+// inside the threshold bin when it holds more than SEL_CANDS logits, then the
+// candidates of the final bin ranked exactly; heavy ties fall back to three
+// radix passes (11, 11, 10 bits of an order-preserving key). Every CTA takes
+// the same decision. The index-ordered compaction gets each CTA's output
+// offset from the counts of the lower ranks, so the set comes out ascending
+// with ties resolved to the lowest index, and the dropped mass is the cluster
+// sum of the unselected weights. Forced keys (sinks, window) are ranked below
+// every other key and left to the caller.
 #include <cooperative_groups.h>
 
 #include "kernels.h"

@@ -65,6 +65,7 @@ def _kv(binding, **over):
     (dict(block_table=512, block_size=8, max_blocks=4, num_blocks=4), 1),
     (dict(block_table=512, block_size=16, max_blocks=0, num_blocks=4), 1),
     (dict(dtype=7), 1),
+    (dict(B=513, Hq=32, Hkv=32), 2),     # 16416 query heads: above the 16384 the kernels take
 ])
 def test_descriptor_rejected_on_host(lib, over, status):
     from sparse_kv_selection_gb300 import binding

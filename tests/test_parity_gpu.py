@@ -588,3 +588,41 @@ def test_decode_step_in_cuda_graph_matches_eager(name):
     eager, graphed = run(False), run(True)
     for a, b in zip(eager, graphed):
         assert torch.equal(a.nan_to_num(), b.nan_to_num())
+
+
+def test_decode_step_max_heads_and_empty_cache():
+    """The largest batch the library takes (B * Hq = 16384 query heads) through
+    one decode step, with some sequences' caches empty: sampled heads against
+    the oracle, empty caches give an empty set, out = 0, lse = -inf, delta = 0."""
+    import sparse_kv_selection_gb300 as S
+    from workloads.torch_io import upload
+    B, Hq = 512, 32
+    wl = make_workload("maxheads", dtype="bf16", B=B, Hq=Hq, Hkv=Hq, d=64, t=(20, 48), t_max=48,
+                       n_clusters=2, width=(2, 4), steps=1, N=6, w=1, seed=13)
+    dev = upload(wl)
+    lens = wl.seq_lens.copy()
+    lens[::97] = 0                                    # a few empty caches
+    kv = S.KVCache(dev["k"], dev["v"], torch.from_numpy(lens).cuda(), Hq)
+    dec = S.SparseDecoder(kv, N=6, w=1, tau=wl.tau, scale=wl.scale)
+    o, l, dl, r, n = dec.alloc_outputs(1)
+    dec.step(dev["q"][0], o[0], l[0], dl[0], r[0], n[0])
+    gi = dec.idx.cpu().numpy()
+    o, l, dl, n = o[0].cpu().numpy(), l[0].cpu().numpy(), dl[0].cpu().numpy(), n[0].cpu().numpy()
+    assert S.last_error() == 0
+    rng = np.random.default_rng(3)
+    heads = [(int(b), int(h)) for b, h in zip(rng.integers(0, B, 48), rng.integers(0, Hq, 48))]
+    heads += [(0, 0), (97, 5), (B - 1, Hq - 1)]
+    for b, h in heads:
+        t = int(lens[b])
+        if t == 0:
+            assert n[b, h] == 0 and dl[b, h] == 0.0 and (o[b, h] == 0).all() and l[b, h] == -math.inf
+            continue
+        K, V = kv_rows64(wl, b, h)
+        K, V = K[:t], V[:t]
+        qv = q64(wl, 0, b, h)
+        sc = P.scores(qv, K, wl.scale)
+        gset = gi[b, h, :n[b, h]]
+        check_topn(gset, sc, 6)
+        assert abs(dl[b, h] - P.dropped_mass(sc, gset)) <= DELTA_TOL, (b, h)
+        ro, rl = P.attention(qv, K, V, gset, wl.scale)
+        assert np.abs(o[b, h] - ro).max() <= OUT_TOL and abs(l[b, h] - rl) <= LSE_TOL, (b, h)

@@ -323,7 +323,6 @@ def run_ours(args):
             S.decode_step(kvs[s % R], q[s], scale, N, wl.w, wl.tau, anchor_idx, anchor_n, q_anchor,
                           idx[s], n_sel[s], reuse[s], delta[s], out[s], lse[s], ws, n_budget=nb)
 
-    launches_per_step = 5 * Sq   # cis, score, select and the two sparse-attention branches
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -331,8 +330,10 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert S.last_error() == 0
     graph = torch.cuda.CUDAGraph()
+    c0 = S.binding.launch_count()
     with torch.cuda.graph(graph, stream=stream):
         enqueue()
+    launches_per_step = S.binding.launch_count() - c0   # kernels recorded into one step
 
     def barrier():
         if world > 1:
@@ -362,10 +363,15 @@ def run_ours(args):
     # ---------------- per-kernel durations over the same steps ----------------
     # Each kernel's launches of one timed step, replayed back to back from a
     # graph of their own, on the per-step inputs the timed run produced
-    # (reuse flags, index sets). Selection is timed as (score + select) minus
-    # score, since it consumes the logits of the score launch before it; the
-    # gate/dilation kernel runs on the anchors left by the last query.
-    names = ["cis", "score", "select", "sparse_attn"]
+    # (reuse flags, index sets). A short cache is scored and selected by one
+    # kernel (score_select); otherwise selection is timed as (score + select)
+    # minus score, since it consumes the logits of the score launch before it.
+    # The gate/dilation kernel runs on the anchors left by the last query.
+    c0 = S.binding.launch_count()
+    S.score_select(kvs[0], q[0], scale, N, torch.zeros(B, Hq, acap, **i32), torch.zeros(B, Hq, **i32),
+                   torch.zeros(B, Hq, device="cuda"), ws, n_budget=nb, head_skip=reuse[0])
+    fused = S.binding.launch_count() - c0 == 1
+    names = ["cis", "score_select", "sparse_attn"] if fused else ["cis", "score", "select", "sparse_attn"]
     cis_idx = torch.zeros(B, Hq, cap, **i32)
     cis_n = torch.zeros(B, Hq, **i32)
     cis_r = torch.zeros(B, Hq, device="cuda", dtype=torch.uint8)
@@ -409,13 +415,21 @@ def run_ours(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
+    def k_score_select():
+        for s in range(Sq):
+            S.score_select(kvs[s % R], q[s], scale, N, sel_i, sel_n, sel_d, ws, n_budget=nb,
+                           head_skip=reuse[s])
+
     t_cis = time_graph(k_cis)
-    t_score = time_graph(lambda: k_score(False))
-    t_ss = time_graph(lambda: k_score(True))
     t_attn = time_graph(k_attn)
+    if fused:
+        ktime = {"cis": t_cis, "score_select": time_graph(k_score_select), "sparse_attn": t_attn}
+    else:
+        t_score = time_graph(lambda: k_score(False))
+        t_ss = time_graph(lambda: k_score(True))
+        ktime = {"cis": t_cis, "score": t_score, "select": max(0.0, t_ss - t_score),
+                 "sparse_attn": t_attn}
     assert S.last_error() == 0
-    ktime = {"cis": t_cis, "score": t_score, "select": max(0.0, t_ss - t_score),
-             "sparse_attn": t_attn}
     launches = {n: Sq * args.steps for n in names}
 
     # algorithmic bytes per launch, from the flags and set sizes the run produced
@@ -432,7 +446,7 @@ def run_ours(args):
     score_bytes /= Sq
     rows = sum(gathered_rows(idx[s].cpu().numpy() if G > 1 else None, n_h[s], G) for s in range(Sq))
     attn_bytes = float(rows * 2 * d * es + 4 * n_h.sum() + Sq * B * Hq * (d * es + 4 * d + 4)) / Sq
-    kb = {"score": score_bytes, "sparse_attn": attn_bytes}
+    kb = {"score_select" if fused else "score": score_bytes, "sparse_attn": attn_bytes}
     peak, peak_kind = measured_peak_gbs()
     traffic = profiled_traffic()
     kern = {}
@@ -445,7 +459,7 @@ def run_ours(args):
             e.update({"alg_bytes_per_launch": kb[n], "achieved_gbs": gbs,
                       "frac_of_measured": gbs / peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS})
         kern[n] = e
-    dom = max(["score", "sparse_attn"], key=lambda n: ktime[n])
+    dom = max([n for n in kb], key=lambda n: ktime[n])
     roof = None
     if kern[dom]["avg_us"]:
         ach = kern[dom]["achieved_gbs"]
@@ -594,8 +608,10 @@ def run_grow(args):
     torch.cuda.synchronize()
     assert S.last_error() == 0
     graph = torch.cuda.CUDAGraph()
+    c0 = S.binding.launch_count()
     with torch.cuda.graph(graph, stream=stream):
         enqueue()
+    launches_per_step = S.binding.launch_count() - c0   # kernels recorded into one step
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
@@ -631,7 +647,7 @@ def run_grow(args):
                                 "n_sink": args.n_sink, "window": args.window},
                        "l2": f"{R} rotating KV copies, every copy appended per query",
                        "fresh_retrieval_fraction": float(1.0 - reuse.float().mean().item())},
-            "gpu_launches": Sq * args.steps * (R + 7),
+            "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -693,6 +709,9 @@ def run_kernels(args):
         "score": (lambda kv: S.binding.score(kv, q, wl.scale, ws), kv_rows * d * es),
         "select": (lambda kv: S.binding.select(kv, q, N, idx, n_sel, delta, ws, n_budget=nb),
                    float(B * Hq * tl.mean() * 4)),
+        # one launch on short caches, score + select otherwise; bytes: the K rows
+        "score_select": (lambda kv: S.score_select(kv, q, wl.scale, N, idx, n_sel, delta, ws,
+                                                   n_budget=nb), kv_rows * d * es),
         "sparse_attn_topN": (lambda kv: S.sparse_attn(kv, q, wl.scale, idx, n_sel, out, lse, ws),
                              float(gathered_rows(idx.cpu().numpy(), n_h, wl.G) * 2 * d * es)),
         "sparse_attn_dilated": (lambda kv: S.sparse_attn(kv, q, wl.scale, didx, dn, out, lse, ws),

@@ -246,6 +246,11 @@ const char* prhs_last_message(void);
  * tests): SM count and split-K factors of the attention kernels. */
 int prhs_num_sms(void);
 
+/* Kernels this library has issued (launched, or recorded into a CUDA graph
+ * being captured) since it was loaded, over all threads. Read it before and
+ * after a call to count that call's launches. */
+unsigned long long prhs_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,8 @@ EXPORTS = ["prhs_workspace_size", "prhs_workspace_init", "prhs_score_select", "p
            "prhs_select", "prhs_cis_dilate",
            "prhs_sparse_attn", "prhs_sparse_attn_noalloc", "prhs_set_mass", "prhs_dense_attn",
            "prhs_decode_step", "prhs_append_kv", "prhs_last_error",
-           "prhs_device_error_bits", "prhs_status_str", "prhs_last_message", "prhs_num_sms"]
+           "prhs_device_error_bits", "prhs_status_str", "prhs_last_message", "prhs_num_sms",
+           "prhs_launch_count"]
 
 
 class PrhsError(RuntimeError):
@@ -71,6 +72,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "prhs_append_kv": (I, [KV, P, P, P]),
         "prhs_last_error": (I, []),
         "prhs_device_error_bits": (ctypes.c_uint, []),
+        "prhs_launch_count": (ctypes.c_ulonglong, []),
         "prhs_status_str": (ctypes.c_char_p, [I]),
         "prhs_last_message": (ctypes.c_char_p, []),
         "prhs_num_sms": (I, []),
@@ -267,6 +269,11 @@ def last_error() -> int:
 
 def num_sms() -> int:
     return int(load().prhs_num_sms())
+
+
+def launch_count() -> int:
+    """Kernels the library has issued since it was loaded (prhs_launch_count)."""
+    return int(load().prhs_launch_count())
 
 
 def status_str(s: int) -> str:

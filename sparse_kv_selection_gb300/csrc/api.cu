@@ -1,6 +1,7 @@
 // C ABI of the PrHS decode path: argument checks, workspace layout, TMA
 // descriptor encoding and kernel launches. Declarations and the contract of
 // every entry point are in include/prhs.h.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -243,8 +244,13 @@ prhs_status make_tmap(const prhs_kv& kv, int box_rows, CUtensorMap* map, const v
   return PRHS_OK;
 }
 
+std::atomic<unsigned long long> g_launches{0};  // kernels issued since load
+
 prhs_status launch_result(cudaError_t e, const char* what) {
-  if (e == cudaSuccess) return PRHS_OK;
+  if (e == cudaSuccess) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PRHS_OK;
+  }
   if (e == cudaErrorNotSupported) return fail(PRHS_EUNSUPPORTED, "%s: shape not built", what);
   return cuda_fail(e, what);
 }
@@ -288,6 +294,8 @@ prhs_status do_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* 
   se.q_anchor = q_anchor;
   se.n_sink = n_sink;
   se.window = window;
+  se.scale = 0.f;
+  se.logits_out = nullptr;
   return launch_result(launch_select(se, st), "select kernel");
 }
 
@@ -296,6 +304,31 @@ prhs_status do_score_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, 
                             int n_sink, int window, const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
                             float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
                             void* q_anchor, cudaStream_t st) {
+  const KVView v = view_of(kv, di->err);
+  if (score_select_fits(v)) {  // short caches: logits computed into shared memory, one launch
+    SelectLaunch se;
+    se.kv = v;
+    se.scores = nullptr;
+    se.N = N;
+    se.n_budget = n_budget;
+    se.head_skip = head_skip;
+    se.idx = idx;
+    se.n_sel = n_sel;
+    se.cap = cap;
+    se.delta = delta;
+    se.anchor_idx = anchor_idx;
+    se.anchor_n = anchor_n;
+    se.anchor_cap = anchor_cap;
+    se.q = q;
+    se.q_anchor = q_anchor;
+    se.n_sink = n_sink;
+    se.window = window;
+    se.scale = scale;
+    // with forced keys the set-mass pass that follows reads the logits
+    se.logits_out = n_sink > 0 || window > 0 ? reinterpret_cast<float*>(static_cast<char*>(ws) + L.scores)
+                                             : nullptr;
+    return launch_result(launch_score_select(se, st), "score-select kernel");
+  }
   prhs_status s = do_score(kv, di, L, ws, q, scale, head_skip, st);
   if (s != PRHS_OK) return s;
   return do_select(kv, di, L, ws, q, N, n_budget, n_sink, window, head_skip, idx, n_sel, cap, delta,
@@ -440,6 +473,7 @@ prhs_status abi_device(unsigned** err, int* sms) {
   return PRHS_OK;
 }
 prhs_status abi_fail(prhs_status s, const char* msg) { return fail(s, "%s", msg); }
+void abi_count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 KVView abi_view(const prhs_kv& kv, unsigned* err) { return view_of(kv, err); }
 int abi_attn_ctas(const prhs_kv& kv, bool sparse, int cap, int sms) {
   return attn_ctas(kv, sparse, cap, sms);
@@ -706,6 +740,8 @@ prhs_status prhs_last_error(void) {
 }
 
 unsigned prhs_device_error_bits(void) { return g_last_bits; }
+
+unsigned long long prhs_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* prhs_status_str(prhs_status s) {
   switch (s) {

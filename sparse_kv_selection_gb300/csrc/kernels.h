@@ -23,6 +23,13 @@ constexpr int SELECT_THREADS = 1024;
 // them from L2.
 constexpr int SELECT_SLICE_ONE = 44032;
 constexpr int SELECT_SLICE_MAX = 16384;
+// Score-and-select kernel: a cluster of up to SELECT_FUSED_CL CTAs per query
+// head, each computing the logits of about SELECT_FUSED_ROWS keys (at most
+// SELECT_FUSED_MAX_ROWS) straight from K; longer caches go through the
+// separate scoring and selection kernels.
+constexpr int SELECT_FUSED_ROWS = 256;
+constexpr int SELECT_FUSED_MAX_ROWS = 512;
+constexpr int SELECT_FUSED_CL = 16;
 
 struct ScoreLaunch {
   KVView kv;
@@ -51,6 +58,10 @@ struct SelectLaunch {
   void* q_anchor;
   int n_sink;  // forced keys are left out of the ranking (the caller adds them)
   int window;
+  // score-and-select kernel only: the logits' scale, and where to leave the
+  // logits (null: kept in shared memory only)
+  float scale;
+  float* logits_out;
 };
 
 struct CisLaunch {
@@ -153,6 +164,10 @@ size_t attn_partial_floats(const KVView& kv, bool sparse, int ctas);
 cudaError_t launch_score(const ScoreLaunch& a, const CUtensorMap* tmap, cudaStream_t s);
 cudaError_t launch_select(const SelectLaunch& a, cudaStream_t s);
 cudaError_t launch_select_global(const SelectLaunch& a, cudaStream_t s);
+// Logits and selection in one launch (a.scale, a.logits_out; a.scores unused).
+// Returns cudaErrorNotSupported when the cache is too long for it.
+bool score_select_fits(const KVView& kv);
+cudaError_t launch_score_select(const SelectLaunch& a, cudaStream_t s);
 cudaError_t launch_cis(const CisLaunch& a, cudaStream_t s);
 cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t s);
 // Sparse attention with one thread-block cluster of a.cluster CTAs per query
@@ -166,6 +181,7 @@ cudaError_t launch_attn_cluster(const AttnLaunch& a, cudaStream_t s);
 prhs_status abi_check_kv(const prhs_kv* kv);
 prhs_status abi_device(unsigned** err, int* sms);
 prhs_status abi_fail(prhs_status s, const char* msg);
+void abi_count_launch();  // one more kernel issued (entry points outside the ABI file)
 KVView abi_view(const prhs_kv& kv, unsigned* err);
 int abi_attn_ctas(const prhs_kv& kv, bool sparse, int cap, int sms);
 

@@ -102,5 +102,6 @@ extern "C" prhs_status prhs_sparse_attn_noalloc(const prhs_kv* kv, const void* q
   a.min_rows = ATTN_MIN_ROWS;
   e = launch_attn(a, true, stream);
   if (e != cudaSuccess) return abi_fail(PRHS_ECUDA, cudaGetErrorString(e));
+  abi_count_launch();
   return PRHS_OK;
 }

@@ -46,6 +46,7 @@ struct SelClusterShared {
   unsigned cnt_gt, cnt_eq;    // this CTA's logits above / equal to the threshold
   float dsum;                 // this CTA's dropped weight
   unsigned digit, krem, cnt_bin, thr, keq;
+  float rmin[SELECT_FUSED_CL], rmax[SELECT_FUSED_CL];  // score-and-select: each rank's logit range
 };
 
 __device__ __forceinline__ void merge_mz(float& m, float& z, float m2, float z2) {
@@ -138,79 +139,79 @@ __device__ __forceinline__ SelClusterShared* rank_shared(cg::cluster_group& clus
   return cluster.map_shared_rank(&sh, r);
 }
 
-template <typename T, bool ONE>
-__global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const SelectLaunch a, int chunk) {
-  extern __shared__ float cache[];
-  __shared__ SelClusterShared sh;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int CL = ONE ? 1 : (int)cluster.num_blocks();
-  const int rank = ONE ? 0 : (int)cluster.block_rank();
-  pdl_wait();
-  pdl_trigger();
-
+// Logits s_i = scale * <q, k_i> of keys [lo, lo + cnt) of query head qh,
+// computed from 16-byte pieces of the K rows (LPR lanes per row, all of a
+// thread's loads issued before the first is used), into a.logits_out when set
+// and into cache (forced keys as -inf) when cache is set, with the range of
+// the unforced ones.
+template <typename T, int DK>
+__device__ __forceinline__ void slice_logits(const SelectLaunch& a, int qh, int b, int lo, int cnt,
+                                             int ns, int we, float* cache, float& vmin, float& vmax) {
   const KVView& kv = a.kv;
-  const int qh = blockIdx.x / CL;  // the cluster's query head (b * Hq + h)
-  const int b = qh / kv.Hq;
-  if (a.head_skip != nullptr && a.head_skip[qh] != 0) return;  // uniform over the cluster
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t = seq_len(kv, b);
-  int Nb = a.n_budget != nullptr ? a.n_budget[b] : a.N;
-  if (Nb < 0) Nb = 0;
-  const int lim = a.anchor_idx != nullptr ? min(a.cap, a.anchor_cap) : a.cap;
-  if (min(Nb, t) > lim) {
-    if (tid == 0 && rank == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
-    Nb = lim;
-  }
-  int32_t* out = a.idx + (long long)qh * a.cap;
-  int32_t* aout = a.anchor_idx != nullptr ? a.anchor_idx + (long long)qh * a.anchor_cap : nullptr;
-  const int lo = min(t, rank * chunk), hi = min(t, lo + chunk), cnt = hi - lo;
-  // forced keys [0, ns) and [we, t) are left out of the ranking: the set is
-  // the top Nb of the middle keys [ns, we), written from position 0
-  const int ns = min(max(a.n_sink, 0), t);
-  const int we = max(ns, t - max(a.window, 0));
-  const int tmid = we - ns;
-
-  if (Nb >= tmid || Nb == 0) {  // keep every middle key (delta = 0 without forced keys) or none
-    const int n = Nb >= tmid ? tmid : 0;
-    for (int i = max(lo, ns) + tid; i < min(hi, ns + n); i += SEL_THREADS) {
-      out[i - ns] = i;
-      if (aout) aout[i - ns] = i;
-    }
-    if (rank == 0) {
-      if (tid == 0) {
-        a.n_sel[qh] = n;
-        a.delta[qh] = n == t ? 0.f : 1.f;  // recomputed over the whole set when keys are forced
-        if (a.anchor_n) a.anchor_n[qh] = n;
+  constexpr int EPC = Elem<T>::per16;       // elements per 16-byte piece
+  constexpr int LPR = DK / EPC;             // lanes per K row: 8, 16 or 32
+  constexpr int RPW = SEL_THREADS / LPR;    // rows per CTA-wide wave of loads
+  constexpr int U = 8;                      // waves in flight per thread
+  static_assert(LPR >= 8 && LPR <= 32 && (LPR & (LPR - 1)) == 0, "row split");
+  const int tid = threadIdx.x;
+  const int j = tid & (LPR - 1);
+  const int kvh = (qh % kv.Hq) / (kv.Hq / kv.Hkv);
+  float qf[EPC];
+  Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.q) +
+                                                       (long long)qh * DK * sizeof(T)) + j), qf);
+  const char* kb = static_cast<const char*>(kv.k);
+  float* lout = a.logits_out != nullptr ? a.logits_out + (long long)qh * kv.t_max + lo : nullptr;
+  for (int r0 = 0; r0 < cnt; r0 += RPW * U) {
+    uint4 raw[U];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int r = r0 + u * RPW + tid / LPR;
+      long long row = -1;
+      if (r < cnt) {
+        row = kv_row(kv, b, kvh, lo + r);
+        if (row < 0 && j == 0) raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
       }
-      if (a.q_anchor) mirror_query<T>(a, qh);
-    }
-    return;
-  }
-
-  // ---- load this CTA's slice; its logit range ----
-  const float* src = a.scores + (long long)qh * kv.t_max + lo;
-  float vmin = INFINITY, vmax = -INFINITY;
-  constexpr int PRE = 8;  // loads in flight per thread before the first is used
-  for (int i0 = 0; i0 < cnt; i0 += SEL_THREADS * PRE) {
-    float v[PRE];
-#pragma unroll
-    for (int k = 0; k < PRE; k++) {
-      const int i = i0 + k * SEL_THREADS + tid;
-      v[k] = i < cnt ? src[i] : 0.f;
+      raw[u] = row >= 0 ? ldg_stream(kb + row * (long long)(DK * sizeof(T)) + 16 * j)
+                        : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int k = 0; k < PRE; k++) {
-      const int i = i0 + k * SEL_THREADS + tid;
-      if (i < cnt) {
-        const bool forced = lo + i < ns || lo + i >= we;  // ranked below every middle key
-        cache[i] = forced ? -INFINITY : v[k];
-        if (!forced) {
-          vmin = fminf(vmin, v[k]);
-          vmax = fmaxf(vmax, v[k]);
+    for (int u = 0; u < U; u++) {
+      float f[EPC];
+      Elem<T>::unpack(raw[u], f);
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPC; e++) acc = fmaf(qf[e], f[e], acc);
+#pragma unroll
+      for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
+      const int r = r0 + u * RPW + tid / LPR;
+      if (j == 0 && r < cnt) {
+        const float v = acc * a.scale;
+        if (lout != nullptr) lout[r] = v;
+        if (cache != nullptr) {
+          const bool forced = lo + r < ns || lo + r >= we;  // ranked below every middle key
+          cache[r] = forced ? -INFINITY : v;
+          if (!forced) {
+            vmin = fminf(vmin, v);
+            vmax = fmaxf(vmax, v);
+          }
         }
       }
     }
   }
+}
+
+// Selection over logits already in shared memory: this CTA holds keys
+// [lo, lo + cnt) of query head qh in cache (forced keys as -inf), and vmin,
+// vmax is its thread's share of their range. The CL CTAs of the cluster call
+// it together (CL = 1 when ONE).
+template <typename T, bool ONE>
+__device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClusterShared& sh,
+                                                 const float* cache, cg::cluster_group& cluster,
+                                                 const int CL, const int rank, const int qh, const int Nb,
+                                                 int32_t* out, int32_t* aout, const int lo, const int cnt,
+                                                 float vmin, float vmax) {
+  const KVView& kv = a.kv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < 2048; i += SEL_THREADS) sh.hist[i] = 0;
   if (!ONE && rank == 0)  // a single CTA finds its bins in its own histogram
     for (int i = tid; i < 2 * 2048; i += SEL_THREADS) (&sh.histg[0][0])[i] = 0;
@@ -507,6 +508,177 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   if (!ONE) head_sync<ONE>(cluster);  // shared memory stays valid until every remote read is done
 }
 
+template <typename T, bool ONE>
+__global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const SelectLaunch a, int chunk) {
+  extern __shared__ float cache[];
+  __shared__ SelClusterShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = ONE ? 1 : (int)cluster.num_blocks();
+  const int rank = ONE ? 0 : (int)cluster.block_rank();
+  pdl_wait();
+  pdl_trigger();
+
+  const KVView& kv = a.kv;
+  const int qh = blockIdx.x / CL;  // the cluster's query head (b * Hq + h)
+  const int b = qh / kv.Hq;
+  if (a.head_skip != nullptr && a.head_skip[qh] != 0) return;  // uniform over the cluster
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = seq_len(kv, b);
+  int Nb = a.n_budget != nullptr ? a.n_budget[b] : a.N;
+  if (Nb < 0) Nb = 0;
+  const int lim = a.anchor_idx != nullptr ? min(a.cap, a.anchor_cap) : a.cap;
+  if (min(Nb, t) > lim) {
+    if (tid == 0 && rank == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
+    Nb = lim;
+  }
+  int32_t* out = a.idx + (long long)qh * a.cap;
+  int32_t* aout = a.anchor_idx != nullptr ? a.anchor_idx + (long long)qh * a.anchor_cap : nullptr;
+  const int lo = min(t, rank * chunk), hi = min(t, lo + chunk), cnt = hi - lo;
+  // forced keys [0, ns) and [we, t) are left out of the ranking: the set is
+  // the top Nb of the middle keys [ns, we), written from position 0
+  const int ns = min(max(a.n_sink, 0), t);
+  const int we = max(ns, t - max(a.window, 0));
+  const int tmid = we - ns;
+
+  if (Nb >= tmid || Nb == 0) {  // keep every middle key (delta = 0 without forced keys) or none
+    const int n = Nb >= tmid ? tmid : 0;
+    for (int i = max(lo, ns) + tid; i < min(hi, ns + n); i += SEL_THREADS) {
+      out[i - ns] = i;
+      if (aout) aout[i - ns] = i;
+    }
+    if (rank == 0) {
+      if (tid == 0) {
+        a.n_sel[qh] = n;
+        a.delta[qh] = n == t ? 0.f : 1.f;  // recomputed over the whole set when keys are forced
+        if (a.anchor_n) a.anchor_n[qh] = n;
+      }
+      if (a.q_anchor) mirror_query<T>(a, qh);
+    }
+    return;
+  }
+
+  // ---- load this CTA's slice; its logit range ----
+  const float* src = a.scores + (long long)qh * kv.t_max + lo;
+  float vmin = INFINITY, vmax = -INFINITY;
+  constexpr int PRE = 8;  // loads in flight per thread before the first is used
+  for (int i0 = 0; i0 < cnt; i0 += SEL_THREADS * PRE) {
+    float v[PRE];
+#pragma unroll
+    for (int k = 0; k < PRE; k++) {
+      const int i = i0 + k * SEL_THREADS + tid;
+      v[k] = i < cnt ? src[i] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < PRE; k++) {
+      const int i = i0 + k * SEL_THREADS + tid;
+      if (i < cnt) {
+        const bool forced = lo + i < ns || lo + i >= we;  // ranked below every middle key
+        cache[i] = forced ? -INFINITY : v[k];
+        if (!forced) {
+          vmin = fminf(vmin, v[k]);
+          vmax = fmaxf(vmax, v[k]);
+        }
+      }
+    }
+  }
+  select_in_shared<T, ONE>(a, sh, cache, cluster, CL, rank, qh, Nb, out, aout, lo, cnt, vmin, vmax);
+}
+
+// Logits and top-N selection of one query head in one launch. The cluster's
+// CL CTAs each compute the logits of one slice of keys straight from K and
+// store them into CTA 0's shared memory (distributed shared memory), with the
+// slice's logit range; after one cluster barrier CTA 0 alone selects from the
+// whole row, as the one-CTA selection does, and the other CTAs are done.
+template <typename T, int DK, bool ONE>
+__global__ void __launch_bounds__(SEL_THREADS, 2) score_select_kernel(const SelectLaunch a, int chunk) {
+  extern __shared__ float cache[];  // CTA 0: the head's logits, t_max floats
+  __shared__ SelClusterShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = ONE ? 1 : (int)cluster.num_blocks();
+  const int rank = ONE ? 0 : (int)cluster.block_rank();
+  pdl_wait();
+  pdl_trigger();
+
+  const KVView& kv = a.kv;
+  const int qh = blockIdx.x / CL;
+  const int b = qh / kv.Hq;
+  if (a.head_skip != nullptr && a.head_skip[qh] != 0) return;  // uniform over the cluster
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = seq_len(kv, b);
+  int Nb = a.n_budget != nullptr ? a.n_budget[b] : a.N;
+  if (Nb < 0) Nb = 0;
+  const int lim = a.anchor_idx != nullptr ? min(a.cap, a.anchor_cap) : a.cap;
+  if (min(Nb, t) > lim) {
+    if (tid == 0 && rank == 0) raise_error(kv.err, PRHS_DEV_CAPACITY);
+    Nb = lim;
+  }
+  int32_t* out = a.idx + (long long)qh * a.cap;
+  int32_t* aout = a.anchor_idx != nullptr ? a.anchor_idx + (long long)qh * a.anchor_cap : nullptr;
+  const int lo = min(t, rank * chunk), hi = min(t, lo + chunk), cnt = hi - lo;
+  const int ns = min(max(a.n_sink, 0), t);   // forced keys [0, ns) and [we, t)
+  const int we = max(ns, t - max(a.window, 0));
+  const int tmid = we - ns;
+
+  if (Nb >= tmid || Nb == 0) {  // every middle key or none: no ranking (uniform over the cluster)
+    const int n = Nb >= tmid ? tmid : 0;
+    for (int i = max(lo, ns) + tid; i < min(hi, ns + n); i += SEL_THREADS) {
+      out[i - ns] = i;
+      if (aout) aout[i - ns] = i;
+    }
+    if (a.logits_out != nullptr) {  // the caller's set-mass pass reads every logit
+      float u0 = 0.f, u1 = 0.f;
+      slice_logits<T, DK>(a, qh, b, lo, cnt, ns, we, nullptr, u0, u1);
+    }
+    if (rank == 0) {
+      if (tid == 0) {
+        a.n_sel[qh] = n;
+        a.delta[qh] = n == t ? 0.f : 1.f;  // recomputed over the whole set when keys are forced
+        if (a.anchor_n) a.anchor_n[qh] = n;
+      }
+      if (a.q_anchor) mirror_query<T>(a, qh);
+    }
+    return;
+  }
+
+  // ---- this CTA's slice of logits, into CTA 0's row; the slice's range ----
+  float* row = ONE ? cache : cluster.map_shared_rank(cache, 0);
+  float vmin = INFINITY, vmax = -INFINITY;
+  slice_logits<T, DK>(a, qh, b, lo, cnt, ns, we, row + lo, vmin, vmax);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    vmin = fminf(vmin, __shfl_xor_sync(FULL_MASK, vmin, o));
+    vmax = fmaxf(vmax, __shfl_xor_sync(FULL_MASK, vmax, o));
+  }
+  if (lane == 0) {
+    sh.red[warp] = vmin;
+    sh.red2[warp] = vmax;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float m0 = INFINITY, m1 = -INFINITY;
+    for (int w = 0; w < SEL_WARPS; w++) {
+      m0 = fminf(m0, sh.red[w]);
+      m1 = fmaxf(m1, sh.red2[w]);
+    }
+    SelClusterShared* root = ONE ? &sh : cluster.map_shared_rank(&sh, 0);
+    root->rmin[rank] = m0;
+    root->rmax[rank] = m1;
+  }
+  if (ONE) {
+    __syncthreads();
+  } else {
+    cluster.sync();  // every slice and range is in CTA 0
+    if (rank != 0) return;
+  }
+  float smin = INFINITY, smax = -INFINITY;
+  for (int r = 0; r < CL; r++) {
+    smin = fminf(smin, sh.rmin[r]);
+    smax = fmaxf(smax, sh.rmax[r]);
+  }
+  __syncthreads();  // sh.red is reused by the selection
+  select_in_shared<T, true>(a, sh, cache, cluster, 1, 0, qh, Nb, out, aout, 0, t, smin, smax);
+}
+
 // Cluster size and slice length: one CTA holds up to SELECT_SLICE_ONE logits;
 // longer caches spread a head over 2..8 CTAs. (Splitting shorter caches to
 // fill the GPU costs more in cluster barriers than it saves.)
@@ -520,6 +692,34 @@ static void select_geometry(const KVView& kv, int sms, int* cl, int* chunk) {
   (void)sms;
   *cl = c;
   *chunk = ((tmax + c - 1) / c + 3) / 4 * 4;
+}
+
+// One cluster of cl CTAs per query head, `floats` logits of shared memory each.
+static cudaError_t launch_clustered(void (*k)(const SelectLaunch, int), const SelectLaunch& a, int cl,
+                                    int chunk, int floats, cudaStream_t st) {
+  const size_t smem = (size_t)floats * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (cl > 8) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int U = a.kv.B * a.kv.Hq;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(U * cl);
+  cfg.blockDim = dim3(SEL_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = cl == 1 ? attr + 1 : attr;  // no cluster attribute for a single CTA
+  cfg.numAttrs = cl == 1 ? 1 : 2;
+  return cudaLaunchKernelEx(&cfg, k, a, chunk);
 }
 
 cudaError_t launch_select(const SelectLaunch& a, cudaStream_t st) {
@@ -536,24 +736,43 @@ cudaError_t launch_select(const SelectLaunch& a, cudaStream_t st) {
     k = cl == 1 ? select_cluster_kernel<__nv_bfloat16, true> : select_cluster_kernel<__nv_bfloat16, false>;
   else
     k = cl == 1 ? select_cluster_kernel<float, true> : select_cluster_kernel<float, false>;
-  const size_t smem = (size_t)chunk * sizeof(float);
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.kv.B * a.kv.Hq * cl);
-  cfg.blockDim = dim3(SEL_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = cl == 1 ? attr + 1 : attr;  // no cluster attribute for a single CTA
-  cfg.numAttrs = cl == 1 ? 1 : 2;
-  return cudaLaunchKernelEx(&cfg, k, a, chunk);
+  return launch_clustered(k, a, cl, chunk, chunk, st);
+}
+
+// Score-and-select geometry: the fewest CTAs (a power of two up to
+// SELECT_FUSED_CL) whose slices hold at most SELECT_FUSED_ROWS keys each, or
+// SELECT_FUSED_CL CTAs of up to SELECT_FUSED_MAX_ROWS.
+static bool fused_geometry(const KVView& kv, int* cl, int* chunk) {
+  int c = 1;
+  while (c < SELECT_FUSED_CL && (kv.t_max + c - 1) / c > SELECT_FUSED_ROWS) c *= 2;
+  if ((kv.t_max + c - 1) / c > SELECT_FUSED_MAX_ROWS) return false;
+  *cl = c;
+  *chunk = ((kv.t_max + c - 1) / c + 3) / 4 * 4;
+  return true;
+}
+
+bool score_select_fits(const KVView& kv) {
+  int cl, chunk;
+  return (kv.d == 64 || kv.d == 128) && fused_geometry(kv, &cl, &chunk);
+}
+
+template <typename T>
+static cudaError_t score_select_dispatch(const SelectLaunch& a, int cl, int chunk, cudaStream_t st) {
+  void (*k)(const SelectLaunch, int);
+  if (a.kv.d == 128)
+    k = cl == 1 ? score_select_kernel<T, 128, true> : score_select_kernel<T, 128, false>;
+  else if (a.kv.d == 64)
+    k = cl == 1 ? score_select_kernel<T, 64, true> : score_select_kernel<T, 64, false>;
+  else
+    return cudaErrorNotSupported;
+  return launch_clustered(k, a, cl, chunk, a.kv.t_max, st);  // CTA 0 holds the whole row
+}
+
+cudaError_t launch_score_select(const SelectLaunch& a, cudaStream_t st) {
+  int cl = 1, chunk = 0;
+  if (!fused_geometry(a.kv, &cl, &chunk)) return cudaErrorNotSupported;
+  return a.kv.dtype == PRHS_BF16 ? score_select_dispatch<__nv_bfloat16>(a, cl, chunk, st)
+                                 : score_select_dispatch<float>(a, cl, chunk, st);
 }
 
 }  // namespace prhs

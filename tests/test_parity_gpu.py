@@ -27,6 +27,9 @@ CASES = {
                           N=50, w=1),
     "f32_d128_paged32": dict(dtype="f32", B=2, Hq=2, Hkv=2, d=128, t=(100, 400), paged=True,
                              block_size=32, n_clusters=4, steps=4, N=40, w=3),
+    # caches of 4097..8192 keys: sixteen CTAs per head in the score-and-select kernel
+    "bf16_long_gqa2": dict(dtype="bf16", B=2, Hq=4, Hkv=2, d=128, t=(5000, 8192), t_max=8192,
+                           n_clusters=48, steps=4, N=300, w=2),
 }
 
 
@@ -539,23 +542,34 @@ def test_set_mass_matches_oracle(name):
         assert abs(dl[b, h] - want) <= DELTA_TOL, (b, h, dl[b, h], want)
 
 
-def test_score_then_select_equals_score_select():
-    S, wl, dev, kv = _setup("gqa4_bf16")
-    N = int(wl.budget[0])
-    outs = []
+@pytest.mark.parametrize("name", ["gqa4_bf16", "mha_bf16_ragged", "paged_bf16", "f32_d64_gqa2",
+                                  "bf16_long_gqa2"])
+def test_score_then_select_and_score_select(name):
+    """prhs_score followed by prhs_select, and prhs_score_select (one launch
+    computing the logits in shared memory when the cache is short), each
+    against the oracle: the top-N set up to near-ties and the dropped mass."""
+    S, wl, dev, kv = _setup(name)
+    nb = dev["budget"] if len(set(wl.budget.tolist())) > 1 else None
+    N = 0 if nb is not None else int(wl.budget[0])   # N is not read with per-sequence budgets
+    cap = int(wl.budget.max())
     for split in (False, True):
-        idx = torch.full((wl.B, wl.Hq, N), -1, dtype=torch.int32, device="cuda")
+        idx = torch.full((wl.B, wl.Hq, cap), -1, dtype=torch.int32, device="cuda")
         n_sel = torch.zeros(wl.B, wl.Hq, dtype=torch.int32, device="cuda")
         delta = torch.zeros(wl.B, wl.Hq, device="cuda")
-        ws = S.make_workspace(kv, N)
+        ws = S.make_workspace(kv, cap)
         if split:
             S.binding.score(kv, dev["q"][3], wl.scale, ws)
-            S.binding.select(kv, dev["q"][3], N, idx, n_sel, delta, ws)
+            S.binding.select(kv, dev["q"][3], N, idx, n_sel, delta, ws, n_budget=nb)
         else:
-            S.score_select(kv, dev["q"][3], wl.scale, N, idx, n_sel, delta, ws)
-        outs.append((idx.cpu(), n_sel.cpu(), delta.cpu()))
-    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
-    assert torch.equal(outs[0][2], outs[1][2])
+            S.score_select(kv, dev["q"][3], wl.scale, N, idx, n_sel, delta, ws, n_budget=nb)
+        assert S.last_error() == 0
+        gi, gn, gd = idx.cpu().numpy(), n_sel.cpu().numpy(), delta.cpu().numpy()
+        for b, h in _heads(wl):
+            K, _ = kv_rows64(wl, b, h // wl.G)
+            sc = P.scores(q64(wl, 3, b, h), K, wl.scale)
+            gset = gi[b, h, :gn[b, h]]
+            check_topn(gset, sc, int(wl.budget[b]))
+            assert abs(gd[b, h] - P.dropped_mass(sc, gset)) <= DELTA_TOL, (split, b, h)
 
 
 @pytest.mark.parametrize("name", ["mha_bf16_ragged", "paged_bf16"])
@@ -626,3 +640,34 @@ def test_decode_step_max_heads_and_empty_cache():
         assert abs(dl[b, h] - P.dropped_mass(sc, gset)) <= DELTA_TOL, (b, h)
         ro, rl = P.attention(qv, K, V, gset, wl.scale)
         assert np.abs(o[b, h] - ro).max() <= OUT_TOL and abs(l[b, h] - rl) <= LSE_TOL, (b, h)
+
+
+def test_launch_counts():
+    """Kernels per call, read from the library's launch counter: prhs_score_select
+    is one launch on a short cache and two (score, select) on a long one; a
+    decode step adds the gate, the two attention branches, and the compose and
+    set-mass launches when keys are forced."""
+    import sparse_kv_selection_gb300 as S
+    from workloads.torch_io import upload
+
+    def count(fn):
+        c0 = S.binding.launch_count()
+        fn()
+        torch.cuda.synchronize()
+        return S.binding.launch_count() - c0
+
+    for t, fused in ((1000, True), (8192, True), (9000, False)):
+        wl = make_workload("lc", dtype="bf16", B=1, Hq=2, Hkv=2, d=128, t=t, n_clusters=8, steps=1,
+                           N=64, w=1, seed=5)
+        dev = upload(wl)
+        kv = S.KVCache(dev["k"], dev["v"], dev["seq_lens"], wl.Hq)
+        idx = torch.zeros(1, 2, 64, dtype=torch.int32, device="cuda")
+        n = torch.zeros(1, 2, dtype=torch.int32, device="cuda")
+        dl = torch.zeros(1, 2, device="cuda")
+        ws = S.make_workspace(kv, 64 * 3 + 16)
+        assert count(lambda: S.score_select(kv, dev["q"][0], wl.scale, 64, idx, n, dl, ws)) == (1 if fused else 2)
+        ss = 1 if fused else 2
+        for n_sink, window, extra in ((0, 0, 0), (2, 8, 2)):
+            dec = S.SparseDecoder(kv, N=64, w=1, tau=wl.tau, scale=wl.scale, n_sink=n_sink, window=window)
+            assert count(lambda: dec.step(dev["q"][0])) == 3 + ss + extra, (t, n_sink)
+        assert S.last_error() == 0

@@ -367,19 +367,19 @@ def run_ours(args):
     # kernel (score_select); otherwise selection is timed as (score + select)
     # minus score, since it consumes the logits of the score launch before it.
     # The gate/dilation kernel runs on the anchors left by the last query.
+    o_tmp = torch.zeros(B, Hq, d, device="cuda")
+    l_tmp = torch.zeros(B, Hq, device="cuda")
     c0 = S.binding.launch_count()
-    S.score_select(kvs[0], q[0], scale, N, torch.zeros(B, Hq, acap, **i32), torch.zeros(B, Hq, **i32),
-                   torch.zeros(B, Hq, device="cuda"), ws, n_budget=nb, head_skip=reuse[0])
-    fused = S.binding.launch_count() - c0 == 1
-    names = ["cis", "score_select", "sparse_attn"] if fused else ["cis", "score", "select", "sparse_attn"]
+    S.retrieve(kvs[0], q[0], scale, N, torch.zeros(B, Hq, acap, **i32), torch.zeros(B, Hq, **i32),
+               torch.zeros(B, Hq, device="cuda"), o_tmp, l_tmp, ws, n_budget=nb, head_skip=reuse[0])
+    fused = S.binding.launch_count() - c0 == 1   # scoring, selection and attention in one kernel
+    names = ["cis", "retrieve", "sparse_attn"] if fused else ["cis", "score", "select", "sparse_attn"]
     cis_idx = torch.zeros(B, Hq, cap, **i32)
     cis_n = torch.zeros(B, Hq, **i32)
     cis_r = torch.zeros(B, Hq, device="cuda", dtype=torch.uint8)
     sel_i = torch.zeros(B, Hq, acap, **i32)
     sel_n = torch.zeros(B, Hq, **i32)
     sel_d = torch.zeros(B, Hq, device="cuda")
-    o_tmp = torch.zeros(B, Hq, d, device="cuda")
-    l_tmp = torch.zeros(B, Hq, device="cuda")
 
     def k_cis():
         for s in range(Sq):
@@ -415,15 +415,15 @@ def run_ours(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
-    def k_score_select():
+    def k_retrieve():
         for s in range(Sq):
-            S.score_select(kvs[s % R], q[s], scale, N, sel_i, sel_n, sel_d, ws, n_budget=nb,
-                           head_skip=reuse[s])
+            S.retrieve(kvs[s % R], q[s], scale, N, sel_i, sel_n, sel_d, o_tmp, l_tmp, ws, n_budget=nb,
+                       head_skip=reuse[s])
 
     t_cis = time_graph(k_cis)
     t_attn = time_graph(k_attn)
     if fused:
-        ktime = {"cis": t_cis, "score_select": time_graph(k_score_select), "sparse_attn": t_attn}
+        ktime = {"cis": t_cis, "retrieve": time_graph(k_retrieve), "sparse_attn": t_attn}
     else:
         t_score = time_graph(lambda: k_score(False))
         t_ss = time_graph(lambda: k_score(True))
@@ -446,7 +446,10 @@ def run_ours(args):
     score_bytes /= Sq
     rows = sum(gathered_rows(idx[s].cpu().numpy() if G > 1 else None, n_h[s], G) for s in range(Sq))
     attn_bytes = float(rows * 2 * d * es + 4 * n_h.sum() + Sq * B * Hq * (d * es + 4 * d + 4)) / Sq
-    kb = {"score_select" if fused else "score": score_bytes, "sparse_attn": attn_bytes}
+    # retrieval: the K rows scored plus the V rows of the fresh sets
+    fresh_rows = sum(float(n_h[s][~r_h[s]].sum()) for s in range(Sq)) / Sq
+    kb = {"retrieve": score_bytes + fresh_rows * d * es, "sparse_attn": attn_bytes} if fused else \
+        {"score": score_bytes, "sparse_attn": attn_bytes}
     peak, peak_kind = measured_peak_gbs()
     traffic = profiled_traffic()
     kern = {}
@@ -712,6 +715,11 @@ def run_kernels(args):
         # one launch on short caches, score + select otherwise; bytes: the K rows
         "score_select": (lambda kv: S.score_select(kv, q, wl.scale, N, idx, n_sel, delta, ws,
                                                    n_budget=nb), kv_rows * d * es),
+        # selection and attention over the set (one launch on short caches);
+        # bytes: the K rows and the V rows of the sets
+        "retrieve": (lambda kv: S.retrieve(kv, q, wl.scale, N, idx, n_sel, delta, out, lse, ws,
+                                           n_budget=nb),
+                     kv_rows * d * es + float(n_h.sum() * d * es)),
         "sparse_attn_topN": (lambda kv: S.sparse_attn(kv, q, wl.scale, idx, n_sel, out, lse, ws),
                              float(gathered_rows(idx.cpu().numpy(), n_h, wl.G) * 2 * d * es)),
         "sparse_attn_dilated": (lambda kv: S.sparse_attn(kv, q, wl.scale, didx, dn, out, lse, ws),

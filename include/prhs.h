@@ -116,6 +116,24 @@ prhs_status prhs_score_select(const prhs_kv* kv, const void* q, float scale, int
                               int anchor_cap, void* q_anchor, void* ws, size_t ws_bytes,
                               cudaStream_t stream);
 
+/* Retrieval for the query heads not flagged in head_skip (in a decode step,
+ * the heads that do not reuse an anchor): the set, its size, delta and the
+ * anchor copies exactly as prhs_score_select writes them (same arguments),
+ * and the attention over that set as prhs_sparse_attn computes it,
+ *   out[b][h] = sum_{i in S} A_i v_i / sum_{i in S} A_i  (fp32, [B][Hq][d]),
+ *   lse[b][h] = log sum_{i in S} exp(s_i)                 ([B][Hq]),
+ * out = 0 and lse = -inf for an empty set. Rows of flagged heads are left
+ * untouched. A cache of t_max <= 8192 without forced keys takes one kernel
+ * launch (logits, selection and attention in one thread-block cluster per
+ * head); otherwise it is scoring, selection (with the forced keys' passes)
+ * and sparse attention. out and lse must be non-null. */
+prhs_status prhs_retrieve(const prhs_kv* kv, const void* q, float scale, int N,
+                          const int32_t* n_budget, int n_sink, int window,
+                          const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
+                          float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
+                          void* q_anchor, float* out, float* lse, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
 /* The two halves of prhs_score_select, for callers that time or reuse them
  * separately. prhs_score writes the logits s_i = scale * <q, k_i> of every
  * query head not flagged in head_skip into the workspace; prhs_select then
@@ -206,8 +224,9 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
 
 /* One decode step with CIS reuse, stream-ordered, no host round trip:
  *   prhs_cis_dilate(anchor -> idx, reuse);
- *   prhs_score_select(head_skip = reuse, anchor outputs = the anchor buffers);
- *   prhs_sparse_attn(idx).
+ *   the reusing heads: prhs_sparse_attn(idx) on an internal side stream;
+ *   the others: prhs_retrieve(head_skip = reuse, anchor outputs = the anchor
+ *   buffers) on `stream`, which then waits for the side stream.
  * Heads that reuse attend the dilated anchor set; the others retrieve a fresh
  * top-N set, attend it and make it (with q) the new anchor. delta is written
  * for retrieving heads only. Start a sequence with anchor_n (and anchor_age)

@@ -7,10 +7,10 @@ sequence. Nothing here falls back to host code: without the built library
 every call raises.
 """
 from .binding import (KVCache, PrhsError, cis_dilate, decode_step, dense_attn, last_error,
-                      load, make_workspace, num_sms, score_select, set_mass, sparse_attn,
-                      workspace_init, workspace_size)
+                      load, make_workspace, num_sms, retrieve, score_select, set_mass,
+                      sparse_attn, workspace_init, workspace_size)
 from .decoder import SparseDecoder
 
 __all__ = ["KVCache", "PrhsError", "SparseDecoder", "cis_dilate", "decode_step", "dense_attn",
-           "last_error", "load", "make_workspace", "num_sms", "score_select", "set_mass",
-           "sparse_attn", "workspace_init", "workspace_size"]
+           "last_error", "load", "make_workspace", "num_sms", "retrieve", "score_select",
+           "set_mass", "sparse_attn", "workspace_init", "workspace_size"]

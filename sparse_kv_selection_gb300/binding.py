@@ -20,7 +20,8 @@ PRHS_F32, PRHS_BF16 = 0, 1
 DEV_TIMEOUT, DEV_BAD_INDEX, DEV_BAD_LEN, DEV_BAD_BLOCK, DEV_CAPACITY = 1, 2, 4, 8, 16
 
 # Entry points declared in include/prhs.h, in declaration order.
-EXPORTS = ["prhs_workspace_size", "prhs_workspace_init", "prhs_score_select", "prhs_score",
+EXPORTS = ["prhs_workspace_size", "prhs_workspace_init", "prhs_score_select", "prhs_retrieve",
+           "prhs_score",
            "prhs_select", "prhs_cis_dilate",
            "prhs_sparse_attn", "prhs_sparse_attn_noalloc", "prhs_set_mass", "prhs_dense_attn",
            "prhs_decode_step", "prhs_append_kv", "prhs_last_error",
@@ -60,6 +61,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "prhs_workspace_size": (Z, [KV, I]),
         "prhs_workspace_init": (I, [P, Z, P]),
         "prhs_score_select": (I, [KV, P, F, I, P, I, I, P, P, P, I, P, P, P, I, P, P, Z, P]),
+        "prhs_retrieve": (I, [KV, P, F, I, P, I, I, P, P, P, I, P, P, P, I, P, P, P, P, Z, P]),
         "prhs_score": (I, [KV, P, F, P, P, Z, P]),
         "prhs_select": (I, [KV, P, I, P, I, I, P, P, P, I, P, P, P, I, P, P, Z, P]),
         "prhs_cis_dilate": (I, [KV, P, P, I, P, P, I, I, I, D, I, P, P, P, I, P, P]),
@@ -187,6 +189,21 @@ def score_select(kv, q, scale, N, idx, n_sel, delta, ws, *, n_budget=None, head_
                                     _ptr(head_skip), _ptr(idx), _ptr(n_sel), cap, _ptr(delta),
                                     _ptr(anchor_idx), _ptr(anchor_n), acap, _ptr(q_anchor),
                                     _ptr(ws), ws.numel(), _stream(stream)), "score_select")
+
+
+def retrieve(kv, q, scale, N, idx, n_sel, delta, out, lse, ws, *, n_budget=None, head_skip=None,
+             anchor_idx=None, anchor_n=None, q_anchor=None, n_sink=0, window=0,
+             stream=None) -> None:
+    """Top-N set, delta and the attention over the set for the heads not
+    flagged in head_skip (prhs_retrieve); out [B][Hq][d] and lse [B][Hq] fp32."""
+    cap = idx.shape[-1]
+    acap = anchor_idx.shape[-1] if anchor_idx is not None else 0
+    _check(load().prhs_retrieve(kv.ref(), _ptr(q), float(scale), int(N), _ptr(n_budget),
+                                int(n_sink), int(window),
+                                _ptr(head_skip), _ptr(idx), _ptr(n_sel), cap, _ptr(delta),
+                                _ptr(anchor_idx), _ptr(anchor_n), acap, _ptr(q_anchor),
+                                _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)),
+           "retrieve")
 
 
 def score(kv, q, scale, ws, *, head_skip=None, stream=None) -> None:

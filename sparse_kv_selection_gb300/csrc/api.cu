@@ -296,6 +296,8 @@ prhs_status do_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* 
   se.window = window;
   se.scale = 0.f;
   se.logits_out = nullptr;
+  se.out = nullptr;
+  se.lse = nullptr;
   return launch_result(launch_select(se, st), "select kernel");
 }
 
@@ -303,7 +305,8 @@ prhs_status do_score_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, 
                             const void* q, float scale, int N, const int32_t* n_budget,
                             int n_sink, int window, const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
                             float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
-                            void* q_anchor, cudaStream_t st) {
+                            void* q_anchor, cudaStream_t st, float* out = nullptr,
+                            float* lse = nullptr) {
   const KVView v = view_of(kv, di->err);
   if (score_select_fits(v)) {  // short caches: logits computed into shared memory, one launch
     SelectLaunch se;
@@ -327,6 +330,8 @@ prhs_status do_score_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, 
     // with forced keys the set-mass pass that follows reads the logits
     se.logits_out = n_sink > 0 || window > 0 ? reinterpret_cast<float*>(static_cast<char*>(ws) + L.scores)
                                              : nullptr;
+    se.out = out;  // with out: the attention over the set too (no forced keys)
+    se.lse = lse;
     return launch_result(launch_score_select(se, st), "score-select kernel");
   }
   prhs_status s = do_score(kv, di, L, ws, q, scale, head_skip, st);
@@ -460,6 +465,29 @@ prhs_status forced_finish(const prhs_kv& kv, DeviceInfo* di, const Layout& L, vo
   return launch_result(launch_mass(m, st), "set mass kernel");
 }
 
+// The retrieving heads (not flagged in head_skip): top-N set, delta and the
+// attention over the set into out/lse. Short caches without forced keys take
+// one launch (score, select and attend); otherwise scoring, selection, the
+// forced keys' composition and set mass, and sparse attention over the heads
+// with head_skip == 0. rows_hint bounds the rows of one head's set.
+prhs_status do_retrieve(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws, const void* q,
+                        float scale, int N, const int32_t* n_budget, int n_sink, int window,
+                        const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap, float* delta,
+                        int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap, void* q_anchor,
+                        float* out, float* lse, int rows_hint, cudaStream_t st) {
+  const bool forced = n_sink > 0 || window > 0;
+  const bool one = !forced && score_select_fits(view_of(kv, di->err));
+  prhs_status s = do_score_select(kv, di, L, ws, q, scale, N, n_budget, n_sink, window, head_skip, idx,
+                                  n_sel, cap, delta, anchor_idx, anchor_n, anchor_cap, q_anchor, st,
+                                  one ? out : nullptr, one ? lse : nullptr);
+  if (s != PRHS_OK || one) return s;
+  if (forced && (s = forced_finish(kv, di, L, ws, head_skip, anchor_idx, anchor_n, anchor_cap, idx,
+                                   n_sel, cap, delta, n_sink, window, st)) != PRHS_OK)
+    return s;
+  return do_attn(kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, st, head_skip, 0, false, 0,
+                 ATTN_MIN_ROWS, rows_hint);
+}
+
 }  // namespace
 
 // Internal hooks for other translation units of the library (no C linkage).
@@ -523,6 +551,28 @@ prhs_status prhs_score_select(const prhs_kv* kv, const void* q, float scale, int
   if (!forced) return PRHS_OK;
   return forced_finish(*kv, di, L, ws, head_skip, anchor_idx, anchor_n, anchor_cap, idx, n_sel, cap,
                        delta, n_sink, window, stream);
+}
+
+prhs_status prhs_retrieve(const prhs_kv* kv, const void* q, float scale, int N, const int32_t* n_budget,
+                          int n_sink, int window, const uint8_t* head_skip, int32_t* idx,
+                          int32_t* n_sel, int cap, float* delta, int32_t* anchor_idx,
+                          int32_t* anchor_n, int anchor_cap, void* q_anchor, float* out, float* lse,
+                          void* ws, size_t ws_bytes, cudaStream_t stream) {
+  prhs_status s = check_kv(kv);
+  if (s != PRHS_OK) return s;
+  if ((s = check_select_args(*kv, q, N, n_budget, idx, n_sel, cap, delta, anchor_idx, anchor_n,
+                             anchor_cap, q_anchor)) != PRHS_OK)
+    return s;
+  if (out == nullptr || lse == nullptr) return fail(PRHS_EINVAL, "out and lse must be non-null");
+  if ((s = check_forced(*kv, n_sink, window)) != PRHS_OK) return s;
+  const bool forced = n_sink > 0 || window > 0;
+  if (forced && anchor_idx == nullptr) return fail(PRHS_EINVAL, "forced keys need the anchor buffers");
+  DeviceInfo* di = nullptr;
+  if ((s = device_info(&di)) != PRHS_OK) return s;
+  Layout L;
+  if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
+  return do_retrieve(*kv, di, L, ws, q, scale, N, n_budget, n_sink, window, head_skip, idx, n_sel, cap,
+                     delta, anchor_idx, anchor_n, anchor_cap, q_anchor, out, lse, cap, stream);
 }
 
 prhs_status prhs_score(const prhs_kv* kv, const void* q, float scale, const uint8_t* head_skip,
@@ -693,16 +743,10 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if ((s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, di->side, reuse, 1,
                    true, 0, ATTN_SIDE_MIN_ROWS)) != PRHS_OK)
     return s;
-  if ((s = do_score_select(*kv, di, L, ws, q, scale, N, n_budget, n_sink, window, reuse, idx,
-                           n_sel, cap, delta, anchor_idx, anchor_n, anchor_cap, q_anchor,
-                           stream)) != PRHS_OK)
-    return s;
-  if (forced && (s = forced_finish(*kv, di, L, ws, reuse, anchor_idx, anchor_n, anchor_cap, idx,
-                                   n_sel, cap, delta, n_sink, window, stream)) != PRHS_OK)
-    return s;
   // the retrieving heads' sets hold at most anchor_cap (+ forced) rows
-  if ((s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, stream, reuse, 0,
-                   false, 0, ATTN_MIN_ROWS, anchor_cap + n_sink + window)) != PRHS_OK)
+  if ((s = do_retrieve(*kv, di, L, ws, q, scale, N, n_budget, n_sink, window, reuse, idx, n_sel, cap,
+                       delta, anchor_idx, anchor_n, anchor_cap, q_anchor, out, lse,
+                       anchor_cap + n_sink + window, stream)) != PRHS_OK)
     return s;
   e = cudaEventRecord(di->join, di->side);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, di->join, 0);

@@ -62,6 +62,10 @@ struct SelectLaunch {
   // logits (null: kept in shared memory only)
   float scale;
   float* logits_out;
+  // score-and-select kernel only, no forced keys: attention over the selected
+  // set into out [B][Hq][d] and lse [B][Hq] (null: selection only)
+  float* out;
+  float* lse;
 };
 
 struct CisLaunch {
@@ -164,7 +168,8 @@ size_t attn_partial_floats(const KVView& kv, bool sparse, int ctas);
 cudaError_t launch_score(const ScoreLaunch& a, const CUtensorMap* tmap, cudaStream_t s);
 cudaError_t launch_select(const SelectLaunch& a, cudaStream_t s);
 cudaError_t launch_select_global(const SelectLaunch& a, cudaStream_t s);
-// Logits and selection in one launch (a.scale, a.logits_out; a.scores unused).
+// Logits and selection in one launch (a.scale, a.logits_out; a.scores unused),
+// and the attention over the selected set when a.out is set (no forced keys).
 // Returns cudaErrorNotSupported when the cache is too long for it.
 bool score_select_fits(const KVView& kv);
 cudaError_t launch_score_select(const SelectLaunch& a, cudaStream_t s);

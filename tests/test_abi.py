@@ -99,6 +99,11 @@ def test_null_arguments_rejected(lib):
     assert lib.prhs_score_select(ctypes.byref(big), 64, 0.1, 8, None, 0, 4, None, 64, 64, 8, 64, 64,
                                  64, 8, 64, 256, 1 << 20, None) == binding.PRHS_EUNSUPPORTED
     assert lib.prhs_append_kv(ctypes.byref(kv), None, 64, None) == binding.PRHS_EINVAL
+    # retrieval needs out and lse
+    assert lib.prhs_retrieve(ctypes.byref(kv), 64, 0.1, 8, None, 0, 0, None, 64, 64, 8, 64, None, None,
+                             0, None, None, 64, 256, 1 << 20, None) == binding.PRHS_EINVAL
+    assert lib.prhs_retrieve(ctypes.byref(kv), 64, 0.1, 8, None, 0, 0, None, 64, 64, 8, 64, None, None,
+                             0, None, 64, None, 256, 1 << 20, None) == binding.PRHS_EINVAL
     # dilation radius and dilated capacity
     assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, -1, 0, 0, 0.8, 0, None, 64, 64, 64,
                                64, None) == binding.PRHS_EINVAL

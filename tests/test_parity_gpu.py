@@ -30,6 +30,9 @@ CASES = {
     # caches of 4097..8192 keys: sixteen CTAs per head in the score-and-select kernel
     "bf16_long_gqa2": dict(dtype="bf16", B=2, Hq=4, Hkv=2, d=128, t=(5000, 8192), t_max=8192,
                            n_clusters=48, steps=4, N=300, w=2),
+    # t_max above 8192: separate scoring, selection and attention launches
+    "bf16_9k_mha": dict(dtype="bf16", B=1, Hq=2, Hkv=2, d=128, t=(8500, 9500), t_max=9600,
+                        n_clusters=32, steps=4, N=256, w=2),
 }
 
 
@@ -666,8 +669,99 @@ def test_launch_counts():
         dl = torch.zeros(1, 2, device="cuda")
         ws = S.make_workspace(kv, 64 * 3 + 16)
         assert count(lambda: S.score_select(kv, dev["q"][0], wl.scale, 64, idx, n, dl, ws)) == (1 if fused else 2)
+        o = torch.zeros(1, 2, 128, device="cuda")
+        lse = torch.zeros(1, 2, device="cuda")
+        # retrieval: one launch on a short cache, else score, select and attention
+        assert count(lambda: S.retrieve(kv, dev["q"][0], wl.scale, 64, idx, n, dl, o, lse, ws)) == (1 if fused else 3)
         ss = 1 if fused else 2
-        for n_sink, window, extra in ((0, 0, 0), (2, 8, 2)):
+        for n_sink, window in ((0, 0), (2, 8)):
             dec = S.SparseDecoder(kv, N=64, w=1, tau=wl.tau, scale=wl.scale, n_sink=n_sink, window=window)
-            assert count(lambda: dec.step(dev["q"][0])) == 3 + ss + extra, (t, n_sink)
+            # gate and side attention, then the retrieval: one launch, or score (+ select),
+            # compose and set mass for forced keys, and attention
+            want = 3 if fused and not n_sink else 2 + ss + (2 if n_sink else 0) + 1
+            assert count(lambda: dec.step(dev["q"][0])) == want, (t, n_sink)
         assert S.last_error() == 0
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_retrieve(name):
+    """prhs_retrieve against the oracle: for the heads not flagged, the top-N
+    set (up to near-ties), delta and the attention over the set; flagged
+    heads' rows untouched."""
+    S, wl, dev, kv = _setup(name)
+    nb = dev["budget"] if len(set(wl.budget.tolist())) > 1 else None
+    N = 0 if nb is not None else int(wl.budget[0])
+    cap = int(wl.budget.max())
+    g = torch.Generator().manual_seed(7)
+    skip = (torch.rand(wl.B, wl.Hq, generator=g) < 0.4).to(torch.uint8)
+    skip.view(-1)[0] = 0
+    idx = torch.full((wl.B, wl.Hq, cap), -7, dtype=torch.int32, device="cuda")
+    n_sel = torch.full((wl.B, wl.Hq), -7, dtype=torch.int32, device="cuda")
+    delta = torch.full((wl.B, wl.Hq), -7.0, device="cuda")
+    out = torch.full((wl.B, wl.Hq, wl.d), -7.0, device="cuda")
+    lse = torch.full((wl.B, wl.Hq), -7.0, device="cuda")
+    ws = S.make_workspace(kv, cap)
+    S.retrieve(kv, dev["q"][2], wl.scale, N, idx, n_sel, delta, out, lse, ws, n_budget=nb,
+               head_skip=skip.cuda())
+    assert S.last_error() == 0
+    gi, gn, gd, go, gl = [x.cpu().numpy() for x in (idx, n_sel, delta, out, lse)]
+    sk = skip.numpy()
+    for b, h in _heads(wl):
+        if sk[b, h]:
+            assert gn[b, h] == -7 and gd[b, h] == -7.0 and (go[b, h] == -7.0).all() and gl[b, h] == -7.0
+            assert (gi[b, h] == -7).all()
+            continue
+        K, V = kv_rows64(wl, b, h // wl.G)
+        qv = q64(wl, 2, b, h)
+        sc = P.scores(qv, K, wl.scale)
+        gset = gi[b, h, :gn[b, h]]
+        check_topn(gset, sc, int(wl.budget[b]))
+        assert abs(gd[b, h] - P.dropped_mass(sc, gset)) <= DELTA_TOL, (b, h)
+        ro, rl = P.attention(qv, K, V, gset, wl.scale)
+        assert np.abs(go[b, h] - ro).max() <= OUT_TOL and abs(gl[b, h] - rl) <= LSE_TOL, (b, h)
+
+
+@pytest.mark.parametrize("t,N,budget_zero", [(300, 400, False), (300, 300, False), (300, 64, True),
+                                             (6000, 6000, False)])
+def test_retrieve_whole_and_empty_sets(t, N, budget_zero):
+    """A budget of at least t keeps every key (delta = 0, attention over the
+    whole cache); a zero budget and an empty cache give the empty set,
+    out = 0 and lse = -inf."""
+    import sparse_kv_selection_gb300 as S
+    from workloads.torch_io import upload
+    wl = make_workload("whole", dtype="bf16", B=3, Hq=2, Hkv=1, d=128, t=t, n_clusters=6, steps=1,
+                       N=N, w=1, seed=11)
+    dev = upload(wl)
+    lens = torch.from_numpy(wl.seq_lens.copy()).cuda()
+    lens[2] = 0                                        # an empty cache
+    kv = S.KVCache(dev["k"], dev["v"], lens, wl.Hq)
+    nb = torch.tensor([N, 0 if budget_zero else N, N], dtype=torch.int32, device="cuda")
+    cap = min(N, t)
+    idx = torch.zeros(3, 2, cap, dtype=torch.int32, device="cuda")
+    n_sel = torch.zeros(3, 2, dtype=torch.int32, device="cuda")
+    delta = torch.full((3, 2), -1.0, device="cuda")
+    out = torch.full((3, 2, 128), 5.0, device="cuda")
+    lse = torch.zeros(3, 2, device="cuda")
+    ws = S.make_workspace(kv, cap)
+    S.retrieve(kv, dev["q"][0], wl.scale, 0, idx, n_sel, delta, out, lse, ws, n_budget=nb)
+    assert S.last_error() == 0
+    gi, gn, gd, go, gl = [x.cpu().numpy() for x in (idx, n_sel, delta, out, lse)]
+    for b in range(3):
+        for h in range(2):
+            tb = int(lens[b])
+            nbud = int(nb[b])
+            if tb == 0 or nbud == 0:
+                assert gn[b, h] == 0 and (go[b, h] == 0).all() and gl[b, h] == -math.inf
+                assert gd[b, h] == (0.0 if tb == 0 else 1.0)
+                continue
+            K, V = kv_rows64(wl, b, 0)
+            qv = q64(wl, 0, b, h)
+            sc = P.scores(qv, K, wl.scale)
+            gset = gi[b, h, :gn[b, h]]
+            if nbud >= tb:
+                assert gset.tolist() == list(range(tb)) and gd[b, h] == 0.0
+            else:
+                check_topn(gset, sc, nbud)
+                assert abs(gd[b, h] - P.dropped_mass(sc, gset)) <= DELTA_TOL
+            ro, rl = P.attention(qv, K, V, gset, wl.scale)
+            assert np.abs(go[b, h] - ro).max() <= OUT_TOL and abs(gl[b, h] - rl) <= LSE_TOL, (b, h)

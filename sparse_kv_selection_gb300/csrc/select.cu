@@ -422,42 +422,61 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
   }
 
   // ---- index-ordered compaction; dropped weight of the rest ----
-  constexpr int E = 8;  // consecutive logits per thread: 4096 per block-wide scan
+  // Warp w takes keys [base + 256 w, base + 256 (w + 1)) of each tile of 4096
+  // keys, lane l the keys base + 256 w + 32 e + l (e < 8, conflict-free
+  // reads): ballots give each key's counts of keys above / at the threshold
+  // before it inside its warp, one prefix over the warps' totals the rest.
+  constexpr int E = 8;
+  constexpr int WSPAN = 32 * E;
   constexpr int TILE = SEL_THREADS * E;
   float dsum = 0.f, ssum = 0.f;  // weights exp(s - max) of dropped / kept logits
+  const unsigned below = (1u << lane) - 1u;
   for (int base = 0; base < cnt; base += TILE) {
-    unsigned u[E];
+    const int wbase = base + warp * WSPAN;
     float sv[E];
-    unsigned cgt = 0, ceq = 0;
+    unsigned mgt[E], meq[E];
+    unsigned ngt = 0, neq = 0;
 #pragma unroll
     for (int e = 0; e < E; e++) {
-      const int i = base + tid * E + e;
+      const int i = wbase + e * 32 + lane;
       sv[e] = i < cnt ? cache[i] : -INFINITY;
-      u[e] = i < cnt ? order_key(sv[e]) : 0u;
-      cgt += u[e] > thr;
-      ceq += (i < cnt) && u[e] == thr;
     }
-    unsigned tot;
-    const unsigned packed = (cgt << 16) | ceq;
-    const unsigned excl = scan_block(packed, sh.scan, tot) - packed;
-    unsigned gt_before = carry_gt + (excl >> 16);
-    unsigned eq_before = carry_eq + (excl & 0xffffu);
 #pragma unroll
     for (int e = 0; e < E; e++) {
-      const int i = base + tid * E + e;
-      if (i >= cnt) break;
+      const int i = wbase + e * 32 + lane;
+      const unsigned u = order_key(sv[e]);
+      mgt[e] = __ballot_sync(FULL_MASK, i < cnt && u > thr);
+      meq[e] = __ballot_sync(FULL_MASK, i < cnt && u == thr);
+      ngt += __popc(mgt[e]);
+      neq += __popc(meq[e]);
+    }
+    if (lane == 0) sh.scan[warp] = (ngt << 16) | neq;  // at most 4096 each
+    __syncthreads();
+    unsigned before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < SEL_WARPS; w++) {
+      const unsigned c = sh.scan[w];
+      before += w < warp ? c : 0u;
+      tot += c;
+    }
+    unsigned gt_before = carry_gt + (before >> 16);
+    unsigned eq_before = carry_eq + (before & 0xffffu);
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+      const int i = wbase + e * 32 + lane;
+      const unsigned g = gt_before + __popc(mgt[e] & below);
+      const unsigned q = eq_before + __popc(meq[e] & below);
+      gt_before += __popc(mgt[e]);
+      eq_before += __popc(meq[e]);
+      if (i >= cnt) continue;
       bool take = false;
       int pos = 0;
-      if (u[e] > thr) {
+      if ((mgt[e] >> lane) & 1u) {
         take = true;
-        pos = (int)(gt_before + min(eq_before, keq));
-        gt_before++;
-      } else if (u[e] == thr) {
-        if (eq_before < keq) {
-          take = true;
-          pos = (int)(gt_before + eq_before);
-        }
-        eq_before++;
+        pos = (int)(g + min(q, keq));
+      } else if (((meq[e] >> lane) & 1u) && q < keq) {
+        take = true;
+        pos = (int)(g + q);
       }
       const float wgt = expf(sv[e] - smax);
       if (take) {
@@ -478,6 +497,7 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
     }
     carry_gt += tot >> 16;
     carry_eq += tot & 0xffffu;
+    if (base + TILE < cnt) __syncthreads();  // the next tile rewrites the warp totals
   }
   dsum = warp_sum(dsum);
   ssum = warp_sum(ssum);
@@ -530,7 +550,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   const int qh = blockIdx.x / CL;  // the cluster's query head (b * Hq + h)
   const int b = qh / kv.Hq;
   if (a.head_skip != nullptr && a.head_skip[qh] != 0) return;  // uniform over the cluster
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int t = seq_len(kv, b);
   int Nb = a.n_budget != nullptr ? a.n_budget[b] : a.N;
   if (Nb < 0) Nb = 0;

@@ -1,21 +1,26 @@
-// Top-N selection and dropped mass from the logits of prhs_score, one
-// thread-block cluster per query head.
+// Top-N selection and dropped mass, one thread-block cluster per query head:
+// from the logits of prhs_score (select_cluster_kernel), or with the logits
+// computed from K in the same launch and, for retrieval, the attention over
+// the selected set (score_select_kernel, caches of up to 8192 keys).
 // "Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference":
-// abstract (top-k oracle selection; the dropped mass delta) and Table I
-// (S_t, N, tau(.), delta(.)).
+// abstract (top-k oracle selection before attention; the dropped mass delta),
+// Table I (S_t, N, tau(.), delta(.)) and the Table V caption (attention over
+// the selected KV entries only).
 //
-// The CL CTAs of a cluster (often one) each hold a contiguous slice of the
-// head's logits in shared memory (one read of the logits from L2/HBM). The
-// threshold is found on value bins: the logit range, a 2048-bin histogram over
-// it summed into CTA 0 through distributed shared memory, a second 2048 bins
-// inside the threshold bin when it holds more than SEL_CANDS logits, then the
-// candidates of the final bin ranked exactly; heavy ties fall back to three
+// select_cluster_kernel: the CL CTAs of a cluster (often one) each hold a
+// contiguous slice of the head's logits in shared memory (one read of the
+// logits from L2/HBM). The threshold is found on value bins: the logit
+// range, a 2048-bin histogram over it summed into CTA 0 through distributed
+// shared memory, a second 2048 bins inside the threshold bin when it holds
+// more than SEL_CANDS logits, then the candidates of the final bin ranked
+// exactly; heavy ties fall back to three
 // radix passes (11, 11, 10 bits of an order-preserving key). Every CTA takes
 // the same decision. The index-ordered compaction gets each CTA's output
 // offset from the counts of the lower ranks, so the set comes out ascending
 // with ties resolved to the lowest index, and the dropped mass is the cluster
 // sum of the unselected weights. Forced keys (sinks, window) are ranked below
-// every other key and left to the caller.
+// every other key and left to the caller. score_select_kernel runs the same
+// one-CTA selection in CTA 0 of its cluster after the cluster has scored.
 #include <cooperative_groups.h>
 
 #include "kernels.h"

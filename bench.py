@@ -115,7 +115,8 @@ def run_reference(args):
     value = done_tot / el_tot
     sample = (f"{heads_tot} (sequence, head) decode runs of {wl.steps} queries each, "
               f"~{per_step:.1f} s per step, fp64 numpy, 1 thread")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+    # n_gpus: the N this arm was launched at (its work runs on rank 0's host cores)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el_tot / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator, workloads/)",

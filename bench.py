@@ -246,9 +246,14 @@ def decode_diagnostics(S, kvs, q, scale, N, nb, idx, n_sel, reuse, delta, ws):
     dl = delta.cpu().numpy()
     fresh = dl[~r_h]
     mean = lambda x: float(np.mean(x)) if len(x) else None
+    # retained mass tau(S) = 1 - delta(S): beta_emp = tau(own top-N) - tau(attended set)
+    #                                              = delta(attended set) - delta(own top-N)
+    beta = [du_ - dt_ for du_, dt_ in zip(d_used, d_top)]
     return {"reuse_delta_of_attended_set": mean(d_used),
             "reuse_delta_of_own_topN": mean(d_top),
             "reuse_topN_covered": mean(cover),
+            "beta_emp": mean(beta),
+            "rho_hat": float((~r_h).mean()),
             "retrieve_delta": mean(fresh[np.isfinite(fresh)]),
             "reuse_pairs": len(d_used),
             "untimed": True}

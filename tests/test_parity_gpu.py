@@ -765,3 +765,53 @@ def test_retrieve_whole_and_empty_sets(t, N, budget_zero):
                 assert abs(gd[b, h] - P.dropped_mass(sc, gset)) <= DELTA_TOL
             ro, rl = P.attention(qv, K, V, gset, wl.scale)
             assert np.abs(go[b, h] - ro).max() <= OUT_TOL and abs(gl[b, h] - rl) <= LSE_TOL, (b, h)
+
+
+@pytest.mark.parametrize("name,n_sink,window", [("gqa4_bf16", 0, 0), ("mha_bf16_ragged", 4, 32),
+                                                ("bf16_9k_mha", 4, 64), ("paged_bf16", 2, 16)])
+def test_retrieve_anchors_and_forced_keys(name, n_sink, window):
+    """prhs_retrieve with the anchor buffers and forced keys: the attended set
+    is the forced keys with the top N of the keys between them, delta its
+    dropped mass and out/lse the attention over it; the anchor row holds the
+    ranked part only, anchor_n its size and q_anchor the query."""
+    S, wl, dev, kv = _setup(name)
+    N = int(wl.budget.min())
+    nb = None
+    if len(set(wl.budget.tolist())) > 1:
+        nb = dev["budget"]
+    cap = int(wl.budget.max()) + n_sink + window
+    acap = int(wl.budget.max())
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx = torch.full((wl.B, wl.Hq, cap), -1, **i32)
+    n_sel = torch.zeros(wl.B, wl.Hq, **i32)
+    delta = torch.zeros(wl.B, wl.Hq, device="cuda")
+    out = torch.zeros(wl.B, wl.Hq, wl.d, device="cuda")
+    lse = torch.zeros(wl.B, wl.Hq, device="cuda")
+    aidx = torch.full((wl.B, wl.Hq, acap), -1, **i32)
+    an = torch.zeros(wl.B, wl.Hq, **i32)
+    qa = torch.zeros_like(dev["q"][1])
+    ws = S.make_workspace(kv, cap)
+    S.retrieve(kv, dev["q"][1], wl.scale, 0 if nb is not None else N, idx, n_sel, delta, out, lse, ws,
+               n_budget=nb, anchor_idx=aidx, anchor_n=an, q_anchor=qa, n_sink=n_sink, window=window)
+    assert S.last_error() == 0
+    gi, gn, gd, go, gl, ga, gan = [x.cpu().numpy() for x in (idx, n_sel, delta, out, lse, aidx, an)]
+    assert torch.equal(qa, dev["q"][1])
+    for b, h in _heads(wl):
+        t = int(wl.seq_lens[b])
+        K, V = kv_rows64(wl, b, h // wl.G)
+        qv = q64(wl, 1, b, h)
+        sc = P.scores(qv, K, wl.scale)
+        nbud = int(wl.budget[b])
+        ranked = ga[b, h, :gan[b, h]]
+        forced = P.forced_set(t, n_sink, window)
+        mid = t - len(forced)
+        assert len(ranked) == min(nbud, mid)
+        if len(ranked) < mid:  # the ranked part against the middle keys' top N, up to near-ties
+            lo = min(n_sink, t)
+            check_topn(ranked - lo, sc[lo:lo + mid], nbud)
+        gset = gi[b, h, :gn[b, h]]
+        want = np.union1d(forced, ranked)
+        assert gset.tolist() == want.tolist(), (b, h)
+        assert abs(gd[b, h] - P.dropped_mass(sc, gset)) <= DELTA_TOL, (b, h)
+        ro, rl = P.attention(qv, K, V, gset, wl.scale)
+        assert np.abs(go[b, h] - ro).max() <= OUT_TOL and abs(gl[b, h] - rl) <= LSE_TOL, (b, h)

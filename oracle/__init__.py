@@ -15,8 +15,9 @@ itself: hand-computed cases, brute force over all subsets on tiny inputs,
 closed-form identities, library routines (torch SDPA, scipy cosine) and the
 Fig. 4 dilation example. The multi-step CIS schedule (which query is the
 anchor, when a fresh retrieval happens) is a reading of Fig. 4 and Fig. 8;
-its parts are pinned, the schedule itself is "parity unpinned" beyond the
-invariants listed in the tests.
+a hand case fixes it where the plausible alternatives part (gating against
+the previous query, an anchor query that never moves), and a hand GQA case
+fixes which KV head each query head reads (h // G).
 """
 from .prhs import (scores, softmax, logsumexp, top_n, dropped_mass, cosine, cis_gate,
                    dilate, attention, dense_attention, decode_head, decode_workload,

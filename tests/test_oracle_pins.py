@@ -245,6 +245,54 @@ def check_max_run(rng):
     assert a == b
 
 
+def check_gate_target_hand():
+    """Four queries whose schedule differs by which query each is gated
+    against: the anchor (the last query that retrieved), not the previous
+    query, and the anchor moves on every retrieval. The expected flags and
+    sets are derived by hand in tests/golden/cis_schedule_hand.txt."""
+    g = _read_golden("cis_schedule_hand.txt")
+    a = np.radians(g["key_angles_deg"])
+    K = g["key_norm"][0] * np.stack([np.cos(a), np.sin(a)], axis=1)
+    b = np.radians(g["query_angles_deg"])
+    qs = np.stack([np.cos(b), np.sin(b)], axis=1)
+    V = np.arange(2 * len(a), dtype=np.float64).reshape(len(a), 2)
+    rec = P.decode_head(qs, K, V, int(g["N"][0]), int(g["w"][0]), g["tau"][0], 1.0)
+    assert [int(r.reuse) for r in rec] == [int(x) for x in g["reuse"]]
+    for s, r in enumerate(rec):
+        assert r.S.tolist() == [int(x) for x in g[f"S{s}"]], s
+        assert r.anchor_S.tolist() == [int(x) for x in g[f"anchor{s}"]], s
+        if not r.reuse:   # a one-key set attends exactly that key's value row
+            assert np.allclose(r.out, V[r.S[0]], atol=0)
+
+
+def _hand_gqa_workload():
+    """Hq = 8 query heads over Hkv = 2 KV heads (group 4), t = 4, d = 2:
+    KV head 0's dominant key (along e1) is key 0, KV head 1's is key 3, and
+    every query is e1. Under the grouped layout query heads 0-3 read KV head 0
+    and heads 4-7 read KV head 1, so their top-1 sets are {0} x4 then {3} x4."""
+    from workloads import Workload
+    K = np.zeros((1, 2, 4, 2), np.float32)
+    K[0, 0] = [[5, 0], [1, 0], [0, 1], [-1, 0]]
+    K[0, 1] = [[-1, 0], [0, 1], [1, 0], [5, 0]]
+    V = np.zeros_like(K)
+    V[0, 0, :, 0] = [10, 11, 12, 13]
+    V[0, 1, :, 0] = [20, 21, 22, 23]
+    q = np.zeros((1, 1, 8, 2), np.float32)
+    q[..., 0] = 1.0
+    return Workload(name="hand_gqa", dtype="f32", B=1, Hq=8, Hkv=2, d=2,
+                    seq_lens=np.array([4], np.int32), t_max=4, paged=False, block_size=16,
+                    block_table=None, K=K, V=V, q=q, budget=np.array([1], np.int32), w=0,
+                    tau=0.8, scale=1.0, steps=1, seed=0)
+
+
+def check_head_map_hand():
+    res = P.decode_workload(_hand_gqa_workload())
+    sets = [res[(0, h)][0].S.tolist() for h in range(8)]
+    assert sets == [[0]] * 4 + [[3]] * 4, sets
+    outs = [res[(0, h)][0].out[0] for h in range(8)]
+    assert outs == [10.0] * 4 + [23.0] * 4, outs
+
+
 def check_widen():
     bits = np.array([0x3F80, 0xC020, 0x0000, 0x8000, 0x7F7F], np.uint16)
     v = P.widen(bits, "bf16")
@@ -508,3 +556,76 @@ def test_mutation_anchor_holds_forced(monkeypatch, rng):
     monkeypatch.setattr(P, "top_n_between",
                         lambda s, N, n, wdw: np.union1d(orig(s, N, n, wdw), P.forced_set(len(s), n, wdw)))
     assert _caught(check_decode_grow, rng)
+
+
+def test_gate_target_hand():
+    check_gate_target_hand()
+
+
+def test_head_map_hand():
+    check_head_map_hand()
+
+
+def _schedule_variant(gate_previous=False, keep_first_anchor_query=False):
+    """decode_head with one planted mistake in its schedule: gating against
+    the previous query instead of the anchor, or never moving the anchor
+    query after the first retrieval."""
+    def bad(q_steps, K, V, N, w, tau, scale, keep_scores=False, max_run=0):
+        K = np.asarray(K, np.float64)
+        V = np.asarray(V, np.float64)
+        t = K.shape[0]
+        anchor_S = anchor_q = prev_q = None
+        rec = []
+        for q in np.asarray(q_steps, np.float64):
+            ref_q = prev_q if gate_previous else anchor_q
+            c, reuse = (None, False) if anchor_S is None else P.cis_gate(q, ref_q, tau)
+            s = P.scores(q, K, scale)
+            delta = None
+            if reuse:
+                S = P.dilate(anchor_S, w, t)
+            else:
+                S = P.top_n(s, N)
+                delta = P.dropped_mass(s, S)
+                anchor_S = S
+                if anchor_q is None or not keep_first_anchor_query:
+                    anchor_q = q
+            prev_q = q
+            out, lse = P.attention(q, K, V, S, scale)
+            rec.append(P.HeadStep(reuse=reuse, cos=c, S=S, anchor_S=anchor_S, delta=delta,
+                                  delta_used=P.dropped_mass(s, S), s_nth=None, out=out, lse=lse))
+        return rec
+    return bad
+
+
+def test_mutation_gate_against_previous_query(monkeypatch):
+    monkeypatch.setattr(P, "decode_head", _schedule_variant(gate_previous=True))
+    assert _caught(check_gate_target_hand)
+
+
+def test_mutation_anchor_query_not_moved(monkeypatch):
+    monkeypatch.setattr(P, "decode_head", _schedule_variant(keep_first_anchor_query=True))
+    assert _caught(check_gate_target_hand)
+
+
+def test_schedule_variant_without_mistake_passes(monkeypatch):
+    """The hand-written variant above is itself correct when no mistake is
+    planted, so the two mutation tests fail for the planted reason only."""
+    monkeypatch.setattr(P, "decode_head", _schedule_variant())
+    check_gate_target_hand()
+
+
+def test_mutation_head_map_modulo(monkeypatch):
+    """Query head h reading KV head h % Hkv (interleaved grouping) instead of
+    h // G (consecutive grouping)."""
+    def bad(wl, heads=None, steps=None, keep_scores=False, max_run=0):
+        heads = [(b, h) for b in range(wl.B) for h in range(wl.Hq)] if heads is None else heads
+        res = {}
+        for b, hq in heads:
+            kvh = hq % wl.Hkv
+            K = P.widen(wl.logical_rows("K", b, kvh), wl.dtype)
+            V = P.widen(wl.logical_rows("V", b, kvh), wl.dtype)
+            qs = P.widen(wl.q[:wl.steps, b, hq], wl.dtype)
+            res[(b, hq)] = P.decode_head(qs, K, V, int(wl.budget[b]), wl.w, wl.tau, wl.scale)
+        return res
+    monkeypatch.setattr(P, "decode_workload", bad)
+    assert _caught(check_head_map_hand)

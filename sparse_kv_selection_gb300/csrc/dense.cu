@@ -399,7 +399,11 @@ __global__ void __maxnreg__(DenseGroups<G>::REGS)
       for (int e = 0; e < S::EL; e++) o[gg][e] *= corr;
       m[gg] = mx;
     }
-    // p * v: lane (r, j) adds the keys of slot r into its d-slice j
+    // p * v: lane (r, j) adds the keys of slot r into its d-slice j. On a
+    // head's last tile the rows past t_b were not loaded on a paged cache
+    // (whatever the shared memory held, possibly not finite): their weight
+    // is 0 and their row is taken as 0, so they add nothing.
+    const bool partial = tile0 + S::TK > k1;
 #pragma unroll
     for (int p = 0; p < 8; p++) {
       const int key = wl * 32 + r * 8 + p;
@@ -409,6 +413,10 @@ __global__ void __maxnreg__(DenseGroups<G>::REGS)
         const int line = key * S::NH + h;
         const uint4 cw = *reinterpret_cast<const uint4*>(vt + line * 128 + ((j ^ (line & 7)) << 4));
         Elem<T>::unpack(cw, vf + h * S::EPC);
+      }
+      if (partial && tile0 + key >= k1) {
+#pragma unroll
+        for (int e = 0; e < S::EL; e++) vf[e] = 0.f;
       }
 #pragma unroll
       for (int gg = 0; gg < GH; gg++) {

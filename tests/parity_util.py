@@ -86,11 +86,18 @@ def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0):
                 assert abs(dl[s, b, h] - rec.delta) <= DELTA_TOL, (b, h, s)
             else:
                 assert same, ("dilated set differs", b, h, s)
-            assert np.abs(o[s, b, h] - rec.out).max() <= OUT_TOL, (b, h, s)
-            assert abs(l[s, b, h] - rec.lse) <= LSE_TOL, (b, h, s)
+            if same:
+                want_o, want_l = rec.out, rec.lse
+            else:
+                # a retrieving set that differs only at near-ties: the attention
+                # is checked on the GPU's own set, then this head stops
+                check_topn(gset, rec.scores, int(wl.budget[b]))
+                K, V = kv_rows64(wl, b, h // wl.G)
+                want_o, want_l = P.attention(q64(wl, s, b, h), K, V, gset, wl.scale)
+            assert np.abs(o[s, b, h] - want_o).max() <= OUT_TOL, (b, h, s)
+            assert abs(l[s, b, h] - want_l) <= LSE_TOL, (b, h, s)
             compared += 1
             if not same:
-                check_topn(gset, rec.scores, int(wl.budget[b]))  # differs only at near-ties
                 break
             assert n[s, b, h] == len(rec.S), (b, h, s)
     return compared, r

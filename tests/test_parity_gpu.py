@@ -33,6 +33,24 @@ CASES = {
     # t_max above 8192: separate scoring, selection and attention launches
     "bf16_9k_mha": dict(dtype="bf16", B=1, Hq=2, Hkv=2, d=128, t=(8500, 9500), t_max=9600,
                         n_clusters=32, steps=4, N=256, w=2),
+    # a cache of one key: every budget covers it (set = {0}, delta = 0)
+    "t1_bf16": dict(dtype="bf16", B=2, Hq=2, Hkv=2, d=128, t=1, n_clusters=0, steps=4, N=4, w=2),
+    "t1_paged_f32": dict(dtype="f32", B=2, Hq=4, Hkv=1, d=64, t=1, paged=True, block_size=16,
+                         n_clusters=0, steps=4, N=1, w=1),
+    # caches of 7 keys (less than one 16-key tile), contiguous and paged, grouped
+    "t7_paged_gqa4": dict(dtype="bf16", B=2, Hq=8, Hkv=2, d=128, t=7, paged=True, block_size=16,
+                          n_clusters=0, steps=4, N=3, w=1),
+    "t7_bf16_gqa4": dict(dtype="bf16", B=1, Hq=4, Hkv=1, d=128, t=7, n_clusters=0, steps=4, N=3,
+                         w=2),
+    # ragged caches of 4 and 7 keys with w = 0 (DirectReuse: the shared set is
+    # the anchor's top-N set itself)
+    "t4to7_f32_w0": dict(dtype="f32", B=3, Hq=2, Hkv=1, d=64, t=(1, 7), t_max=7, n_clusters=0,
+                         steps=4, N=2, w=0),
+    "w0_bf16_gqa4": dict(dtype="bf16", B=2, Hq=8, Hkv=2, d=128, t=1200, n_clusters=16, steps=6,
+                         N=64, w=0),
+    # budget above some caches of a grouped paged batch (lengths 212..387, N = 300)
+    "paged_gqa4_n_gt_t": dict(dtype="bf16", B=4, Hq=8, Hkv=2, d=128, t=(5, 400), paged=True,
+                              block_size=16, n_clusters=lambda tb: tb // 64, steps=6, N=300, w=2),
 }
 
 

@@ -32,6 +32,10 @@
  *    Query head h reads KV head h / (Hq / Hkv).
  *  - Inputs must be finite; NaN or Inf in q, K or V gives undefined results.
  *  - No call is thread-safe against another call using the same workspace.
+ *    prhs_decode_step keeps one internal side stream (and fork/join events)
+ *    per caller stream, created by the first decode step on that stream:
+ *    make that first step outside stream capture. Steps on different caller
+ *    streams, each with its own workspace and buffers, may run concurrently.
  */
 #ifndef PRHS_H
 #define PRHS_H
@@ -248,6 +252,15 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
  * is already t_max is left as it is and flagged (PRHS_DEV_CAPACITY). */
 prhs_status prhs_append_kv(const prhs_kv* kv, const void* k_new, const void* v_new,
                            cudaStream_t stream);
+
+/* Self-test of the kernels' failure path (no counterpart in the paper): one
+ * warp waits on a shared-memory mbarrier that nothing arrives on, through the
+ * same bounded wait every TMA pipeline of the library uses, but giving up
+ * after limit_us microseconds (1 <= limit_us <= 1000000) instead of about a
+ * second. The wait runs out, PRHS_DEV_TIMEOUT is set in the device error word
+ * and the kernel returns; no fault, the context stays usable. A following
+ * prhs_last_error() returns PRHS_EDEVICE with that bit. */
+prhs_status prhs_selftest_wait_timeout(unsigned limit_us, cudaStream_t stream);
 
 /* Synchronise the current device, read and clear the device error word.
  * PRHS_OK when it was zero, PRHS_EDEVICE otherwise, PRHS_ECUDA when the

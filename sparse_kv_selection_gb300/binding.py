@@ -24,7 +24,7 @@ EXPORTS = ["prhs_workspace_size", "prhs_workspace_init", "prhs_score_select", "p
            "prhs_score",
            "prhs_select", "prhs_cis_dilate",
            "prhs_sparse_attn", "prhs_sparse_attn_noalloc", "prhs_set_mass", "prhs_dense_attn",
-           "prhs_decode_step", "prhs_append_kv", "prhs_last_error",
+           "prhs_decode_step", "prhs_append_kv", "prhs_selftest_wait_timeout", "prhs_last_error",
            "prhs_device_error_bits", "prhs_status_str", "prhs_last_message", "prhs_num_sms",
            "prhs_launch_count"]
 
@@ -72,6 +72,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "prhs_decode_step": (I, [KV, P, F, I, P, I, I, I, D, I, P, P, P, I, P, P, P, I, P, P, P, P, P, Z,
                                  P]),
         "prhs_append_kv": (I, [KV, P, P, P]),
+        "prhs_selftest_wait_timeout": (I, [ctypes.c_uint, P]),
         "prhs_last_error": (I, []),
         "prhs_device_error_bits": (ctypes.c_uint, []),
         "prhs_launch_count": (ctypes.c_ulonglong, []),
@@ -272,6 +273,13 @@ def append_kv(kv, k_new, v_new, stream=None) -> None:
     """Write one key and value row per (sequence, KV head) at each
     sequence's current length and advance kv.seq_lens (prhs_append_kv)."""
     _check(load().prhs_append_kv(kv.ref(), _ptr(k_new), _ptr(v_new), _stream(stream)), "append_kv")
+
+
+def selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (prhs_selftest_wait_timeout): its
+    wait runs out after limit_us and sets DEV_TIMEOUT in the error word."""
+    _check(load().prhs_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "selftest_wait_timeout")
 
 
 def last_error() -> int:

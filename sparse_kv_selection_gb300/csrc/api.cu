@@ -5,8 +5,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "kernels.h"
 
@@ -34,13 +36,24 @@ prhs_status cuda_fail(cudaError_t e, const char* what) {
   return fail(PRHS_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// The second branch of prhs_decode_step for one caller stream: its own side
+// stream and fork/join events, so that decode steps issued on different
+// caller streams (other host threads, other workspaces) never share an event
+// or land on a stream another caller is capturing. `mu` keeps one step's
+// record/wait sequence whole when several threads use the same caller stream.
+struct SideBranch {
+  cudaStream_t caller = nullptr;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+
 constexpr int MAX_DEVICES = 64;
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   unsigned* err = nullptr;
-  cudaStream_t side = nullptr;   // second branch of prhs_decode_step
-  cudaEvent_t fork = nullptr, join = nullptr;
+  std::vector<std::unique_ptr<SideBranch>> branches;  // one per caller stream seen
 };
 DeviceInfo g_dev[MAX_DEVICES];
 std::mutex g_dev_mu;
@@ -60,14 +73,32 @@ prhs_status device_info(DeviceInfo** out) {
     e = cudaGetSymbolAddress(&p, g_error_word);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
     di.err = static_cast<unsigned*>(p);
-    e = cudaStreamCreateWithFlags(&di.side, cudaStreamNonBlocking);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
-    e = cudaEventCreateWithFlags(&di.fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&di.join, cudaEventDisableTiming);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreateWithFlags");
     di.ready = true;
   }
   *out = &di;
+  return PRHS_OK;
+}
+
+// The side branch of `caller` on the current device, created on first use.
+prhs_status side_branch(DeviceInfo* di, cudaStream_t caller, SideBranch** out) {
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  for (auto& b : di->branches)
+    if (b->caller == caller) {
+      *out = b.get();
+      return PRHS_OK;
+    }
+  std::unique_ptr<SideBranch> b(new SideBranch);
+  b->caller = caller;
+  cudaError_t e = cudaStreamCreateWithFlags(&b->side, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags (decode side stream)");
+  e = cudaEventCreateWithFlags(&b->fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(b->side);
+    return cuda_fail(e, "cudaEventCreateWithFlags (decode fork/join)");
+  }
+  *out = b.get();
+  di->branches.push_back(std::move(b));
   return PRHS_OK;
 }
 
@@ -488,6 +519,19 @@ prhs_status do_retrieve(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void
                  ATTN_MIN_ROWS, rows_hint);
 }
 
+// One warp waits on an mbarrier that nothing ever arrives on: the bounded
+// wait of the other kernels gives up after limit_ns, raises PRHS_DEV_TIMEOUT
+// and the kernel returns (nothing else is in flight on the barrier).
+__global__ void __launch_bounds__(32) wait_selftest_kernel(unsigned* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  mbar_wait(&bar, 0, err, limit_ns);
+}
+
 }  // namespace
 
 // Internal hooks for other translation units of the library (no C linkage).
@@ -737,27 +781,37 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   // dilated sets and attend on the side stream, while the retrieving heads
   // score, select and attend on the caller's stream; the caller's stream then
   // waits for the side branch.
-  cudaError_t e = cudaEventRecord(di->fork, stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(di->side, di->fork, 0);
+  SideBranch* br = nullptr;
+  if ((s = side_branch(di, stream, &br)) != PRHS_OK) return s;
+  std::lock_guard<std::mutex> branch_lock(br->mu);
+  cudaError_t e = cudaEventRecord(br->fork, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(br->side, br->fork, 0);
   if (e != cudaSuccess) return cuda_fail(e, "decode: fork");
   // The branch more likely to be the longer one is issued first, so its CTAs
   // are placed first: the one-launch retrieval on short caches, the reusing
   // heads' attention otherwise (measured both ways on 4K-, 32K- and 128K-key
   // caches). The retrieving heads' sets hold at most anchor_cap (+ forced) rows.
   const bool retrieve_first = !forced && score_select_fits(view_of(*kv, di->err));
-  for (int branch = 0; branch < 2; branch++) {
+  for (int branch = 0; branch < 2 && s == PRHS_OK; branch++) {
     if ((branch == 0) == retrieve_first) {
       s = do_retrieve(*kv, di, L, ws, q, scale, N, n_budget, n_sink, window, reuse, idx, n_sel, cap,
                       delta, anchor_idx, anchor_n, anchor_cap, q_anchor, out, lse,
                       anchor_cap + n_sink + window, stream);
     } else {
-      s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, di->side, reuse, 1, true, 0,
+      s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, br->side, reuse, 1, true, 0,
                   ATTN_SIDE_MIN_ROWS);
     }
-    if (s != PRHS_OK) return s;
   }
-  e = cudaEventRecord(di->join, di->side);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, di->join, 0);
+  // The join is recorded even after a failed launch, so the side stream never
+  // stays forked (a capture would otherwise end unjoined); the first failure
+  // is what the caller sees.
+  const std::string first_message = t_message;
+  e = cudaEventRecord(br->join, br->side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, br->join, 0);
+  if (s != PRHS_OK) {
+    t_message = first_message;
+    return s;
+  }
   return e == cudaSuccess ? PRHS_OK : cuda_fail(e, "decode: join");
 }
 
@@ -775,6 +829,16 @@ prhs_status prhs_append_kv(const prhs_kv* kv, const void* k_new, const void* v_n
   a.v_new = v_new;
   a.seq_lens = const_cast<int32_t*>(kv->seq_lens);
   return launch_result(launch_append(a, stream), "append kernel");
+}
+
+prhs_status prhs_selftest_wait_timeout(unsigned limit_us, cudaStream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u)
+    return fail(PRHS_EINVAL, "limit_us must be in [1, 1000000] (got %u)", limit_us);
+  DeviceInfo* di = nullptr;
+  prhs_status s = device_info(&di);
+  if (s != PRHS_OK) return s;
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(di->err, 1000ull * limit_us);
+  return launch_result(cudaGetLastError(), "wait self-test kernel");
 }
 
 prhs_status prhs_last_error(void) {

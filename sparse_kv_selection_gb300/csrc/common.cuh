@@ -143,15 +143,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Wait for the phase of `parity` to complete, giving up after about a second.
-// On timeout the error word gets PRHS_DEV_TIMEOUT and false is returned.
+// Wait for the phase of `parity` to complete, giving up after limit_ns (about
+// a second unless a caller asks for less). On timeout the error word gets
+// PRHS_DEV_TIMEOUT and false is returned.
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (unsigned n = 1;; n++) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 255u) == 0 && globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+    if ((n & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       raise_error(err, PRHS_DEV_TIMEOUT);
       return false;
     }

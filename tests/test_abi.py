@@ -119,6 +119,9 @@ def test_null_arguments_rejected(lib):
                                64, None) == binding.PRHS_EINVAL
     assert lib.prhs_dense_attn(ctypes.byref(kv), None, 0.1, 64, 64, 256, 1 << 20, None) == binding.PRHS_EINVAL
     assert lib.prhs_workspace_init(None, 0, None) == binding.PRHS_EWORKSPACE
+    # the wait self-test takes a limit of 1 us .. 1 s
+    assert lib.prhs_selftest_wait_timeout(0, None) == binding.PRHS_EINVAL
+    assert lib.prhs_selftest_wait_timeout(1000001, None) == binding.PRHS_EINVAL
 
 
 def test_status_strings(lib):

@@ -459,7 +459,8 @@ def run_ours(args):
     S.retrieve(kvs[0], q[0], scale, N, torch.zeros(B, Hq, acap, **i32), torch.zeros(B, Hq, **i32),
                torch.zeros(B, Hq, device="cuda"), o_tmp, l_tmp, ws, n_budget=nb, head_skip=reuse[0])
     fused = S.binding.launch_count() - c0 == 1   # scoring, selection and attention in one kernel
-    names = ["cis", "retrieve", "sparse_attn"] if fused else ["cis", "score", "select", "sparse_attn"]
+    names = (["cis", "retrieve", "sparse_attn"] if fused else
+             ["cis", "score", "select", "retrieve_attn", "sparse_attn"])
     cis_idx = torch.zeros(B, Hq, cap, **i32)
     cis_n = torch.zeros(B, Hq, **i32)
     cis_r = torch.zeros(B, Hq, device="cuda", dtype=torch.uint8)
@@ -511,10 +512,13 @@ def run_ours(args):
     if fused:
         ktime = {"cis": t_cis, "retrieve": time_graph(k_retrieve), "sparse_attn": t_attn}
     else:
+        # the retrieval's attention (V rows weighted by the workspace logits)
+        # is timed as the whole retrieval minus its scoring and selection
         t_score = time_graph(lambda: k_score(False))
         t_ss = time_graph(lambda: k_score(True))
+        t_ret = time_graph(k_retrieve)
         ktime = {"cis": t_cis, "score": t_score, "select": max(0.0, t_ss - t_score),
-                 "sparse_attn": t_attn}
+                 "retrieve_attn": max(0.0, t_ret - t_ss), "sparse_attn": t_attn}
     assert S.last_error() == 0
     launches = {n: Sq * args.steps for n in names}
 
@@ -532,10 +536,11 @@ def run_ours(args):
     score_bytes /= Sq
     rows = sum(gathered_rows(idx[s].cpu().numpy() if G > 1 else None, n_h[s], G) for s in range(Sq))
     attn_bytes = float(rows * 2 * d * es + 4 * n_h.sum() + Sq * B * Hq * (d * es + 4 * d + 4)) / Sq
-    # retrieval: the K rows scored plus the V rows of the fresh sets
+    # retrieval: the K rows scored plus the V rows of the fresh sets (and
+    # their logits when the attention is a launch of its own)
     fresh_rows = sum(float(n_h[s][~r_h[s]].sum()) for s in range(Sq)) / Sq
     kb = {"retrieve": score_bytes + fresh_rows * d * es, "sparse_attn": attn_bytes} if fused else \
-        {"score": score_bytes, "sparse_attn": attn_bytes}
+        {"score": score_bytes, "retrieve_attn": fresh_rows * (d * es + 4), "sparse_attn": attn_bytes}
     peak, peak_kind = measured_peak_gbs()
     traffic = profiled_traffic()
     kern = {}

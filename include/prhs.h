@@ -130,7 +130,9 @@ prhs_status prhs_score_select(const prhs_kv* kv, const void* q, float scale, int
  * untouched. A cache of t_max <= 8192 without forced keys takes one kernel
  * launch (logits, selection and attention in one thread-block cluster per
  * head); otherwise it is scoring, selection (with the forced keys' passes)
- * and sparse attention. out and lse must be non-null. */
+ * and an attention launch that weights each selected V row by the logit the
+ * scoring left in the workspace (K rows are read once, by the scoring).
+ * out and lse must be non-null. */
 prhs_status prhs_retrieve(const prhs_kv* kv, const void* q, float scale, int N,
                           const int32_t* n_budget, int n_sink, int window,
                           const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,

@@ -396,7 +396,8 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
                     float scale, const int32_t* idx, const int32_t* n_sel, int cap, float* out,
                     float* lse, bool sparse, cudaStream_t st, const uint8_t* unit_mask = nullptr,
                     int mask_want = 0, bool second_region = false, int max_ctas = 0,
-                    int min_rows = ATTN_MIN_ROWS, int rows_hint = 0) {
+                    int min_rows = ATTN_MIN_ROWS, int rows_hint = 0,
+                    const float* logits = nullptr) {
   // the kernels index the concatenated rows of all units with 32-bit integers
   if ((long long)kv.B * kv.Hq * (sparse ? cap : t_max_of(kv)) >= (1ll << 30))
     return fail(PRHS_EUNSUPPORTED, "B * Hq * %s = %lld rows above 2^30", sparse ? "cap" : "t_max",
@@ -417,6 +418,7 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
   a.ctas = attn_ctas(kv, sparse, cap, di->sms);
   a.min_rows = min_rows;
   a.cluster = sparse ? attn_cluster_size(kv, rows_hint > 0 ? rows_hint : cap, di->sms) : 0;
+  a.logits = sparse ? logits : nullptr;
   if (max_ctas > 0 && a.ctas > max_ctas) a.ctas = max_ctas;
   return launch_result(launch_attn(a, sparse, st), sparse ? "sparse attention" : "dense attention");
 }
@@ -500,7 +502,9 @@ prhs_status forced_finish(const prhs_kv& kv, DeviceInfo* di, const Layout& L, vo
 // attention over the set into out/lse. Short caches without forced keys take
 // one launch (score, select and attend); otherwise scoring, selection, the
 // forced keys' composition and set mass, and sparse attention over the heads
-// with head_skip == 0. rows_hint bounds the rows of one head's set.
+// with head_skip == 0, which weights each selected V row by the logit the
+// scoring left in the workspace (K is not read again). rows_hint bounds the
+// rows of one head's set.
 prhs_status do_retrieve(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws, const void* q,
                         float scale, int N, const int32_t* n_budget, int n_sink, int window,
                         const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap, float* delta,
@@ -516,7 +520,8 @@ prhs_status do_retrieve(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void
                                    n_sel, cap, delta, n_sink, window, st)) != PRHS_OK)
     return s;
   return do_attn(kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, st, head_skip, 0, false, 0,
-                 ATTN_MIN_ROWS, rows_hint);
+                 ATTN_MIN_ROWS, rows_hint,
+                 reinterpret_cast<const float*>(static_cast<const char*>(ws) + L.scores));
 }
 
 // One warp waits on an mbarrier that nothing ever arrives on: the bounded

@@ -23,6 +23,10 @@
 // log2 e). Units are query heads in both kernels; the kernel template can
 // also give one unit the G query heads of a KV head (registers per thread
 // grow with G, which costs more occupancy than the L2 re-reads it saves).
+//
+// Logit source (LG). After a fresh selection the logits of every key are
+// still in the workspace: the retrieving heads' attention then reads each
+// selected row's logit (4 bytes) and its V row only, not its K row.
 #include "kernels.h"
 
 namespace prhs {
@@ -63,10 +67,11 @@ __device__ __forceinline__ void merge_coeffs(float m1, float m2, float& M, float
   c2 = M == -INFINITY ? 0.f : exp2f(m2 - M);
 }
 
-template <typename T, int D, int G, bool SPARSE>
+template <typename T, int D, int G, bool SPARSE, bool LG>
 __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch a) {
   using S = AttnShape<T, D>;
-  constexpr int UNROLL = AttnUnroll<S::CPL, G>::value;
+  static_assert(!LG || (SPARSE && G == 1), "logit source: sparse, one query head per unit");
+  constexpr int UNROLL = AttnUnroll<S::CPL, G>::value * (LG ? 2 : 1);
   constexpr int STEP = 16 * UNROLL;  // rows per CTA iteration
   constexpr int PW = D + 4;          // partial record: m, l, 2 pad, o[D] (16-byte aligned)
   static_assert(D <= ATTN_THREADS && D % 64 == 0, "merge maps one thread per output element");
@@ -217,9 +222,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
     for (int g = 0; g < G; g++)
 #pragma unroll
       for (int cc = 0; cc < S::CPL; cc++)
-        qraw[g][cc] = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.q) +
-                                                           ((long long)(qh0 + g) * D) * sizeof(T)) +
-                            cc * 8 + j);
+        qraw[g][cc] = LG ? make_uint4(0, 0, 0, 0)
+                         : __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.q) +
+                                                                ((long long)(qh0 + g) * D) * sizeof(T)) +
+                                 cc * 8 + j);
+    const float* lrow = LG ? a.logits + (long long)u * kv.t_max : nullptr;
     const int32_t* rows = SPARSE ? a.idx + (long long)u * a.cap : nullptr;
     if (SPARSE) {
       __syncthreads();  // earlier readers of the buffer are done
@@ -253,39 +260,49 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
       }
       for (int base = sb; base < se; base += STEP) {
         long long row[UNROLL];
+        int keyv[UNROLL];
 #pragma unroll
         for (int uu = 0; uu < UNROLL; uu++) {
           const int r = base + uu * 16 + warp * 4 + sg;
           row[uu] = -1;
+          keyv[uu] = 0;
           if (r < se) {
             const int key = SPARSE ? sh_idx[r - sb] : r;
             if ((unsigned)key < (unsigned)t) {
               row[uu] = kv_row(kv, b, kvh, key);
+              keyv[uu] = key;
               if (row[uu] < 0) raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
             } else {
               raise_error(kv.err, PRHS_DEV_BAD_INDEX);
             }
           }
         }
-        uint4 kc[UNROLL][S::CPL], vc[UNROLL][S::CPL];
+        uint4 kc[LG ? 1 : UNROLL][S::CPL], vc[UNROLL][S::CPL];
+        float lg[LG ? UNROLL : 1];
 #pragma unroll
-        for (int uu = 0; uu < UNROLL; uu++)
+        for (int uu = 0; uu < UNROLL; uu++) {
+          if (LG) lg[uu] = row[uu] >= 0 ? __ldg(lrow + keyv[uu]) : 0.f;
 #pragma unroll
           for (int cc = 0; cc < S::CPL; cc++) {
             if (row[uu] >= 0) {
-              kc[uu][cc] = ldg_stream(kbase + row[uu] * S::RB + (cc * 8 + j) * 16);
+              if (!LG) kc[uu][cc] = ldg_stream(kbase + row[uu] * S::RB + (cc * 8 + j) * 16);
               vc[uu][cc] = ldg_stream(vbase + row[uu] * S::RB + (cc * 8 + j) * 16);
             } else {
-              kc[uu][cc] = make_uint4(0, 0, 0, 0);
+              if (!LG) kc[uu][cc] = make_uint4(0, 0, 0, 0);
               vc[uu][cc] = make_uint4(0, 0, 0, 0);
             }
           }
+        }
         float s[UNROLL][G];
 #pragma unroll
         for (int uu = 0; uu < UNROLL; uu++) {
+          if (LG) {
+            s[uu][0] = row[uu] >= 0 ? lg[uu] * LOG2E : -INFINITY;
+            continue;
+          }
           float kf[S::EL];
 #pragma unroll
-          for (int cc = 0; cc < S::CPL; cc++) Elem<T>::unpack(kc[uu][cc], kf + cc * S::EPC);
+          for (int cc = 0; cc < S::CPL; cc++) Elem<T>::unpack(kc[LG ? 0 : uu][cc], kf + cc * S::EPC);
 #pragma unroll
           for (int g = 0; g < G; g++) {
             float acc = 0.f;
@@ -483,11 +500,11 @@ size_t attn_partial_floats(const KVView& kv, bool sparse, int ctas) {
   return ((size_t)ctas + attn_units(kv, sparse)) * (kv.d + 4);
 }
 
-template <typename T, int D, int G, bool SPARSE>
+template <typename T, int D, int G, bool SPARSE, bool LG>
 static cudaError_t attn_go(const AttnLaunch& a, cudaStream_t st) {
   const size_t units = (size_t)attn_units(a.kv, SPARSE);
   const size_t smem = (units + 1) * sizeof(int) * (units <= (size_t)ATTN_ALIGN_UNITS ? 2 : 1);
-  auto k = attn_kernel<T, D, G, SPARSE>;
+  auto k = attn_kernel<T, D, G, SPARSE, LG>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -497,8 +514,9 @@ static cudaError_t attn_go(const AttnLaunch& a, cudaStream_t st) {
 
 template <typename T, int D>
 static cudaError_t attn_dispatch(const AttnLaunch& a, bool sparse, cudaStream_t st) {
-  if (sparse) return attn_go<T, D, 1, true>(a, st);
-  return attn_go<T, D, 1, false>(a, st);
+  if (sparse && a.logits != nullptr) return attn_go<T, D, 1, true, true>(a, st);
+  if (sparse) return attn_go<T, D, 1, true, false>(a, st);
+  return attn_go<T, D, 1, false, false>(a, st);
 }
 
 cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t st) {

@@ -13,7 +13,9 @@
 // and stores it into CTA 0's shared memory through distributed shared
 // memory; after one cluster barrier CTA 0 merges the CL states from its own
 // shared memory and writes out and lse. No workspace and no global-memory
-// round trip take part in the merge.
+// round trip take part in the merge. With a logit source (LG: the logits
+// the scoring kernel left in the workspace, after a fresh selection) a row
+// costs its 4-byte logit and its V row; its K row is not read.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -28,13 +30,13 @@ constexpr int ACL_STAGE = 2048;  // row numbers staged in shared memory at a tim
 constexpr float ACL_LOG2E = 1.4426950408889634f;
 constexpr float ACL_LN2 = 0.6931471805599453f;
 
-template <typename T, int D>
+template <typename T, int D, bool LG>
 __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const AttnLaunch a) {
   constexpr int RB = D * (int)sizeof(T);  // bytes per row
   constexpr int CPL = RB / 16 / 8;        // 16-byte chunks per lane
   constexpr int EPC = 16 / (int)sizeof(T);
   constexpr int EL = CPL * EPC;           // elements per lane
-  constexpr int UP = CPL >= 4 ? 1 : 2;          // rows per 8-lane group per batch
+  constexpr int UP = (CPL >= 4 ? 1 : 2) * (LG ? 2 : 1);  // rows per 8-lane group per batch
   constexpr int STEP = 4 * ACL_WARPS * UP;       // rows per batch per CTA
   static_assert(RB % 128 == 0 && D <= ACL_THREADS, "row of whole 128-byte lines, one thread per output");
   __shared__ int sh_idx[ACL_STAGE];
@@ -60,8 +62,10 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
   uint4 qraw[CPL];
 #pragma unroll
   for (int cc = 0; cc < CPL; cc++)
-    qraw[cc] = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.q) + (long long)u * RB) +
-                     cc * 8 + j);
+    qraw[cc] = LG ? make_uint4(0, 0, 0, 0)
+                  : __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.q) + (long long)u * RB) +
+                          cc * 8 + j);
+  const float* lrow = LG ? a.logits + (long long)u * kv.t_max : nullptr;
   const int32_t* rows = a.idx + (long long)u * a.cap;
   const int mine_cap = a.cap > rank ? (a.cap - rank + CL - 1) / CL : 0;
   const int spec = min(ACL_STAGE, mine_cap);
@@ -103,17 +107,23 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
     // Two batches of UP rows per 8-lane group in flight: the loads of the
     // next batch are issued before the current one is consumed, so a CTA
     // never waits a full memory round trip between batches.
+    constexpr int UK = LG ? 1 : UP;  // K pieces are kept only when the logits are computed here
     long long rowA[UP], rowB[UP];
-    uint4 kA[UP][CPL], vA[UP][CPL], kB[UP][CPL], vB[UP][CPL];
-    auto issue = [&](int base, long long (&row)[UP], uint4 (&kc)[UP][CPL], uint4 (&vc)[UP][CPL]) {
+    uint4 kA[UK][CPL], vA[UP][CPL], kB[UK][CPL], vB[UP][CPL];
+    float lA[UP], lB[UP];
+    auto issue = [&](int base, long long (&row)[UP], uint4 (&kc)[UK][CPL], uint4 (&vc)[UP][CPL],
+                     float (&lg)[UP]) {
+      int keyv[UP];
 #pragma unroll
       for (int uu = 0; uu < UP; uu++) {
         const int r = base + uu * 4 * ACL_WARPS + warp * 4 + sg;
         row[uu] = -1;
+        keyv[uu] = 0;
         if (r < se) {
           const int key = sh_idx[r - sb];
           if ((unsigned)key < (unsigned)t) {
             row[uu] = kv_row(kv, b, kvh, key);
+            keyv[uu] = key;
             if (row[uu] < 0) raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
           } else {
             raise_error(kv.err, PRHS_DEV_BAD_INDEX);
@@ -121,26 +131,32 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
         }
       }
 #pragma unroll
-      for (int uu = 0; uu < UP; uu++)
+      for (int uu = 0; uu < UP; uu++) {
+        lg[uu] = LG && row[uu] >= 0 ? __ldg(lrow + keyv[uu]) : 0.f;
 #pragma unroll
         for (int cc = 0; cc < CPL; cc++) {
           if (row[uu] >= 0) {
-            kc[uu][cc] = ldg_stream(kbase + row[uu] * RB + (cc * 8 + j) * 16);
+            if (!LG) kc[LG ? 0 : uu][cc] = ldg_stream(kbase + row[uu] * RB + (cc * 8 + j) * 16);
             vc[uu][cc] = ldg_stream(vbase + row[uu] * RB + (cc * 8 + j) * 16);
           } else {
-            kc[uu][cc] = make_uint4(0, 0, 0, 0);
+            if (!LG) kc[LG ? 0 : uu][cc] = make_uint4(0, 0, 0, 0);
             vc[uu][cc] = make_uint4(0, 0, 0, 0);
           }
         }
+      }
     };
-    auto consume = [&](const long long (&row)[UP], const uint4 (&kc)[UP][CPL],
-                       const uint4 (&vc)[UP][CPL]) {
+    auto consume = [&](const long long (&row)[UP], const uint4 (&kc)[UK][CPL],
+                       const uint4 (&vc)[UP][CPL], const float (&lg)[UP]) {
       float s[UP];
 #pragma unroll
       for (int uu = 0; uu < UP; uu++) {
+        if (LG) {
+          s[uu] = row[uu] >= 0 ? lg[uu] * ACL_LOG2E : -INFINITY;
+          continue;
+        }
         float kf[EL];
 #pragma unroll
-        for (int cc = 0; cc < CPL; cc++) Elem<T>::unpack(kc[uu][cc], kf + cc * EPC);
+        for (int cc = 0; cc < CPL; cc++) Elem<T>::unpack(kc[LG ? 0 : uu][cc], kf + cc * EPC);
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < EL; e++) acc = fmaf(qf[e], kf[e], acc);
@@ -169,14 +185,14 @@ __global__ void __launch_bounds__(ACL_THREADS, 2) attn_cluster_kernel(const Attn
       }
       m = mx;
     };
-    issue(sb, rowA, kA, vA);
+    issue(sb, rowA, kA, vA, lA);
     for (int base = sb; base < se; base += 2 * STEP) {  // uniform over the CTA
       const bool more = base + STEP < se;
-      if (more) issue(base + STEP, rowB, kB, vB);
-      consume(rowA, kA, vA);
+      if (more) issue(base + STEP, rowB, kB, vB, lB);
+      consume(rowA, kA, vA, lA);
       if (!more) break;
-      if (base + 2 * STEP < se) issue(base + 2 * STEP, rowA, kA, vA);
-      consume(rowB, kB, vB);
+      if (base + 2 * STEP < se) issue(base + 2 * STEP, rowA, kA, vA, lA);
+      consume(rowB, kB, vB, lB);
     }
   }
 
@@ -271,7 +287,8 @@ static cudaError_t cluster_go(const AttnLaunch& a, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = a.cluster == 1 ? attr + 1 : attr;
   cfg.numAttrs = a.cluster == 1 ? 1 : 2;
-  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<T, D>, a);
+  if (a.logits != nullptr) return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<T, D, true>, a);
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<T, D, false>, a);
 }
 
 cudaError_t launch_attn_cluster(const AttnLaunch& a, cudaStream_t st) {

@@ -112,6 +112,10 @@ struct AttnLaunch {
   int ctas;              // CTAs sharing the rows of all units
   int min_rows;          // fewest rows a CTA takes (fewer CTAs join small batches)
   int cluster = 0;       // sparse only: > 0 runs the cluster kernel with this many CTAs per head
+  // sparse only, nullable: the logits scale * <q, k_i> of every query head
+  // ([B][Hq][t_max], as the scoring kernel leaves them); the attention then
+  // takes each selected row's weight from there and reads only its V row
+  const float* logits = nullptr;
 };
 
 // Dropped mass of given sets over the logits in `scores` ([B][Hq][t_max]).

@@ -343,6 +343,47 @@ def test_score_select_long_cache(t, N):
         assert abs(delta.cpu().numpy()[0, h] - P.dropped_mass(s, P.top_n(s, N))) <= DELTA_TOL
 
 
+@pytest.mark.parametrize("t,N,Hq,Hkv,paged", [(70001, 1500, 2, 1, False), (131072, 4096, 8, 2, False),
+                                               (200003, 777, 2, 1, False), (40000, 2500, 4, 4, True)])
+def test_retrieve_long_cache(t, N, Hq, Hkv, paged):
+    """prhs_retrieve past the one-launch limit: scoring, selection, then an
+    attention launch that weights the selected V rows by the logits the
+    scoring left in the workspace. Set (up to near-ties), delta, out and lse
+    of every retrieving head against the oracle; a skipped head untouched."""
+    import sparse_kv_selection_gb300 as S
+    from workloads.torch_io import upload
+    wl = make_workload("long", dtype="bf16", B=1, Hq=Hq, Hkv=Hkv, d=128, t=t, n_clusters=40,
+                       sinks=4, steps=1, N=N, w=1, paged=paged, block_size=16)
+    dev = upload(wl)
+    kv = S.KVCache(dev["k"], dev["v"], dev["seq_lens"], wl.Hq, block_table=dev["block_table"])
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx = torch.full((1, Hq, N), -7, **i32)
+    n_sel = torch.full((1, Hq), -7, **i32)
+    delta = torch.full((1, Hq), -7.0, device="cuda")
+    out = torch.full((1, Hq, 128), -7.0, device="cuda")
+    lse = torch.full((1, Hq), -7.0, device="cuda")
+    skip = torch.zeros(1, Hq, dtype=torch.uint8, device="cuda")
+    skip[0, Hq - 1] = 1
+    ws = S.make_workspace(kv, N)
+    c0 = S.binding.launch_count()
+    S.retrieve(kv, dev["q"][0], wl.scale, N, idx, n_sel, delta, out, lse, ws, head_skip=skip)
+    assert S.binding.launch_count() - c0 == 3   # scoring, selection, attention
+    assert S.last_error() == 0
+    gi, gn, gd, go, gl = [x.cpu().numpy() for x in (idx, n_sel, delta, out, lse)]
+    for h in range(Hq):
+        if h == Hq - 1:
+            assert gn[0, h] == -7 and (go[0, h] == -7.0).all() and gl[0, h] == -7.0
+            continue
+        K, V = kv_rows64(wl, 0, h // wl.G)
+        qv = q64(wl, 0, 0, h)
+        sc = P.scores(qv, K, wl.scale)
+        gset = gi[0, h, :gn[0, h]]
+        check_topn(gset, sc, N)
+        assert abs(gd[0, h] - P.dropped_mass(sc, gset)) <= DELTA_TOL, h
+        ro, rl = P.attention(qv, K, V, gset, wl.scale)
+        assert np.abs(go[0, h] - ro).max() <= OUT_TOL and abs(gl[0, h] - rl) <= LSE_TOL, h
+
+
 # --------------------------------------------------------------------------- #
 # CIS gate and dilation
 # --------------------------------------------------------------------------- #

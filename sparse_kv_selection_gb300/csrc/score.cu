@@ -56,6 +56,23 @@ __device__ __forceinline__ float transpose_reduce8(const float (&v)[8], int j) {
   return keep + __shfl_xor_sync(FULL_MASK, send, 1);
 }
 
+// Tensor-core pieces of the grouped scoring: a 16x16 bf16 tile of K (keys as
+// rows) from shared memory into the A fragment of mma.m16n8k16, and the mma
+// itself (bf16 inputs, fp32 accumulation).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(160) score_kernel(const __grid_constant__ CUtensorMap tmap,
                                                     const ScoreLaunch a) {
@@ -186,6 +203,70 @@ __global__ void __launch_bounds__(160) score_kernel(const __grid_constant__ CUte
   }
 
   // ---------------- consumers: 32 keys per warp per stage ----------------
+  // A bf16 cache read by a group of query heads is a real contraction: the
+  // stage's keys times the group's queries, on the tensor cores (keys as the
+  // M dimension, 16 per tile; the group as N, padded to 8; d as K). fp32
+  // caches and single heads take the CUDA-core form below.
+  constexpr bool MMA = sizeof(T) == 2 && G >= 2;
+  if constexpr (MMA) {
+    constexpr int KS = D / 16;           // k-steps of 16 dimensions
+    constexpr int EPS = 128 / 2;         // bf16 elements per 128-byte segment
+    uint32_t bq[KS][2];                  // B fragments: q[n][k], n = lane / 4
+    const int n_b = lane >> 2, kq = (lane & 3) * 2;
+    int cur_u = -1, qh0 = 0, k1 = 0;
+    for (int it = 0; it < ntiles; it++) {
+      int u, tile0;
+      tile_at(it, u, tile0);
+      if (u != cur_u) {
+        cur_u = u;
+        const int b = u / kv.Hkv, kvh = u % kv.Hkv;
+        qh0 = b * kv.Hq + kvh * G;
+        k1 = seq_len(kv, b);
+        const uint16_t* qb = static_cast<const uint16_t*>(a.q) + (long long)(qh0 + n_b) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ks++) {
+          bq[ks][0] = n_b < G ? *reinterpret_cast<const uint32_t*>(qb + ks * 16 + kq) : 0u;
+          bq[ks][1] = n_b < G ? *reinterpret_cast<const uint32_t*>(qb + ks * 16 + 8 + kq) : 0u;
+        }
+      }
+      const int s = it % S::STAGES;
+      if (!mbar_wait(&full[s], (it / S::STAGES) & 1, kv.err)) break;
+      const uint32_t stage = smem_addr(smem + s * S::STAGE_BYTES);
+      float c[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; mt++) {
+#pragma unroll
+        for (int e = 0; e < 4; e++) c[mt][e] = 0.f;
+        // lane l addresses row (l % 16) of the 16-key tile, dims +8 (l / 16)
+        const int key = warp * 32 + mt * 16 + (lane & 15);
+#pragma unroll
+        for (int ks = 0; ks < KS; ks++) {
+          const int kd = ks * 16 + (lane >> 4) * 8;
+          const int line = key * S::NH + kd / EPS;           // 128-byte line of the stage
+          const int ch = (kd % EPS) / 8;                     // its 16-byte chunk, swizzled
+          uint32_t af[4];
+          ldsm_x4(stage + line * 128 + ((ch ^ (line & 7)) << 4), af);
+          mma_16816_bf16(c[mt], af, bq[ks][0], bq[ks][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      // c[mt][0..1]: key (lane / 4), heads 2 (lane % 4) + {0, 1}; c[mt][2..3]: key + 8
+      const int n0 = (lane & 3) * 2;
+#pragma unroll
+      for (int mt = 0; mt < 2; mt++) {
+        const int key = tile0 + warp * 32 + mt * 16 + (lane >> 2);
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          const int kk = key + 8 * h;
+          if (kk >= k1) continue;
+          if (n0 < G) a.scores[(long long)(qh0 + n0) * kv.t_max + kk] = c[mt][2 * h] * a.scale;
+          if (n0 + 1 < G) a.scores[(long long)(qh0 + n0 + 1) * kv.t_max + kk] = c[mt][2 * h + 1] * a.scale;
+        }
+      }
+    }
+    return;
+  }
   const int r = lane >> 3;  // key slot 0..3 (8 keys each)
   const int j = lane & 7;   // 16-byte chunk within each 128-byte segment
   float qf[G][S::EL];

@@ -456,8 +456,11 @@ def run_ours(args):
     o_tmp = torch.zeros(B, Hq, d, device="cuda")
     l_tmp = torch.zeros(B, Hq, device="cuda")
     c0 = S.binding.launch_count()
-    S.retrieve(kvs[0], q[0], scale, N, torch.zeros(B, Hq, acap, **i32), torch.zeros(B, Hq, **i32),
-               torch.zeros(B, Hq, device="cuda"), o_tmp, l_tmp, ws, n_budget=nb, head_skip=reuse[0])
+    # on the same stream as everything else that uses this workspace
+    with torch.cuda.stream(stream):
+        S.retrieve(kvs[0], q[0], scale, N, torch.zeros(B, Hq, acap, **i32), torch.zeros(B, Hq, **i32),
+                   torch.zeros(B, Hq, device="cuda"), o_tmp, l_tmp, ws, n_budget=nb, head_skip=reuse[0])
+    torch.cuda.synchronize()
     fused = S.binding.launch_count() - c0 == 1   # scoring, selection and attention in one kernel
     names = (["cis", "retrieve", "sparse_attn"] if fused else
              ["cis", "score", "select", "retrieve_attn", "sparse_attn"])

@@ -182,6 +182,7 @@ KVView view_of(const prhs_kv& kv, unsigned* err) {
   v.max_blocks = kv.block_table ? kv.max_blocks : 0;
   v.num_blocks = kv.block_table ? kv.num_blocks : 0;
   v.err = err;
+  v.pdl = v.t_max <= PDL_MAX_KEYS;
   return v;
 }
 

@@ -509,7 +509,7 @@ static cudaError_t attn_go(const AttnLaunch& a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(k, dim3(a.ctas), dim3(ATTN_THREADS), smem, st, a);
+  return launch_pdl(k, dim3(a.ctas), dim3(ATTN_THREADS), smem, st, a.kv.pdl, a);
 }
 
 template <typename T, int D>

@@ -286,7 +286,7 @@ static cudaError_t cluster_go(const AttnLaunch& a, cudaStream_t st) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = a.cluster == 1 ? attr + 1 : attr;
-  cfg.numAttrs = a.cluster == 1 ? 1 : 2;
+  cfg.numAttrs = (a.cluster == 1 ? 0 : 1) + (a.kv.pdl ? 1 : 0);
   if (a.logits != nullptr) return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<T, D, true>, a);
   return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<T, D, false>, a);
 }

@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
 
 cudaError_t launch_cis(const CisLaunch& a, cudaStream_t st) {
   void (*k)(const CisLaunch) = a.kv.dtype == PRHS_BF16 ? cis_kernel<__nv_bfloat16> : cis_kernel<float>;
-  return launch_pdl(k, dim3(a.kv.B * a.kv.Hq), dim3(CIS_THREADS), 0, st, a);
+  return launch_pdl(k, dim3(a.kv.B * a.kv.Hq), dim3(CIS_THREADS), 0, st, a.kv.pdl, a);
 }
 
 }  // namespace prhs

@@ -439,7 +439,7 @@ static cudaError_t dense_go(const DenseLaunch& a, const CUtensorMap* km, const C
   const size_t smem = S::SMEM + ((size_t)a.kv.B * a.kv.Hkv + 1) * sizeof(int);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(a.ctas), dim3(32 * (S::NW * DenseGroups<G>::NGR + 1)), smem, st, *km, *vm, a);
+  return launch_pdl(k, dim3(a.ctas), dim3(32 * (S::NW * DenseGroups<G>::NGR + 1)), smem, st, a.kv.pdl, *km, *vm, a);
 }
 
 template <typename T, int D>

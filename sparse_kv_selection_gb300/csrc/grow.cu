@@ -99,13 +99,13 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendLaun
 }
 
 cudaError_t launch_compose(const ComposeLaunch& a, cudaStream_t st) {
-  return launch_pdl(compose_kernel, dim3(a.kv.B * a.kv.Hq), dim3(GROW_THREADS), 0, st, a);
+  return launch_pdl(compose_kernel, dim3(a.kv.B * a.kv.Hq), dim3(GROW_THREADS), 0, st, a.kv.pdl, a);
 }
 
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t st) {
   if (a.kv.dtype == PRHS_BF16)
-    return launch_pdl(append_kernel<__nv_bfloat16>, dim3(a.kv.B), dim3(APPEND_THREADS), 0, st, a);
-  return launch_pdl(append_kernel<float>, dim3(a.kv.B), dim3(APPEND_THREADS), 0, st, a);
+    return launch_pdl(append_kernel<__nv_bfloat16>, dim3(a.kv.B), dim3(APPEND_THREADS), 0, st, a.kv.pdl, a);
+  return launch_pdl(append_kernel<float>, dim3(a.kv.B), dim3(APPEND_THREADS), 0, st, a.kv.pdl, a);
 }
 
 }  // namespace prhs

@@ -110,7 +110,7 @@ cudaError_t launch_mass(const MassLaunch& a, cudaStream_t st) {
   MassLaunch m = a;
   m.chunk = (a.kv.t_max + P - 1) / P;
   if (P > 1 && (a.partials == nullptr || a.counters == nullptr)) return cudaErrorInvalidValue;
-  return launch_pdl(mass_kernel, dim3(a.kv.B * a.kv.Hq, P), dim3(MASS_THREADS), 0, st, m);
+  return launch_pdl(mass_kernel, dim3(a.kv.B * a.kv.Hq, P), dim3(MASS_THREADS), 0, st, a.kv.pdl, m);
 }
 
 }  // namespace prhs

@@ -340,7 +340,7 @@ static cudaError_t score_dispatch_g(const ScoreLaunch& a, const CUtensorMap* tma
   const size_t smem = S::SMEM + ((size_t)a.kv.B * a.kv.Hkv + 1) * sizeof(int);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(a.ctas), dim3(32 * (S::NW + 1)), smem, st, *tmap, a);
+  return launch_pdl(k, dim3(a.ctas), dim3(32 * (S::NW + 1)), smem, st, a.kv.pdl, *tmap, a);
 }
 
 size_t score_smem_bytes(prhs_dtype dt, int d) {
@@ -625,7 +625,7 @@ cudaError_t launch_select_global(const SelectLaunch& a, cudaStream_t st) {
                                                           : select_kernel<float>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(a.kv.B * a.kv.Hq), dim3(SELECT_THREADS), smem, st, a);
+  return launch_pdl(k, dim3(a.kv.B * a.kv.Hq), dim3(SELECT_THREADS), smem, st, a.kv.pdl, a);
 }
 
 }  // namespace prhs

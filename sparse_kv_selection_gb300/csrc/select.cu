@@ -874,7 +874,7 @@ static cudaError_t launch_clustered(void (*k)(const SelectLaunch, int), const Se
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = cl == 1 ? attr + 1 : attr;  // no cluster attribute for a single CTA
-  cfg.numAttrs = cl == 1 ? 1 : 2;
+  cfg.numAttrs = (cl == 1 ? 0 : 1) + (a.kv.pdl ? 1 : 0);
   return cudaLaunchKernelEx(&cfg, k, a, chunk);
 }
 

@@ -20,9 +20,9 @@ the previous query, an anchor query that never moves), and a hand GQA case
 fixes which KV head each query head reads (h // G).
 """
 from .prhs import (scores, softmax, logsumexp, top_n, dropped_mass, cosine, cis_gate,
-                   dilate, attention, dense_attention, decode_head, decode_workload,
-                   HeadStep, widen)
+                   dilate, dilate_budget, shared_set, attention, dense_attention, decode_head,
+                   decode_workload, decode_head_grow, HeadStep, widen)
 
 __all__ = ["scores", "softmax", "logsumexp", "top_n", "dropped_mass", "cosine", "cis_gate",
-           "dilate", "attention", "dense_attention", "decode_head", "decode_workload",
-           "HeadStep", "widen"]
+           "dilate", "dilate_budget", "shared_set", "attention", "dense_attention", "decode_head",
+           "decode_workload", "decode_head_grow", "HeadStep", "widen"]

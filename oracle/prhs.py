@@ -119,6 +119,30 @@ def dilate(S: np.ndarray, w: int, t: int) -> np.ndarray:
     return np.nonzero(mask)[0].astype(np.int64)
 
 
+def dilate_budget(S: np.ndarray, w: int, t: int, m: int) -> np.ndarray:
+    """Budgeted dilation: S and at most m of its +/- w neighbours.
+
+    Fig. 9a varies the "dilation strength" m = floor(k / n_den) (a smaller
+    n_den dilates more). Reading: k is the size of the shared set S and m
+    the number of positions dilation may add to it; the candidates are the
+    positions of dilate(S, w, t) not in S, taken nearest to S first and, at
+    equal distance, lowest position first. m >= all candidates gives
+    dilate(S, w, t); m = 0 gives S itself (direct reuse). Result ascending.
+    """
+    S = np.asarray(S, np.int64)
+    full = dilate(S, w, t)
+    inS = np.zeros(t, bool)
+    inS[S] = True
+    cand = [p for p in full.tolist() if not inS[p]]
+    if S.size:
+        dist = {p: int(np.min(np.abs(S - p))) for p in cand}
+    else:
+        dist = {}
+    cand.sort(key=lambda p: (dist[p], p))
+    keep = cand[:max(0, m)]
+    return np.sort(np.concatenate([S, np.asarray(keep, np.int64)])).astype(np.int64)
+
+
 # --------------------------------------------------------------------------- #
 # attention over a selected set (abstract; Table V caption, sparse kernel)
 # --------------------------------------------------------------------------- #
@@ -160,9 +184,18 @@ class HeadStep:
     scores: np.ndarray | None = None
 
 
+def shared_set(anchor_S: np.ndarray, w: int, t: int, n_den: int) -> np.ndarray:
+    """The set a reusing query attends: the anchor's set dilated by +/- w
+    (Fig. 4, Table VIII), or with n_den > 0 the budgeted dilation of Fig. 9a
+    with m = floor(|anchor set| / n_den) added positions."""
+    if n_den > 0:
+        return dilate_budget(anchor_S, w, t, len(anchor_S) // n_den)
+    return dilate(anchor_S, w, t)
+
+
 def decode_head(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, N: int, w: int,
                 tau: float, scale: float, keep_scores: bool = False,
-                max_run: int = 0) -> list[HeadStep]:
+                max_run: int = 0, n_den: int = 0) -> list[HeadStep]:
     """One head through a sequence of decode queries with CIS reuse.
 
     Reading of Fig. 4 ("critical tokens from query 405 are shared to queries
@@ -177,6 +210,8 @@ def decode_head(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, N: int, w: in
     s - 1 reuses the next query retrieves whatever its similarity. 0 = no
     bound. Parity unpinned beyond its two limits (s = 1 always retrieves;
     s = 2 with every gate open alternates), which the tests check.
+
+    n_den > 0 bounds the dilation (shared_set, Fig. 9a).
     """
     K = np.asarray(K, np.float64)
     V = np.asarray(V, np.float64)
@@ -193,7 +228,7 @@ def decode_head(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, N: int, w: in
         s = scores(q, K, scale)
         delta = s_nth = None
         if reuse:
-            S = dilate(anchor_S, w, t)
+            S = shared_set(anchor_S, w, t, n_den)
         else:
             S = top_n(s, N)
             delta = dropped_mass(s, S)
@@ -207,7 +242,7 @@ def decode_head(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, N: int, w: in
     return rec
 
 
-def decode_workload(wl, heads=None, steps=None, keep_scores=False, max_run=0):
+def decode_workload(wl, heads=None, steps=None, keep_scores=False, max_run=0, n_den=0):
     """Run decode_head over (b, query head) pairs of a ``workloads.Workload``.
 
     Query head hq reads KV head hq // (Hq / Hkv) (consecutive grouping, the
@@ -226,7 +261,7 @@ def decode_workload(wl, heads=None, steps=None, keep_scores=False, max_run=0):
         K, V = cache[(b, kvh)]
         qs = widen(wl.q[:nsteps, b, hq], wl.dtype)
         res[(b, hq)] = decode_head(qs, K, V, int(wl.budget[b]), wl.w, wl.tau, wl.scale,
-                                   keep_scores=keep_scores, max_run=max_run)
+                                   keep_scores=keep_scores, max_run=max_run, n_den=n_den)
     return res
 
 
@@ -257,7 +292,8 @@ def top_n_between(s: np.ndarray, N: int, n_sink: int, window: int) -> np.ndarray
 
 def decode_head_grow(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, t0: int, N: int, w: int,
                      tau: float, scale: float, n_sink: int, window: int,
-                     keep_scores: bool = False, max_run: int = 0) -> list[HeadStep]:
+                     keep_scores: bool = False, max_run: int = 0, n_den: int = 0,
+                     gate: str = "query") -> list[HeadStep]:
     """decode_head on a cache that gains one key per query, with a forced set.
 
     Query s sees the first t_s = t0 + s + 1 rows of K and V (the current
@@ -267,7 +303,14 @@ def decode_head_grow(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, t0: int,
     the anchor's set dilated by +/- w and clipped to [0, t_s). delta is the
     dropped mass of the attended set on retrieving queries. With n_sink =
     window = 0 and a fixed cache this is decode_head.
+
+    gate = "key" is the "Key" similarity design of Table IX: the gate
+    compares the current token's key (row t_s - 1, appended at this step)
+    with the key the anchor query's token appended, instead of the two
+    queries. n_den > 0 bounds the dilation as in decode_head.
     """
+    if gate not in ("query", "key"):
+        raise ValueError(gate)
     K = np.asarray(K, np.float64)
     V = np.asarray(V, np.float64)
     anchor_S = anchor_q = None
@@ -276,7 +319,8 @@ def decode_head_grow(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, t0: int,
     for step, q in enumerate(np.asarray(q_steps, np.float64)):
         t = t0 + step + 1
         Kt, Vt = K[:t], V[:t]
-        c, reuse = (None, False) if anchor_S is None else cis_gate(q, anchor_q, tau)
+        g = q if gate == "query" else K[t - 1]   # the vector this step is gated on
+        c, reuse = (None, False) if anchor_S is None else cis_gate(g, anchor_q, tau)
         if max_run > 0 and age >= max_run - 1:
             reuse = False
         age = age + 1 if reuse else 0
@@ -284,12 +328,12 @@ def decode_head_grow(q_steps: np.ndarray, K: np.ndarray, V: np.ndarray, t0: int,
         F = forced_set(t, n_sink, window)
         delta = s_nth = None
         if reuse:
-            S = np.union1d(F, dilate(anchor_S, w, t)).astype(np.int64)
+            S = np.union1d(F, shared_set(anchor_S, w, t, n_den)).astype(np.int64)
         else:
             T = top_n_between(s, N, n_sink, window)
             S = np.union1d(F, T).astype(np.int64)
             delta = dropped_mass(s, S)
-            anchor_S, anchor_q = T, q
+            anchor_S, anchor_q = T, g
         out, lse = attention(q, Kt, Vt, S, scale)
         rec.append(HeadStep(reuse=reuse, cos=c, S=S, anchor_S=anchor_S, delta=delta,
                             delta_used=dropped_mass(s, S), s_nth=s_nth, out=out, lse=lse,

@@ -293,6 +293,86 @@ def check_head_map_hand():
     assert outs == [10.0] * 4 + [23.0] * 4, outs
 
 
+def check_dilate_budget_hand():
+    g = _read_golden("budget_dilation_hand.txt")
+    ints = lambda k: [int(x) for x in g[k]]
+    for case, ms in (("a", (0, 1, 3, 4, 5, 8)), ("b", (3,)), ("c", (2,))):
+        S = np.array(ints(f"{case}_S"), np.int64)
+        w, t = int(g[f"{case}_w"][0]), int(g[f"{case}_t"][0])
+        for m in ms:
+            assert P.dilate_budget(S, w, t, m).tolist() == ints(f"{case}_m{m}"), (case, m)
+    # more than every candidate: the full +-w dilation
+    S = np.array(ints("a_S"), np.int64)
+    assert P.dilate_budget(S, 2, 30, 10 ** 6).tolist() == P.dilate(S, 2, 30).tolist()
+
+
+def check_dilate_budget_bruteforce(rng):
+    """Invariants against a distance computed by brute force: S kept, only
+    +-w neighbours added, min(m, candidates) of them, each added position
+    nearer (lower at equal distance) than every candidate left out, and the
+    sets nested in m."""
+    for trial in range(80):
+        t = int(rng.integers(1, 60))
+        n = int(rng.integers(0, min(t, 12) + 1))
+        w = int(rng.integers(0, 5))
+        S = np.sort(rng.choice(t, size=n, replace=False))
+        full = set(P.dilate(S, w, t).tolist())
+        cand = sorted(full - set(S.tolist()))
+        prev = set(S.tolist())
+        for m in range(0, len(cand) + 2):
+            out = P.dilate_budget(S, w, t, m).tolist()
+            assert out == sorted(set(out)) and set(S.tolist()) <= set(out) <= full
+            added = set(out) - set(S.tolist())
+            assert len(added) == min(m, len(cand))
+            key = lambda p: (min(abs(p - a) for a in S.tolist()), p)
+            left = set(cand) - added
+            if added and left:
+                assert max(key(p) for p in added) < min(key(p) for p in left)
+            assert prev <= set(out)
+            prev = set(out)
+
+
+def check_decode_budget(rng):
+    """A reusing query attends the anchor set with floor(|anchor| / n_den)
+    dilated positions (every gate open, so every later query reuses)."""
+    t, d, N, w = 150, 16, 12, 2
+    K = rng.normal(size=(t, d))
+    V = rng.normal(size=(t, d))
+    qs = rng.normal(size=(4, d))
+    sc = 1 / math.sqrt(d)
+    for n_den in (1, 3, 5, 100):
+        rec = P.decode_head(qs, K, V, N, w, -1.5, sc, n_den=n_den)
+        S0 = rec[0].S
+        assert len(S0) == N
+        for r in rec[1:]:
+            assert r.reuse
+            assert len(r.S) == N + min(N // n_den, len(P.dilate(S0, w, t)) - N)
+            assert set(S0.tolist()) <= set(r.S.tolist()) <= set(P.dilate(S0, w, t).tolist())
+    full = P.decode_head(qs, K, V, N, w, -1.5, sc)
+    assert all(a.S.tolist() == b.S.tolist() for a, b in zip(full, P.decode_head(qs, K, V, N, w, -1.5, sc, n_den=0)))
+
+
+def check_key_gate_hand():
+    """The "Key" similarity design (Table IX) on a growing cache: the gate
+    compares the key each query appends with the anchor's appended key.
+    d = 2, t0 = 4 visible keys, four queries. Every query is e1 (gating on
+    queries would reuse at every step after the first); the appended keys
+    point at 0, 30, 90 and 110 degrees: cos(30, 0) = 0.866 -> reuse;
+    cos(90, 0) = 0 -> retrieve, the anchor becomes query 2 (key at 90);
+    cos(110, 90) = 0.94 -> reuse. Flags: retrieve, reuse, retrieve, reuse."""
+    t0 = 4
+    ang = np.radians([0.0, 30.0, 90.0, 110.0])
+    K = np.zeros((t0 + 4, 2))
+    K[:t0] = [[1.0, 0.0], [0.0, 1.0], [-1.0, 0.0], [0.0, -1.0]]
+    K[t0:] = np.stack([np.cos(ang), np.sin(ang)], axis=1)
+    V = np.arange(2 * (t0 + 4), dtype=np.float64).reshape(t0 + 4, 2)
+    qs = np.tile([1.0, 0.0], (4, 1))
+    rec = P.decode_head_grow(qs, K, V, t0, 2, 1, 0.8, 1.0, 0, 0, gate="key")
+    assert [r.reuse for r in rec] == [False, True, False, True]
+    byq = P.decode_head_grow(qs, K, V, t0, 2, 1, 0.8, 1.0, 0, 0, gate="query")
+    assert [r.reuse for r in byq] == [False, True, True, True]
+
+
 def check_widen():
     bits = np.array([0x3F80, 0xC020, 0x0000, 0x8000, 0x7F7F], np.uint16)
     v = P.widen(bits, "bf16")
@@ -629,3 +709,59 @@ def test_mutation_head_map_modulo(monkeypatch):
         return res
     monkeypatch.setattr(P, "decode_workload", bad)
     assert _caught(check_head_map_hand)
+
+
+def test_dilate_budget_hand():
+    check_dilate_budget_hand()
+
+
+def test_dilate_budget_bruteforce(rng):
+    check_dilate_budget_bruteforce(rng)
+
+
+def test_decode_budget(rng):
+    check_decode_budget(rng)
+
+
+def test_key_gate_hand():
+    check_key_gate_hand()
+
+
+def test_mutation_budget_farthest_first(monkeypatch):
+    """Adding the farthest neighbours first must fail the hand cases."""
+    def bad(S, w, t, m):
+        S = np.asarray(S, np.int64)
+        cand = sorted(set(P.dilate(S, w, t).tolist()) - set(S.tolist()),
+                      key=lambda p: (-min(abs(p - a) for a in S.tolist()), p))
+        return np.sort(np.concatenate([S, np.asarray(cand[:max(0, m)], np.int64)]))
+    monkeypatch.setattr(P, "dilate_budget", bad)
+    assert _caught(check_dilate_budget_hand)
+
+
+def test_mutation_budget_highest_position_first(monkeypatch):
+    def bad(S, w, t, m):
+        S = np.asarray(S, np.int64)
+        cand = sorted(set(P.dilate(S, w, t).tolist()) - set(S.tolist()),
+                      key=lambda p: (min(abs(p - a) for a in S.tolist()), -p))
+        return np.sort(np.concatenate([S, np.asarray(cand[:max(0, m)], np.int64)]))
+    monkeypatch.setattr(P, "dilate_budget", bad)
+    assert _caught(check_dilate_budget_hand)
+
+
+def test_mutation_key_gate_uses_query(monkeypatch):
+    """Gating on the queries while asked for keys must fail the hand case."""
+    good = P.decode_head_grow
+
+    def bad(*args, gate="query", **kw):
+        return good(*args, gate="query", **kw)
+    monkeypatch.setattr(P, "decode_head_grow", bad)
+    assert _caught(check_key_gate_hand)
+
+
+def test_mutation_budget_from_budget_not_anchor(monkeypatch, rng):
+    """m taken from a fixed 2 N instead of the anchor's size must fail."""
+    good = P.shared_set
+    monkeypatch.setattr(P, "shared_set",
+                        lambda a, w, t, n_den: good(a, w, t, n_den) if n_den <= 0 else
+                        P.dilate_budget(a, w, t, 2 * len(a) // n_den))
+    assert _caught(check_decode_budget, rng)

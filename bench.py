@@ -58,6 +58,12 @@ def parse_args():
                         "and attends the forced sinks and window too (not the bench line)")
     p.add_argument("--n-sink", type=int, default=4)
     p.add_argument("--window", type=int, default=64)
+    p.add_argument("--gate", choices=["query", "key"], default="query",
+                   help="with --grow: the reuse gate compares the queries, or the keys each query "
+                        "appends (the Key similarity design)")
+    p.add_argument("--n-den", type=int, default=0,
+                   help="with --grow: budgeted dilation, floor(anchor size / n_den) neighbours added "
+                        "(0: all of the +-w neighbours)")
     p.add_argument("--kernels", action="store_true",
                    help="time each kernel alone on the workload (all heads retrieving) instead")
     p.add_argument("--only", default=None,
@@ -660,9 +666,22 @@ def run_grow(args):
     from workloads.torch_io import tensor_of, upload
 
     wl = preset(args.config, seed=rank)
-    dev = upload(wl)
     Sq, B, Hq, Hkv, d = wl.steps, wl.B, wl.Hq, wl.Hkv, wl.d
     t0 = (wl.seq_lens.astype(np.int64) - Sq).astype(np.int32)
+    if args.gate == "key":
+        # the generator's keys are independent from position to position; for
+        # the key gate the appended keys follow each KV head's first query
+        # head's query sequence (correlated from step to step)
+        for b in range(B):
+            for h in range(Hkv):
+                for s in range(Sq):
+                    i = int(t0[b]) + s
+                    row = wl.q[s, b, h * wl.G]
+                    if wl.paged:
+                        wl.K[wl.block_table[b, i // wl.block_size], h, i % wl.block_size] = row
+                    else:
+                        wl.K[b, h, i] = row
+    dev = upload(wl)
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     R = max(1, math.ceil(2 * l2 / wl.kv_bytes()))
     t0_dev = torch.from_numpy(t0).cuda()
@@ -675,6 +694,9 @@ def run_grow(args):
                                                         for h in range(Hkv)]) for b in range(B)])
                                    for s in range(Sq)])
     new_k, new_v = tensor_of(rows("K"), wl.dtype, "cuda"), tensor_of(rows("V"), wl.dtype, "cuda")
+    # gate vectors per step: each query head's KV head's appended key
+    gates = (new_k[:, :, torch.arange(Hq, device="cuda") // wl.G].contiguous()
+             if args.gate == "key" else None)
     varied = len(set(wl.budget.tolist())) > 1
     N = 0 if varied else int(wl.budget[0])
     nb = dev["budget"] if varied else None
@@ -701,7 +723,8 @@ def run_grow(args):
                 S.binding.append_kv(kvr, new_k[s], new_v[s])
             S.decode_step(kvs[s % R], dev["q"][s], wl.scale, N, wl.w, wl.tau, anchor_idx, anchor_n,
                           q_anchor, idx, n_sel, reuse[s], delta, out, lse, ws, n_budget=nb,
-                          n_sink=args.n_sink, window=args.window)
+                          n_sink=args.n_sink, window=args.window, n_den=args.n_den,
+                          gate=None if gates is None else gates[s])
 
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
@@ -746,7 +769,8 @@ def run_grow(args):
                        "step": f"one decode sequence of {Sq} queries x {B * Hq} heads, each query "
                                f"appending one key per sequence first",
                        "grow": {"t_first": int(t0.max()) + 1, "t_last": int(wl.seq_lens.max()),
-                                "n_sink": args.n_sink, "window": args.window},
+                                "n_sink": args.n_sink, "window": args.window, "gate": args.gate,
+                                "n_den": args.n_den},
                        "l2": f"{R} rotating KV copies, every copy appended per query",
                        "fresh_retrieval_fraction": float(1.0 - reuse.float().mean().item())},
             "gpu_launches": launches_per_step * args.steps,

@@ -166,16 +166,24 @@ prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* 
  * reuse ? age + 1 : 0.
  * When reuse: idx = union over anchor entries a of [a - w, a + w] clipped to
  * [0, t_b), ascending without repeats, n_sel its size (<= cap required).
+ * Budgeted dilation (Fig. 9a, dilation strength m = floor(k / n_den)): with
+ * n_den > 0 only m = floor(anchor_n / n_den) of those neighbours are added to
+ * the anchor entries, the nearest to an anchor entry first and, at equal
+ * distance, the lowest position first (n_den = 0: all of them; m = 0: the
+ * anchor set itself).
  * When not: idx and n_sel rows are left untouched. reuse [B][Hq] is always
  * written. anchor_idx rows must be ascending and inside [0, t_b).
+ * q is the vectors the gate compares with q_anchor: the queries, or for the
+ * "Key" similarity design of Table IX the current tokens' keys (one per query
+ * head, [B][Hq][d]).
  * Forced keys (n_sink, window as in prhs_score_select): the dilated set is
  * united with [0, n_sink) and [t_b - window, t_b) (clipped), still ascending
  * without repeats; cap >= min(t_max, anchor_cap * (2w + 1) + n_sink + window). */
 prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx,
                             const int32_t* anchor_n, int anchor_cap, const void* q,
-                            const void* q_anchor, int w, int n_sink, int window, double tau,
-                            int max_run, int32_t* anchor_age, int32_t* idx, int32_t* n_sel,
-                            int cap, uint8_t* reuse, cudaStream_t stream);
+                            const void* q_anchor, int w, int n_den, int n_sink, int window,
+                            double tau, int max_run, int32_t* anchor_age, int32_t* idx,
+                            int32_t* n_sel, int cap, uint8_t* reuse, cudaStream_t stream);
 
 /* Dropped attention mass of given index sets under the current query (a
  * diagnostic for reuse steps, whose set was not selected under this query;
@@ -234,13 +242,19 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
  *   the others: prhs_retrieve(head_skip = reuse, anchor outputs = the anchor
  *   buffers) on `stream`, which then waits for the side stream.
  * Heads that reuse attend the dilated anchor set; the others retrieve a fresh
- * top-N set, attend it and make it (with q) the new anchor. delta is written
- * for retrieving heads only. Start a sequence with anchor_n (and anchor_age)
- * all zero; max_run and anchor_age as in prhs_cis_dilate; n_sink and window
- * (forced keys) as in prhs_score_select and prhs_cis_dilate. */
-prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int N,
-                             const int32_t* n_budget, int n_sink, int window, int w, double tau,
-                             int max_run, int32_t* anchor_age, int32_t* anchor_idx,
+ * top-N set, attend it and make it (with the gated vector) the new anchor.
+ * delta is written for retrieving heads only. Start a sequence with anchor_n
+ * (and anchor_age) all zero; max_run, anchor_age and n_den (budgeted
+ * dilation) as in prhs_cis_dilate; n_sink and window (forced keys) as in
+ * prhs_score_select and prhs_cis_dilate.
+ * gate (nullable, [B][Hq][d], the cache's element type, 16-byte aligned):
+ * the vectors the CIS gate compares, in place of q; the "Key" similarity
+ * design of Table IX passes the key each sequence appended for this token
+ * (its KV head's row for every query head of the group). q_anchor then holds
+ * the gate vector of each head's anchor. */
+prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, const void* gate, float scale, int N,
+                             const int32_t* n_budget, int n_sink, int window, int w, int n_den,
+                             double tau, int max_run, int32_t* anchor_age, int32_t* anchor_idx,
                              int32_t* anchor_n, int anchor_cap, void* q_anchor, int32_t* idx,
                              int32_t* n_sel, int cap, uint8_t* reuse, float* delta, float* out,
                              float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);

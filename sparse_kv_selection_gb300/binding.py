@@ -64,13 +64,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "prhs_retrieve": (I, [KV, P, F, I, P, I, I, P, P, P, I, P, P, P, I, P, P, P, P, Z, P]),
         "prhs_score": (I, [KV, P, F, P, P, Z, P]),
         "prhs_select": (I, [KV, P, I, P, I, I, P, P, P, I, P, P, P, I, P, P, Z, P]),
-        "prhs_cis_dilate": (I, [KV, P, P, I, P, P, I, I, I, D, I, P, P, P, I, P, P]),
+        "prhs_cis_dilate": (I, [KV, P, P, I, P, P, I, I, I, I, D, I, P, P, P, I, P, P]),
         "prhs_sparse_attn": (I, [KV, P, F, P, P, I, P, P, P, Z, P]),
         "prhs_sparse_attn_noalloc": (I, [KV, P, F, P, P, I, P, P, P]),
         "prhs_set_mass": (I, [KV, P, F, P, P, I, P, P, Z, P]),
         "prhs_dense_attn": (I, [KV, P, F, P, P, P, Z, P]),
-        "prhs_decode_step": (I, [KV, P, F, I, P, I, I, I, D, I, P, P, P, I, P, P, P, I, P, P, P, P, P, Z,
-                                 P]),
+        "prhs_decode_step": (I, [KV, P, P, F, I, P, I, I, I, I, D, I, P, P, P, I, P, P, P, I, P, P, P, P,
+                                 P, Z, P]),
         "prhs_append_kv": (I, [KV, P, P, P]),
         "prhs_selftest_wait_timeout": (I, [ctypes.c_uint, P]),
         "prhs_last_error": (I, []),
@@ -224,10 +224,10 @@ def select(kv, q, N, idx, n_sel, delta, ws, *, n_budget=None, head_skip=None, an
 
 
 def cis_dilate(kv, anchor_idx, anchor_n, q, q_anchor, w, tau, idx, n_sel, reuse, *, max_run=0,
-               anchor_age=None, n_sink=0, window=0, stream=None) -> None:
+               anchor_age=None, n_sink=0, window=0, n_den=0, stream=None) -> None:
     _check(load().prhs_cis_dilate(kv.ref(), _ptr(anchor_idx), _ptr(anchor_n), anchor_idx.shape[-1],
-                                  _ptr(q), _ptr(q_anchor), int(w), int(n_sink), int(window),
-                                  float(tau), int(max_run),
+                                  _ptr(q), _ptr(q_anchor), int(w), int(n_den), int(n_sink),
+                                  int(window), float(tau), int(max_run),
                                   _ptr(anchor_age), _ptr(idx), _ptr(n_sel), idx.shape[-1],
                                   _ptr(reuse), _stream(stream)), "cis_dilate")
 
@@ -259,9 +259,9 @@ def dense_attn(kv, q, scale, out, lse, ws, stream=None) -> None:
 
 def decode_step(kv, q, scale, N, w, tau, anchor_idx, anchor_n, q_anchor, idx, n_sel, reuse, delta,
                 out, lse, ws, *, n_budget=None, max_run=0, anchor_age=None, n_sink=0, window=0,
-                stream=None) -> None:
-    _check(load().prhs_decode_step(kv.ref(), _ptr(q), float(scale), int(N), _ptr(n_budget),
-                                   int(n_sink), int(window), int(w),
+                n_den=0, gate=None, stream=None) -> None:
+    _check(load().prhs_decode_step(kv.ref(), _ptr(q), _ptr(gate), float(scale), int(N),
+                                   _ptr(n_budget), int(n_sink), int(window), int(w), int(n_den),
                                    float(tau), int(max_run), _ptr(anchor_age), _ptr(anchor_idx),
                                    _ptr(anchor_n),
                                    anchor_idx.shape[-1], _ptr(q_anchor), _ptr(idx), _ptr(n_sel),

@@ -308,7 +308,8 @@ prhs_status do_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* 
                       const void* q, int N, const int32_t* n_budget, int n_sink, int window,
                       const uint8_t* head_skip,
                       int32_t* idx, int32_t* n_sel, int cap, float* delta, int32_t* anchor_idx,
-                      int32_t* anchor_n, int anchor_cap, void* q_anchor, cudaStream_t st) {
+                      int32_t* anchor_n, int anchor_cap, void* q_anchor, cudaStream_t st,
+                      const void* q_src = nullptr) {
   SelectLaunch se;
   se.kv = view_of(kv, di->err);
   se.scores = reinterpret_cast<float*>(static_cast<char*>(ws) + L.scores);
@@ -324,6 +325,7 @@ prhs_status do_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* 
   se.anchor_cap = anchor_cap;
   se.q = q;
   se.q_anchor = q_anchor;
+  se.q_src = q_src != nullptr ? q_src : q;
   se.n_sink = n_sink;
   se.window = window;
   se.scale = 0.f;
@@ -338,7 +340,7 @@ prhs_status do_score_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, 
                             int n_sink, int window, const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap,
                             float* delta, int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap,
                             void* q_anchor, cudaStream_t st, float* out = nullptr,
-                            float* lse = nullptr) {
+                            float* lse = nullptr, const void* q_src = nullptr) {
   const KVView v = view_of(kv, di->err);
   if (score_select_fits(v)) {  // short caches: logits computed into shared memory, one launch
     SelectLaunch se;
@@ -356,6 +358,7 @@ prhs_status do_score_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, 
     se.anchor_cap = anchor_cap;
     se.q = q;
     se.q_anchor = q_anchor;
+    se.q_src = q_src != nullptr ? q_src : q;
     se.n_sink = n_sink;
     se.window = window;
     se.scale = scale;
@@ -369,7 +372,7 @@ prhs_status do_score_select(const prhs_kv& kv, DeviceInfo* di, const Layout& L, 
   prhs_status s = do_score(kv, di, L, ws, q, scale, head_skip, st);
   if (s != PRHS_OK) return s;
   return do_select(kv, di, L, ws, q, N, n_budget, n_sink, window, head_skip, idx, n_sel, cap, delta,
-                   anchor_idx, anchor_n, anchor_cap, q_anchor, st);
+                   anchor_idx, anchor_n, anchor_cap, q_anchor, st, q_src);
 }
 
 // Host checks shared by the selection entry points.
@@ -426,8 +429,9 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
 
 prhs_status do_cis(const prhs_kv& kv, DeviceInfo* di, const int32_t* anchor_idx,
                    const int32_t* anchor_n, int anchor_cap, const void* q, const void* q_anchor,
-                   int w, int n_sink, int window, double tau, int max_run, int32_t* anchor_age,
-                   int32_t* idx, int32_t* n_sel, int cap, uint8_t* reuse, cudaStream_t st) {
+                   int w, int n_den, int n_sink, int window, double tau, int max_run,
+                   int32_t* anchor_age, int32_t* idx, int32_t* n_sel, int cap, uint8_t* reuse,
+                   cudaStream_t st) {
   CisLaunch c;
   c.kv = view_of(kv, di->err);
   c.anchor_idx = anchor_idx;
@@ -436,6 +440,7 @@ prhs_status do_cis(const prhs_kv& kv, DeviceInfo* di, const int32_t* anchor_idx,
   c.q = q;
   c.q_anchor = q_anchor;
   c.w = w;
+  c.n_den = n_den;
   c.tau = tau;
   c.max_run = max_run;
   c.anchor_age = anchor_age;
@@ -510,12 +515,13 @@ prhs_status do_retrieve(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void
                         float scale, int N, const int32_t* n_budget, int n_sink, int window,
                         const uint8_t* head_skip, int32_t* idx, int32_t* n_sel, int cap, float* delta,
                         int32_t* anchor_idx, int32_t* anchor_n, int anchor_cap, void* q_anchor,
-                        float* out, float* lse, int rows_hint, cudaStream_t st) {
+                        float* out, float* lse, int rows_hint, cudaStream_t st,
+                        const void* q_src = nullptr) {
   const bool forced = n_sink > 0 || window > 0;
   const bool one = !forced && score_select_fits(view_of(kv, di->err));
   prhs_status s = do_score_select(kv, di, L, ws, q, scale, N, n_budget, n_sink, window, head_skip, idx,
                                   n_sel, cap, delta, anchor_idx, anchor_n, anchor_cap, q_anchor, st,
-                                  one ? out : nullptr, one ? lse : nullptr);
+                                  one ? out : nullptr, one ? lse : nullptr, q_src);
   if (s != PRHS_OK || one) return s;
   if (forced && (s = forced_finish(kv, di, L, ws, head_skip, anchor_idx, anchor_n, anchor_cap, idx,
                                    n_sel, cap, delta, n_sink, window, st)) != PRHS_OK)
@@ -689,9 +695,10 @@ prhs_status prhs_select(const prhs_kv* kv, const void* q, int N, const int32_t* 
 }
 
 prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx, const int32_t* anchor_n,
-                            int anchor_cap, const void* q, const void* q_anchor, int w, int n_sink,
-                            int window, double tau, int max_run, int32_t* anchor_age, int32_t* idx,
-                            int32_t* n_sel, int cap, uint8_t* reuse, cudaStream_t stream) {
+                            int anchor_cap, const void* q, const void* q_anchor, int w, int n_den,
+                            int n_sink, int window, double tau, int max_run, int32_t* anchor_age,
+                            int32_t* idx, int32_t* n_sel, int cap, uint8_t* reuse,
+                            cudaStream_t stream) {
   prhs_status s = check_kv(kv);
   if (s != PRHS_OK) return s;
   if ((q && !aligned16(q)) || (q_anchor && !aligned16(q_anchor)))
@@ -699,6 +706,7 @@ prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx, const 
   if (!anchor_idx || !anchor_n || !q || !q_anchor || !idx || !n_sel || !reuse)
     return fail(PRHS_EINVAL, "cis: null pointer argument");
   if (w < 0) return fail(PRHS_EINVAL, "w must be >= 0 (got %d)", w);
+  if (n_den < 0) return fail(PRHS_EINVAL, "n_den must be >= 0 (got %d)", n_den);
   if (max_run < 0) return fail(PRHS_EINVAL, "max_run must be >= 0 (got %d)", max_run);
   if (max_run > 0 && anchor_age == nullptr) return fail(PRHS_EINVAL, "max_run > 0 needs anchor_age");
   if (anchor_cap <= 0 || cap <= 0) return fail(PRHS_EINVAL, "capacities must be positive");
@@ -708,7 +716,7 @@ prhs_status prhs_cis_dilate(const prhs_kv* kv, const int32_t* anchor_idx, const 
     return fail(PRHS_EINVAL, "cap %d < min(t_max, anchor_cap * (2w + 1) + n_sink + window)", cap);
   DeviceInfo* di = nullptr;
   if ((s = device_info(&di)) != PRHS_OK) return s;
-  return do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, n_sink, window, tau,
+  return do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, n_den, n_sink, window, tau,
                 max_run, anchor_age, idx, n_sel, cap, reuse, stream);
 }
 
@@ -752,9 +760,9 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
                        "dense attention");
 }
 
-prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int N,
-                             const int32_t* n_budget, int n_sink, int window, int w, double tau,
-                             int max_run,
+prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, const void* gate, float scale, int N,
+                             const int32_t* n_budget, int n_sink, int window, int w, int n_den,
+                             double tau, int max_run,
                              int32_t* anchor_age, int32_t* anchor_idx,
                              int32_t* anchor_n, int anchor_cap, void* q_anchor, int32_t* idx,
                              int32_t* n_sel, int cap, uint8_t* reuse, float* delta, float* out,
@@ -763,9 +771,11 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if (s != PRHS_OK) return s;
   if (!q || !anchor_idx || !anchor_n || !q_anchor || !idx || !n_sel || !reuse || !delta || !out || !lse)
     return fail(PRHS_EINVAL, "decode: null pointer argument");
-  if (!aligned16(q) || !aligned16(q_anchor)) return fail(PRHS_EINVAL, "q and q_anchor must be 16-byte aligned");
+  if (!aligned16(q) || !aligned16(q_anchor) || !aligned16(gate))
+    return fail(PRHS_EINVAL, "q, gate and q_anchor must be 16-byte aligned");
   if (n_budget == nullptr && N <= 0) return fail(PRHS_EINVAL, "N must be positive (got %d)", N);
   if (w < 0) return fail(PRHS_EINVAL, "w must be >= 0 (got %d)", w);
+  if (n_den < 0) return fail(PRHS_EINVAL, "n_den must be >= 0 (got %d)", n_den);
   if (max_run < 0) return fail(PRHS_EINVAL, "max_run must be >= 0 (got %d)", max_run);
   if (max_run > 0 && anchor_age == nullptr) return fail(PRHS_EINVAL, "max_run > 0 needs anchor_age");
   const int tmax = t_max_of(*kv);
@@ -780,8 +790,10 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
   if ((s = device_info(&di)) != PRHS_OK) return s;
   Layout L;
   if ((s = check_ws(*kv, di->sms, ws, ws_bytes, &L)) != PRHS_OK) return s;
-  if ((s = do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, q, q_anchor, w, n_sink, window, tau,
-                  max_run, anchor_age, idx, n_sel, cap, reuse, stream)) != PRHS_OK)
+  // the gate compares `gate` (or q) with the anchor's copy of it
+  const void* gv = gate != nullptr ? gate : q;
+  if ((s = do_cis(*kv, di, anchor_idx, anchor_n, anchor_cap, gv, q_anchor, w, n_den, n_sink, window,
+                  tau, max_run, anchor_age, idx, n_sel, cap, reuse, stream)) != PRHS_OK)
     return s;
   // Two branches after the gate: heads that reuse their anchor only need the
   // dilated sets and attend on the side stream, while the retrieving heads
@@ -802,7 +814,7 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, float scale, int 
     if ((branch == 0) == retrieve_first) {
       s = do_retrieve(*kv, di, L, ws, q, scale, N, n_budget, n_sink, window, reuse, idx, n_sel, cap,
                       delta, anchor_idx, anchor_n, anchor_cap, q_anchor, out, lse,
-                      anchor_cap + n_sink + window, stream);
+                      anchor_cap + n_sink + window, stream, gv);
     } else {
       s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, br->side, reuse, 1, true, 0,
                   ATTN_SIDE_MIN_ROWS);

@@ -33,6 +33,177 @@ __device__ __forceinline__ double warp_sum_f64(double v) {
 constexpr int CIS_PER = 4;  // anchor entries per thread per chunk
 constexpr float CIS_MARGIN = 1e-4f;
 
+// Block-wide sum (all CIS_THREADS threads call it; `tot` is shared scratch
+// of CIS_THREADS / 32 ints, free again on return).
+__device__ __forceinline__ int block_sum(int v, int* tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  if (lane == 0) tot[warp] = v;
+  __syncthreads();
+  int s = 0;
+#pragma unroll
+  for (int w2 = 0; w2 < CIS_THREADS / 32; w2++) s += tot[w2];
+  __syncthreads();
+  return s;
+}
+
+// Block-wide exclusive scan; *total gets the sum. Same calling rules.
+__device__ __forceinline__ int block_excl_scan(int v, int* tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL_MASK, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tot[warp] = x;
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w2 = 0; w2 < CIS_THREADS / 32; w2++) {
+    before += w2 < warp ? tot[w2] : 0;
+    all += tot[w2];
+  }
+  __syncthreads();
+  *total = all;
+  return before + x - v;
+}
+
+// Budgeted dilation (Fig. 9a: dilation strength m = floor(k / n_den)): the
+// anchor set and at most m of its +-w neighbours, nearest first, the lowest
+// position first at equal distance; forced sinks before and the window after,
+// as in the unbounded rule. Unit j of the anchor row (ascending x_j) owns the
+// neighbours between x_{j-1} and x_j (those of the first anchor below it; the
+// last unit also those above the last anchor). A candidate p of unit j lies
+// at distance min(p - x_{j-1}, x_j - p) (x_j - p for j = 0, p - x_last above
+// the last anchor). Pass 1 finds the distance D at which the budget runs out
+// (C(d), the candidates within d, for d = 1, 2, ...) and how many of the
+// candidates at exactly D fit; pass 2 writes, unit by unit, the gap's chosen
+// candidates, the anchor and (last unit) the chosen candidates above it, with
+// every write position from a block scan.
+__device__ void dilate_budgeted(const CisLaunch& a, const int32_t* anc, int n, int t, int ns,
+                                int32_t* out, int qh, int* tot) {
+  const KVView& kv = a.kv;
+  const int w = a.w, tid = threadIdx.x;
+  // the anchor row must be ascending inside [0, t): otherwise it is flagged
+  // and the head attends its forced keys only
+  {
+    int bad = 0;
+    for (int j = tid; j < n; j += CIS_THREADS) {
+      const int x = anc[j];
+      bad += x < 0 || x >= t || (j > 0 && anc[j - 1] >= x);
+    }
+    if (block_sum(bad, tot) > 0) {
+      if (tid == 0) raise_error(kv.err, PRHS_DEV_BAD_INDEX);
+      n = 0;
+    }
+  }
+  const int m = n / a.n_den;
+  // candidates of unit j within distance d of the anchors
+  auto unit_within = [&](int j, int d) {
+    const int x = anc[j];
+    int c;
+    if (j == 0) {
+      c = min(d, x);
+    } else {
+      const int g = x - anc[j - 1] - 1;
+      c = min(g, 2 * d);
+    }
+    if (j == n - 1) c += min(d, t - 1 - x);
+    return c;
+  };
+  // ---- pass 1: the cut distance D and the candidates taken at exactly D ----
+  int D = 0, take_at_D = 0, below = 0;  // below = C(D - 1)
+  if (m > 0) {
+    for (int d = 1; d <= w; d++) {
+      int loc = 0;
+      for (int j = tid; j < n; j += CIS_THREADS) loc += unit_within(j, d);
+      const int cd = block_sum(loc, tot);
+      D = d;
+      take_at_D = min(m, cd) - below;
+      if (cd >= m) break;
+      below = cd;
+    }
+  }
+  // ---- pass 2: write ----
+  for (int i = tid; i < ns; i += CIS_THREADS) {
+    if (i < a.cap) out[i] = i;
+    else raise_error(kv.err, PRHS_DEV_CAPACITY);
+  }
+  int carry = ns, rank0 = 0;  // entries written so far; candidates at distance D in earlier chunks
+  int last = ns - 1;          // the highest position written
+  __shared__ int sh_last;
+  for (int base = 0; base < n; base += CIS_THREADS) {
+    const int j = base + tid;
+    const bool has = j < n;
+    const int x = has ? anc[j] : 0;
+    const bool first = j == 0;
+    const int xp = has && !first ? anc[j - 1] : 0;
+    // the unit's candidates, ascending: [lo1, hi1] near x_{j-1}, [lo2, x - 1]
+    // near x_j, and for the last unit [x + 1, hi3] above it
+    const int lo1 = xp + 1, hi1 = first ? xp : min(xp + w, x - 1);
+    const int lo2 = max(first ? x - w : max(hi1 + 1, x - w), 0);
+    const int hi3 = has && j == n - 1 ? min(t - 1, x + w) : x;
+    auto dist = [&](int p) { return p > x ? p - x : (first ? x - p : min(p - xp, x - p)); };
+    int atD = 0;
+    if (has && D > 0) {
+      for (int p = lo1; p <= hi1; p++) atD += dist(p) == D;
+      for (int p = lo2; p < x; p++) atD += dist(p) == D;
+      for (int p = x + 1; p <= hi3; p++) atD += dist(p) == D;
+    }
+    int at_total;
+    const int rank_first = rank0 + block_excl_scan(atD, tot, &at_total);
+    // a candidate is kept if nearer than D, or at D within the budget's
+    // remainder (rank counted over all candidates at D, ascending); kept
+    // positions below the sinks' end are already written
+    auto keep = [&](int p, int& rank) {
+      const int dd = dist(p);
+      const bool c = dd < D || (dd == D && rank++ < take_at_D);
+      return c && p >= ns;
+    };
+    int k = 0;
+    if (has) {
+      int rank = rank_first;
+      for (int p = lo1; p <= hi1; p++) k += keep(p, rank);
+      for (int p = lo2; p < x; p++) k += keep(p, rank);
+      k += x >= ns;
+      for (int p = x + 1; p <= hi3; p++) k += keep(p, rank);
+    }
+    int total;
+    int pos = carry + block_excl_scan(k, tot, &total);
+    int top = -1;
+    if (has) {
+      int rank = rank_first;
+      auto emit = [&](int p) {
+        if (pos < a.cap) out[pos] = p;
+        else raise_error(kv.err, PRHS_DEV_CAPACITY);
+        pos++;
+        top = p;
+      };
+      for (int p = lo1; p <= hi1; p++) if (keep(p, rank)) emit(p);
+      for (int p = lo2; p < x; p++) if (keep(p, rank)) emit(p);
+      if (x >= ns) emit(x);
+      for (int p = x + 1; p <= hi3; p++) if (keep(p, rank)) emit(p);
+    }
+    // units write in ascending order: the chunk's last unit holds its highest position
+    if (j == min(n, base + CIS_THREADS) - 1) sh_last = top;
+    __syncthreads();
+    last = max(last, sh_last);
+    __syncthreads();
+    carry += total;
+    rank0 += at_total;
+  }
+  // the window, past both the sinks and the last position written
+  const int wstart = max(max(ns, t - max(a.window, 0)), last + 1);
+  for (int i = tid; i < t - wstart; i += CIS_THREADS) {
+    if (carry + i < a.cap) out[carry + i] = wstart + i;
+    else raise_error(kv.err, PRHS_DEV_CAPACITY);
+  }
+  carry += max(0, t - wstart);
+  if (tid == 0) a.n_sel[qh] = min(carry, a.cap);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   __shared__ int sh_reuse;
@@ -114,6 +285,10 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   const int w = a.w;
   // forced keys: sinks [0, ns) first, the window after the dilated entries
   const int ns = min(max(a.n_sink, 0), t);
+  if (a.n_den > 0) {  // uniform over the block
+    dilate_budgeted(a, anc, n, t, ns, out, qh, warp_tot);
+    return;
+  }
   for (int i = tid; i < ns; i += CIS_THREADS) {
     if (i < a.cap) out[i] = i;
     else raise_error(kv.err, PRHS_DEV_CAPACITY);

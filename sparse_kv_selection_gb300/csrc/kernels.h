@@ -56,6 +56,7 @@ struct SelectLaunch {
   int anchor_cap;
   const void* q;
   void* q_anchor;
+  const void* q_src;  // what the anchor copies into q_anchor: q, or the vectors gated on
   int n_sink;  // forced keys are left out of the ranking (the caller adds them)
   int window;
   // score-and-select kernel only: the logits' scale, and where to leave the
@@ -73,9 +74,10 @@ struct CisLaunch {
   const int32_t* anchor_idx;
   const int32_t* anchor_n;
   int anchor_cap;
-  const void* q;
+  const void* q;          // the vectors gated on (queries, or the current tokens' keys)
   const void* q_anchor;
   int w;
+  int n_den;              // > 0: budgeted dilation, floor(anchor_n / n_den) positions added
   double tau;
   int max_run;           // 0: reuse runs are unbounded
   int32_t* anchor_age;   // [B][Hq] reuses since the anchor retrieved (null when max_run == 0)

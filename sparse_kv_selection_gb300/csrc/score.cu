@@ -398,7 +398,7 @@ template <typename T>
 __device__ __forceinline__ void copy_query(const SelectLaunch& a, int qh) {
   const int d = a.kv.d;
   for (int i = threadIdx.x; i < d; i += blockDim.x)
-    copy_elem<T>(a.q_anchor, a.q, (long long)qh * d + i);
+    copy_elem<T>(a.q_anchor, a.q_src, (long long)qh * d + i);
 }
 
 template <typename T>

@@ -91,7 +91,7 @@ __device__ __forceinline__ unsigned scan_block(unsigned v, unsigned* warp_tot, u
 template <typename T>
 __device__ __forceinline__ void mirror_query(const SelectLaunch& a, int qh) {
   for (int i = threadIdx.x; i < a.kv.d; i += blockDim.x)
-    copy_elem<T>(a.q_anchor, a.q, (long long)qh * a.kv.d + i);
+    copy_elem<T>(a.q_anchor, a.q_src, (long long)qh * a.kv.d + i);
 }
 
 // Bin of a histogram (nb bins, highest first) holding the krem-th largest

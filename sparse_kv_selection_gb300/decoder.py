@@ -21,7 +21,7 @@ from . import binding as _b
 class SparseDecoder:
     def __init__(self, kv: _b.KVCache, *, N: int | None = None, n_budget=None, w: int = 2,
                  tau: float = 0.8, scale: float | None = None, max_run: int = 0, n_sink: int = 0,
-                 window: int = 0, stream=None):
+                 window: int = 0, n_den: int = 0, stream=None):
         dev = kv.k.device
         self.kv, self.w, self.tau = kv, int(w), float(tau)
         self.scale = scale if scale is not None else kv.desc.d ** -0.5
@@ -31,6 +31,7 @@ class SparseDecoder:
         tmax = kv.t_max
         self.anchor_cap = max(1, min(nmax, tmax))
         self.n_sink, self.window = int(n_sink), int(window)
+        self.n_den = int(n_den)  # > 0: budgeted dilation (Fig. 9a)
         self.cap = max(1, min(tmax, self.anchor_cap * (2 * self.w + 1) + self.n_sink + self.window))
         B, Hq, d = kv.B, kv.Hq, kv.desc.d
         qdt = kv.k.dtype
@@ -54,10 +55,13 @@ class SparseDecoder:
         self.anchor_n.zero_()
         self.anchor_age.zero_()
 
-    def step(self, q: torch.Tensor, out=None, lse=None, delta=None, reuse=None, n_sel=None) -> None:
+    def step(self, q: torch.Tensor, out=None, lse=None, delta=None, reuse=None, n_sel=None,
+             gate=None) -> None:
         """One decode query per head (q [B][Hq][d] on the device). Results go
         to the given [B][Hq](...) views, else to the decoder's own buffers.
-        delta is written for retrieving heads only."""
+        delta is written for retrieving heads only. gate ([B][Hq][d], optional):
+        the vectors the reuse gate compares in place of q (the "Key"
+        similarity design: the key each sequence appended, per query head)."""
         _b.decode_step(self.kv, q, self.scale, self.N, self.w, self.tau, self.anchor_idx,
                        self.anchor_n, self.q_anchor, self.idx,
                        self.n_sel if n_sel is None else n_sel,
@@ -67,7 +71,7 @@ class SparseDecoder:
                        self.lse if lse is None else lse,
                        self.ws, n_budget=self.n_budget, max_run=self.max_run,
                        anchor_age=self.anchor_age, n_sink=self.n_sink, window=self.window,
-                       stream=self.stream)
+                       n_den=self.n_den, gate=gate, stream=self.stream)
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor) -> None:
         """Grow the cache by one key per sequence ([B][Hkv][d] device rows,

@@ -49,7 +49,7 @@ def q64(wl, step, b, hq):
     return P.widen(wl.q[step, b, hq], wl.dtype)
 
 
-def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0):
+def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0, n_den=0):
     """Decode on the device query by query and compare sampled heads with
     oracle.decode_head: reuse flags, the attended set, its size, delta, out
     and lse. A retrieving step whose set differs from the oracle's only at
@@ -62,7 +62,7 @@ def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0):
     steps = wl.steps if steps is None else steps
     nb = dev["budget"] if len(set(wl.budget.tolist())) > 1 else None
     dec = S.SparseDecoder(kv, N=int(wl.budget[0]) if nb is None else None, n_budget=nb, w=wl.w,
-                          tau=wl.tau, scale=wl.scale, max_run=max_run)
+                          tau=wl.tau, scale=wl.scale, max_run=max_run, n_den=n_den)
     o, l, dl, r, n = dec.alloc_outputs(steps)
     dl.fill_(float("nan"))
     bi = torch.tensor([b for b, _ in heads], device="cuda")
@@ -72,7 +72,8 @@ def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0):
         dec.step(dev["q"][s], o[s], l[s], dl[s], r[s], n[s])
         gpu_sets.append((dec.idx[bi, hi].cpu().numpy(), n[s][bi, hi].cpu().numpy()))
     o, l, dl, r, n = [x.cpu().numpy() for x in (o, l, dl, r, n)]
-    ref = P.decode_workload(wl, heads=heads, steps=steps, keep_scores=True, max_run=max_run)
+    ref = P.decode_workload(wl, heads=heads, steps=steps, keep_scores=True, max_run=max_run,
+                            n_den=n_den)
     compared = 0
     for k, ((b, h), recs) in enumerate(ref.items()):
         for s, rec in enumerate(recs):
@@ -103,7 +104,7 @@ def compare_decode(wl, dev, kv, heads, steps=None, N=None, max_run=0):
     return compared, r
 
 
-def compare_decode_forced(wl, dev, kv, heads, steps=None, max_run=0):
+def compare_decode_forced(wl, dev, kv, heads, steps=None, max_run=0, n_den=0):
     """Teacher-forced decode: before every query the sampled heads get the
     oracle's anchor state (its undilated set, the anchor query, the reuse
     count), so a near-tie at one query cannot carry over to the next and
@@ -116,8 +117,9 @@ def compare_decode_forced(wl, dev, kv, heads, steps=None, max_run=0):
     steps = wl.steps if steps is None else steps
     nb = dev["budget"] if len(set(wl.budget.tolist())) > 1 else None
     dec = S.SparseDecoder(kv, N=int(wl.budget[0]) if nb is None else None, n_budget=nb, w=wl.w,
-                          tau=wl.tau, scale=wl.scale, max_run=max_run)
-    ref = P.decode_workload(wl, heads=heads, steps=steps, keep_scores=True, max_run=max_run)
+                          tau=wl.tau, scale=wl.scale, max_run=max_run, n_den=n_den)
+    ref = P.decode_workload(wl, heads=heads, steps=steps, keep_scores=True, max_run=max_run,
+                            n_den=n_den)
     o, l, dl, r, n = dec.alloc_outputs(1)
     compared = 0
     for s in range(steps):

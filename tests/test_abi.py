@@ -105,20 +105,21 @@ def test_null_arguments_rejected(lib):
     assert lib.prhs_retrieve(ctypes.byref(kv), 64, 0.1, 8, None, 0, 0, None, 64, 64, 8, 64, None, None,
                              0, None, 64, None, 256, 1 << 20, None) == binding.PRHS_EINVAL
     # dilation radius and dilated capacity
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, -1, 0, 0, 0.8, 0, None, 64, 64, 64,
-                               64, None) == binding.PRHS_EINVAL
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 0, 0.8, 0, None, 64, 64, 39,
-                               64, None) == binding.PRHS_EINVAL
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, -1, 0, 0, 0, 0.8, 0, None, 64, 64, 64, 64, None) == binding.PRHS_EINVAL
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 0, 0, 0.8, 0, None, 64, 64, 39, 64, None) == binding.PRHS_EINVAL
     # the dilated capacity must hold the forced keys too
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 2, 2, 0.8, 0, None, 64, 64, 40,
-                               64, None) == binding.PRHS_EINVAL
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 2, 2, 0.8, 0, None, 64, 64, 40, 64, None) == binding.PRHS_EINVAL
     # a bounded reuse run needs the per-head age counters; a negative bound is invalid
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 0, 0.8, 4, None, 64, 64, 64,
-                               64, None) == binding.PRHS_EINVAL
-    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 0, 0.8, -1, 64, 64, 64, 64,
-                               64, None) == binding.PRHS_EINVAL
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 0, 0, 0.8, 4, None, 64, 64, 64, 64, None) == binding.PRHS_EINVAL
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, 0, 0, 0, 0.8, -1, 64, 64, 64, 64, 64, None) == binding.PRHS_EINVAL
     assert lib.prhs_dense_attn(ctypes.byref(kv), None, 0.1, 64, 64, 256, 1 << 20, None) == binding.PRHS_EINVAL
     assert lib.prhs_workspace_init(None, 0, None) == binding.PRHS_EWORKSPACE
+    # the dilation budget's denominator is non-negative
+    assert lib.prhs_cis_dilate(ctypes.byref(kv), 64, 64, 8, 64, 64, 2, -1, 0, 0, 0.8, 0, None, 64, 64,
+                               64, 64, None) == binding.PRHS_EINVAL
+    # a gate array must be 16-byte aligned like q
+    assert lib.prhs_decode_step(ctypes.byref(kv), 64, 72, 0.1, 8, None, 0, 0, 2, 0, 0.8, 0, None, 64,
+                                64, 8, 64, 64, 64, 64, 64, 64, 64, 64, 256, 1 << 20, None) == binding.PRHS_EINVAL
     # the wait self-test takes a limit of 1 us .. 1 s
     assert lib.prhs_selftest_wait_timeout(0, None) == binding.PRHS_EINVAL
     assert lib.prhs_selftest_wait_timeout(1000001, None) == binding.PRHS_EINVAL

@@ -121,3 +121,75 @@ def test_score_select_forced_keys():
             assert ai[b, h, :ann[b, h]].tolist() == T.tolist(), (b, h)
             assert gi[b, h, :gn[b, h]].tolist() == Sx.tolist(), (b, h)
             assert abs(dd[b, h] - P.dropped_mass(sc, Sx)) <= DELTA_TOL, (b, h)
+
+
+@pytest.mark.parametrize("name,n_sink,window,gate,n_den", [
+    ("gqa4_bf16", 4, 16, "key", 0), ("mha_bf16", 0, 8, "key", 2), ("gqa4_bf16", 3, 0, "query", 3),
+    ("mha_bf16", 4, 16, "key", 1)])
+def test_grow_key_gate_and_budget(name, n_sink, window, gate, n_den):
+    """Growing-cache decode with the "Key" similarity gate of Table IX (the
+    key each sequence appends, per query head, against the anchor's) and
+    with budgeted dilation (Fig. 9a), every (head, query) against the
+    oracle. The appended keys are made correlated from step to step (each
+    KV head's row at position t0 + s is its first query head's query s), so
+    the key gate both reuses and retrieves."""
+    import sparse_kv_selection_gb300 as S
+    from workloads.torch_io import tensor_of, upload
+    wl = make_workload(name, seed=6, **GROW[name])
+    steps, G = wl.steps, wl.G
+    t_full = wl.seq_lens.astype(np.int64)
+    t0 = t_full - steps
+    for b in range(wl.B):
+        for kvh in range(wl.Hkv):
+            for s in range(steps):
+                wl.K[b, kvh, int(t0[b]) + s] = wl.q[s, b, kvh * G]
+    dev = upload(wl)
+    lens = torch.from_numpy(t0.astype(np.int32)).cuda()
+    k, v = dev["k"].clone(), dev["v"].clone()
+    for b in range(wl.B):
+        k[b, :, int(t0[b]):] = 0
+        v[b, :, int(t0[b]):] = 0
+    kv = S.KVCache(k, v, lens, wl.Hq)
+    dec = S.SparseDecoder(kv, N=int(wl.budget[0]), w=wl.w, tau=wl.tau, scale=wl.scale,
+                          n_sink=n_sink, window=window, n_den=n_den)
+    o, l, dl, r, n = dec.alloc_outputs(steps)
+    dl.fill_(float("nan"))
+    sets = []
+    hkv = torch.arange(wl.Hq, device="cuda") // G
+    for s in range(steps):
+        rows_k = np.stack([np.stack([wl.logical_rows("K", b, h)[int(t0[b]) + s] for h in range(wl.Hkv)])
+                           for b in range(wl.B)])
+        rows_v = np.stack([np.stack([wl.logical_rows("V", b, h)[int(t0[b]) + s] for h in range(wl.Hkv)])
+                           for b in range(wl.B)])
+        kt, vt = tensor_of(rows_k, wl.dtype, "cuda"), tensor_of(rows_v, wl.dtype, "cuda")
+        dec.append(kt, vt)
+        g = kt[:, hkv].contiguous() if gate == "key" else None   # [B][Hq][d]
+        dec.step(dev["q"][s], o[s], l[s], dl[s], r[s], n[s], gate=g)
+        sets.append((dec.idx.cpu().numpy(), n[s].cpu().numpy()))
+    assert S.last_error() == 0
+    o, l, dl, r = [x.cpu().numpy() for x in (o, l, dl, r)]
+    compared = reused = 0
+    for b in range(wl.B):
+        for h in range(wl.Hq):
+            K, V = kv_rows64(wl, b, h // G)
+            qs = np.stack([q64(wl, s, b, h) for s in range(steps)])
+            recs = P.decode_head_grow(qs, K, V, int(t0[b]), int(wl.budget[b]), wl.w, wl.tau,
+                                      wl.scale, n_sink, window, keep_scores=True, n_den=n_den,
+                                      gate=gate)
+            for s, rec in enumerate(recs):
+                if rec.cos is not None and abs(rec.cos - wl.tau) < GATE_GAP:
+                    break
+                assert bool(r[s, b, h]) == rec.reuse, (b, h, s)
+                gi, gn = sets[s]
+                gset = gi[b, h, :gn[b, h]]
+                if gset.size != rec.S.size or (gset != rec.S).any():
+                    assert not rec.reuse, ("shared set differs", b, h, s)
+                    break   # a near-tie among the ranked keys: later queries may differ
+                if not rec.reuse:
+                    assert abs(dl[s, b, h] - rec.delta) <= DELTA_TOL, (b, h, s)
+                assert np.abs(o[s, b, h] - rec.out).max() <= OUT_TOL, (b, h, s)
+                assert abs(l[s, b, h] - rec.lse) <= LSE_TOL, (b, h, s)
+                compared += 1
+                reused += rec.reuse
+    assert compared >= wl.B * wl.Hq * steps // 2, compared
+    assert reused > 0 and reused < compared, (reused, compared)

@@ -440,6 +440,67 @@ def test_cis_dilate(dtype, d):
                 assert gn[b, h] == -4 and (gi[b, h] == -4).all()
 
 
+@pytest.mark.parametrize("w,n_den,n_sink,window", [(2, 1, 0, 0), (2, 2, 0, 0), (3, 5, 0, 0), (1, 3, 0, 0),
+                                                    (4, 2, 0, 0), (0, 2, 0, 0), (2, 3, 4, 16),
+                                                    (3, 1, 2, 0), (2, 4, 0, 9)])
+def test_cis_dilate_budget(w, n_den, n_sink, window):
+    """Budgeted dilation (Fig. 9a): every reusing head's set against the
+    oracle's dilate_budget with m = floor(anchor_n / n_den), united with
+    the forced keys; anchor rows of every size, some running into either
+    end of the cache, some over 1024 entries (several passes of the kernel)."""
+    import sparse_kv_selection_gb300 as S
+    rng = np.random.default_rng(31 + w + 7 * n_den)
+    B, H, d, acap = 2, 6, 64, 1500
+    lens = np.array([3000, 700], np.int32)
+    t_max = int(lens.max())
+    cap = min(t_max, acap * (2 * w + 1) + n_sink + window)
+    k = torch.zeros(B, H, t_max, d, device="cuda")
+    kv = S.KVCache(k, k, torch.from_numpy(lens).cuda(), H)
+    q = torch.from_numpy(rng.normal(size=(B, H, d)).astype(np.float32)).cuda()
+    an = np.zeros((B, H), np.int32)
+    aidx = np.zeros((B, H, acap), np.int32)
+    sizes = [1, 7, 300, 1100, 1500, 40]
+    for b in range(B):
+        t = int(lens[b])
+        lo, hi = min(n_sink, t), max(min(n_sink, t), t - window)   # anchors avoid the forced keys
+        for h in range(H):
+            n_ = min(sizes[h], hi - lo, acap)
+            an[b, h] = n_
+            if h == 5:      # runs into both ends of the middle range
+                row = np.concatenate([np.arange(lo, lo + n_ // 2), np.arange(hi - (n_ - n_ // 2), hi)])
+            else:
+                row = np.sort(lo + rng.choice(hi - lo, size=n_, replace=False))
+            aidx[b, h, :n_] = row
+    idx = torch.full((B, H, cap), -4, dtype=torch.int32, device="cuda")
+    n_sel = torch.full((B, H), -4, dtype=torch.int32, device="cuda")
+    reuse = torch.zeros((B, H), dtype=torch.uint8, device="cuda")
+    S.cis_dilate(kv, torch.from_numpy(aidx).cuda(), torch.from_numpy(an).cuda(), q, q, w, 0.8, idx,
+                 n_sel, reuse, n_sink=n_sink, window=window, n_den=n_den)
+    assert S.last_error() == 0
+    gi, gn = idx.cpu().numpy(), n_sel.cpu().numpy()
+    assert reuse.cpu().numpy().all()
+    for b in range(B):
+        t = int(lens[b])
+        for h in range(H):
+            A = aidx[b, h, :an[b, h]].astype(np.int64)
+            want = np.union1d(P.forced_set(t, n_sink, window),
+                              P.dilate_budget(A, w, t, len(A) // n_den))
+            assert gn[b, h] == len(want), (b, h, gn[b, h], len(want))
+            assert gi[b, h, :gn[b, h]].tolist() == want.tolist(), (b, h)
+
+
+@pytest.mark.parametrize("name,n_den", [("mha_bf16_ragged", 2), ("gqa4_bf16", 4), ("paged_bf16", 1),
+                                        ("f32_d64_gqa2", 3)])
+def test_decode_budgeted_dilation(name, n_den):
+    """Decode with budgeted dilation against the oracle, free-running and
+    teacher-forced."""
+    S, wl, dev, kv = _setup(name)
+    compared, r = compare_decode(wl, dev, kv, _heads(wl), n_den=n_den)
+    assert compared >= len(_heads(wl)) * wl.steps // 2 and r[1:].any()
+    compared = compare_decode_forced(wl, dev, kv, _heads(wl), n_den=n_den)
+    assert compared >= len(_heads(wl)) * wl.steps - 2, compared
+
+
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
 @pytest.mark.parametrize("gap", [1e-3, 2e-4, 5e-5, 1e-6, 1e-9, 1e-11])
 def test_cis_gate_near_threshold(dtype, d, gap):

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libprhs.so")
-SOURCES = ["api.cu", "score.cu", "cis.cu", "attn.cu", "attn_cluster.cu", "select.cu", "dense.cu",
+SOURCES = ["api.cu", "score.cu", "cis.cu", "attn.cu", "attn_cluster.cu", "select.cu", "retrieve.cu", "dense.cu",
            "noalloc.cu", "mass.cu", "grow.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

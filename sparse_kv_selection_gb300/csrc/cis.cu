@@ -7,9 +7,10 @@
 //
 // One CTA per query head. The gate takes the decision of the float64 formula
 // c = <q, q_a> / (sqrt(|q|^2) sqrt(|q_a|^2)) >= tau. Its first warp forms the
-// three sums in fp32 (bf16 products are exact in fp32; tree sums of d <= 128
-// terms stay within 8 roundings, so the fp32 cosine is within about 2e-6 of
-// the exact one) and decides from them when that cosine lies farther than
+// three sums in fp32 (on bf16 caches the products are exact in fp32, on fp32
+// ones each adds one rounding; tree sums of d <= 128 terms stay within 8
+// roundings, so the fp32 cosine is within a few 1e-6 of the exact one, far
+// inside the margin) and decides from them when that cosine lies farther than
 // CIS_MARGIN = 1e-4 from tau; otherwise, or when a sum is not finite or a norm
 // is tiny, the same warp recomputes the sums and the ratio in float64. fp64 is
 // slow on this part, so the common case avoids it. The dilated set

@@ -179,6 +179,15 @@ cudaError_t launch_select_global(const SelectLaunch& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the cache is too long for it.
 bool score_select_fits(const KVView& kv);
 cudaError_t launch_score_select(const SelectLaunch& a, cudaStream_t s);
+// The cluster size and slice length of the score-and-select kernels (false:
+// the cache is too long for them), and their launch: one cluster of cl CTAs
+// per query head, with programmatic dependent launch when the view allows it.
+bool score_select_geometry(const KVView& kv, int* cl, int* chunk);
+cudaError_t launch_select_grid(void (*k)(const SelectLaunch, int), const SelectLaunch& a, int cl,
+                               int chunk, size_t smem, cudaStream_t s);
+// Retrieval in one launch (logits, selection spread over the cluster, the
+// attention over the set): a.out and a.lse set, no forced keys.
+cudaError_t launch_retrieve(const SelectLaunch& a, cudaStream_t s);
 cudaError_t launch_cis(const CisLaunch& a, cudaStream_t s);
 cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t s);
 // Sparse attention with one thread-block cluster of a.cluster CTAs per query

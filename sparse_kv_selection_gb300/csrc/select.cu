@@ -1,7 +1,7 @@
 // Top-N selection and dropped mass, one thread-block cluster per query head:
 // from the logits of prhs_score (select_cluster_kernel), or with the logits
-// computed from K in the same launch and, for retrieval, the attention over
-// the selected set (score_select_kernel, caches of up to 8192 keys).
+// computed from K in the same launch (score_select_kernel, caches of up to
+// 8192 keys; the retrieval with its attention is in retrieve.cu).
 // "Near-Oracle KV Selection via Pre-hoc Sparsity for Long-Context Inference":
 // abstract (top-k oracle selection before attention; the dropped mass delta),
 // Table I (S_t, N, tau(.), delta(.)) and the Table V caption (attention over
@@ -209,16 +209,12 @@ __device__ __forceinline__ void slice_logits(const SelectLaunch& a, int qh, int 
 // [lo, lo + cnt) of query head qh in cache (forced keys as -inf), and vmin,
 // vmax is its thread's share of their range. The CL CTAs of the cluster call
 // it together (CL = 1 when ONE).
-// With wout and sel_out (one CTA, lo = 0), it also leaves the set in sel_out
-// (ascending, in shared memory) and, in place of each selected logit in
-// wout, its weight exp(s - max).
 template <typename T, bool ONE>
 __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClusterShared& sh,
                                                  const float* cache, cg::cluster_group& cluster,
                                                  const int CL, const int rank, const int qh, const int Nb,
                                                  int32_t* out, int32_t* aout, const int lo, const int cnt,
-                                                 float vmin, float vmax, float* wout = nullptr,
-                                                 int32_t* sel_out = nullptr) {
+                                                 float vmin, float vmax) {
   const KVView& kv = a.kv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < 2048; i += SEL_THREADS) sh.hist[i] = 0;
@@ -489,10 +485,6 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
         if (pos < Nb) {
           out[pos] = lo + i;
           if (aout) aout[pos] = lo + i;
-          if (sel_out) {  // only this thread reads cache[i]
-            sel_out[pos] = lo + i;
-            wout[i] = wgt;
-          }
         } else {
           raise_error(kv.err, PRHS_DEV_CAPACITY);
         }
@@ -617,22 +609,15 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   select_in_shared<T, ONE>(a, sh, cache, cluster, CL, rank, qh, Nb, out, aout, lo, cnt, vmin, vmax);
 }
 
-// Logits and top-N selection of one query head in one launch, and with ATTN
-// the attention over the selected set. The cluster's CL CTAs each compute the
-// logits of one slice of keys straight from K and store them into CTA 0's
+// Logits and top-N selection of one query head in one launch (the retrieval
+// with its attention is retrieve_kernel). The cluster's CL CTAs each compute
+// the logits of one slice of keys straight from K and store them into CTA 0's
 // shared memory (distributed shared memory), with the slice's logit range;
 // after one cluster barrier CTA 0 alone selects from the whole row, as the
-// one-CTA selection does. Without ATTN the other CTAs are then done. With
-// ATTN (no forced keys) CTA 0 also leaves the set and each selected key's
-// weight exp(s - max) in its shared memory; after a second barrier every CTA
-// gathers the V rows of an equal share of the set, weighting them by those
-// weights (no second read of K), and pushes its sums into CTA 0, which after
-// a third barrier writes out = sum(w v) / sum(w) and lse = max + ln sum(w).
-// The weights are all relative to the head's largest logit, which is always
-// selected, so the shares add without rescaling.
-template <typename T, int DK, bool ONE, bool ATTN>
+// one-CTA selection does, and the other CTAs are done.
+template <typename T, int DK, bool ONE>
 __global__ void __launch_bounds__(SEL_THREADS, 2) score_select_kernel(const SelectLaunch a, int chunk) {
-  extern __shared__ float cache[];  // CTA 0: the head's logits (t_max), then with ATTN the set (t_max)
+  extern __shared__ float cache[];  // CTA 0: the head's logits (t_max)
   __shared__ SelClusterShared sh;
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = ONE ? 1 : (int)cluster.num_blocks();
@@ -656,13 +641,12 @@ __global__ void __launch_bounds__(SEL_THREADS, 2) score_select_kernel(const Sele
   int32_t* out = a.idx + (long long)qh * a.cap;
   int32_t* aout = a.anchor_idx != nullptr ? a.anchor_idx + (long long)qh * a.anchor_cap : nullptr;
   const int lo = min(t, rank * chunk), hi = min(t, lo + chunk), cnt = hi - lo;
-  const int ns = min(max(a.n_sink, 0), t);   // forced keys [0, ns) and [we, t) (never with ATTN)
+  const int ns = min(max(a.n_sink, 0), t);   // forced keys [0, ns) and [we, t)
   const int we = max(ns, t - max(a.window, 0));
   const int tmid = we - ns;
 
-  // every middle key or none, without ranking (uniform over the cluster); with
-  // ATTN only the empty set comes here, every key goes through the attention
-  if (Nb == 0 || (ATTN ? tmid == 0 : Nb >= tmid)) {
+  // every middle key or none, without ranking (uniform over the cluster)
+  if (Nb == 0 || Nb >= tmid) {
     const int n = Nb >= tmid ? tmid : 0;
     for (int i = max(lo, ns) + tid; i < min(hi, ns + n); i += SEL_THREADS) {
       out[i - ns] = i;
@@ -677,10 +661,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 2) score_select_kernel(const Sele
         a.n_sel[qh] = n;
         a.delta[qh] = n == t ? 0.f : 1.f;  // recomputed over the whole set when keys are forced
         if (a.anchor_n) a.anchor_n[qh] = n;
-        if (ATTN) a.lse[qh] = -INFINITY;
       }
-      if (ATTN)
-        for (int e = tid; e < DK; e += SEL_THREADS) a.out[(long long)qh * DK + e] = 0.f;
       if (a.q_anchor) mirror_query<T>(a, qh);
     }
     return;
@@ -714,125 +695,15 @@ __global__ void __launch_bounds__(SEL_THREADS, 2) score_select_kernel(const Sele
     __syncthreads();
   } else {
     cluster.sync();  // every slice and range is in CTA 0
-    if (!ATTN && rank != 0) return;
-  }
-  int32_t* sel = reinterpret_cast<int32_t*>(cache + kv.t_max);  // CTA 0, with ATTN: the set
-  float smax = -INFINITY;
-  if (rank == 0) {
-    float smin = INFINITY;
-    for (int r = 0; r < CL; r++) {
-      smin = fminf(smin, sh.rmin[r]);
-      smax = fmaxf(smax, sh.rmax[r]);
-    }
-    __syncthreads();  // sh.red is reused by the selection
-    if (ATTN && Nb >= t) {  // every key: weights exp(s - max), delta = 0
-      for (int i = tid; i < t; i += SEL_THREADS) {
-        out[i] = i;
-        if (aout) aout[i] = i;
-        sel[i] = i;
-        cache[i] = expf(cache[i] - smax);
-      }
-      if (tid == 0) {
-        a.n_sel[qh] = t;
-        a.delta[qh] = 0.f;
-        if (a.anchor_n) a.anchor_n[qh] = t;
-      }
-      if (a.q_anchor) mirror_query<T>(a, qh);
-    } else {
-      select_in_shared<T, true>(a, sh, cache, cluster, 1, 0, qh, Nb, out, aout, 0, t, smin, smax,
-                                ATTN ? cache : nullptr, ATTN ? sel : nullptr);
-    }
-  }
-  if constexpr (ATTN) {
-    // ---- attention: this CTA's share of the set, V rows weighted from CTA 0 ----
-    if (ONE) __syncthreads(); else cluster.sync();  // the set and its weights are in CTA 0
-    constexpr int EPC = Elem<T>::per16;
-    constexpr int LPR = DK / EPC;            // lanes per V row
-    constexpr int RPW = SEL_THREADS / LPR;   // rows per CTA-wide wave
-    constexpr int U = 4;                     // waves in flight per thread
-    const int n = min(Nb, t);
-    const int j = tid & (LPR - 1), rsub = tid / LPR;
-    const int kvh = (qh % kv.Hq) / (kv.Hq / kv.Hkv);
-    const int per = (n + CL - 1) / CL;
-    const int p0 = min(n, rank * per), p1 = min(n, p0 + per);
-    const int32_t* sel0 = ONE ? sel : cluster.map_shared_rank(sel, 0);
-    const float* w0 = ONE ? cache : cluster.map_shared_rank(cache, 0);
-    const char* vb = static_cast<const char*>(kv.v);
-    float acc[EPC];
-#pragma unroll
-    for (int e = 0; e < EPC; e++) acc[e] = 0.f;
-    float lsum = 0.f;
-    for (int pb = p0; pb < p1; pb += RPW * U) {
-      int ii[U];
-      float ww[U];
-      uint4 raw[U];
-#pragma unroll
-      for (int u = 0; u < U; u++) {
-        const int p = pb + u * RPW + rsub;
-        ii[u] = p < p1 ? sel0[p] : -1;
-        if (ii[u] >= t) ii[u] = -1;  // only after a failed selection (flagged there)
-      }
-#pragma unroll
-      for (int u = 0; u < U; u++) {
-        ww[u] = ii[u] >= 0 ? w0[ii[u]] : 0.f;
-        long long r = -1;
-        if (ii[u] >= 0) {
-          r = kv_row(kv, b, kvh, ii[u]);
-          if (r < 0 && j == 0) raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
-        }
-        raw[u] = r >= 0 ? ldg_stream(vb + r * (long long)(DK * sizeof(T)) + 16 * j)
-                        : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < U; u++) {
-        float f[EPC];
-        Elem<T>::unpack(raw[u], f);
-#pragma unroll
-        for (int e = 0; e < EPC; e++) acc[e] = fmaf(ww[u], f[e], acc[e]);
-        lsum += ww[u];
-      }
-    }
-    // sum over the rows of a warp (lanes with the same j), then over warps
-#pragma unroll
-    for (int o = LPR; o < 32; o <<= 1) {
-#pragma unroll
-      for (int e = 0; e < EPC; e++) acc[e] += __shfl_xor_sync(FULL_MASK, acc[e], o);
-      lsum += __shfl_xor_sync(FULL_MASK, lsum, o);
-    }
-    float* wsum = reinterpret_cast<float*>(sh.hist);  // [SEL_WARPS][DK], free after the selection
-    static_assert(SEL_WARPS * DK <= 2048, "warp sums fit the histogram");
-    if (lane < LPR)
-#pragma unroll
-      for (int e = 0; e < EPC; e++) wsum[warp * DK + j * EPC + e] = acc[e];
-    if (lane == 0) sh.red[warp] = lsum;
-    __syncthreads();
-    // this CTA's sums into CTA 0's partial table (its pass-1 totals, unused by one CTA)
-    SelClusterShared* root = ONE ? &sh : cluster.map_shared_rank(&sh, 0);
-    float* part = reinterpret_cast<float*>(&root->histg[0][0]) + rank * (DK + 1);
-    static_assert(SELECT_FUSED_CL * (DK + 1) <= 2 * 2048, "partials fit the totals table");
-    for (int e = tid; e < DK; e += SEL_THREADS) {
-      float o = 0.f;
-      for (int w = 0; w < SEL_WARPS; w++) o += wsum[w * DK + e];
-      part[e] = o;
-    }
-    if (tid == 0) {
-      float l = 0.f;
-      for (int w = 0; w < SEL_WARPS; w++) l += sh.red[w];
-      part[DK] = l;
-    }
-    if (ONE) __syncthreads(); else cluster.sync();  // every share is in CTA 0
     if (rank != 0) return;
-    const float* pt = reinterpret_cast<const float*>(&sh.histg[0][0]);
-    for (int e = tid; e < DK; e += SEL_THREADS) {
-      float O = 0.f, L = 0.f;
-      for (int r = 0; r < CL; r++) {
-        O += pt[r * (DK + 1) + e];
-        L += pt[r * (DK + 1) + DK];
-      }
-      a.out[(long long)qh * DK + e] = L > 0.f ? O / L : 0.f;
-      if (e == 0) a.lse[qh] = L > 0.f ? smax + logf(L) : -INFINITY;
-    }
   }
+  float smin = INFINITY, smax = -INFINITY;
+  for (int r = 0; r < CL; r++) {
+    smin = fminf(smin, sh.rmin[r]);
+    smax = fmaxf(smax, sh.rmax[r]);
+  }
+  __syncthreads();  // sh.red is reused by the selection
+  select_in_shared<T, true>(a, sh, cache, cluster, 1, 0, qh, Nb, out, aout, 0, t, smin, smax);
 }
 
 // Cluster size and slice length: one CTA holds up to SELECT_SLICE_ONE logits;
@@ -850,10 +721,9 @@ static void select_geometry(const KVView& kv, int sms, int* cl, int* chunk) {
   *chunk = ((tmax + c - 1) / c + 3) / 4 * 4;
 }
 
-// One cluster of cl CTAs per query head, `floats` logits of shared memory each.
-static cudaError_t launch_clustered(void (*k)(const SelectLaunch, int), const SelectLaunch& a, int cl,
-                                    int chunk, int floats, cudaStream_t st) {
-  const size_t smem = (size_t)floats * sizeof(float);
+// One cluster of cl CTAs per query head, smem bytes of dynamic shared memory each.
+cudaError_t launch_select_grid(void (*k)(const SelectLaunch, int), const SelectLaunch& a, int cl,
+                               int chunk, size_t smem, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (cl > 8) {
@@ -892,13 +762,13 @@ cudaError_t launch_select(const SelectLaunch& a, cudaStream_t st) {
     k = cl == 1 ? select_cluster_kernel<__nv_bfloat16, true> : select_cluster_kernel<__nv_bfloat16, false>;
   else
     k = cl == 1 ? select_cluster_kernel<float, true> : select_cluster_kernel<float, false>;
-  return launch_clustered(k, a, cl, chunk, chunk, st);
+  return launch_select_grid(k, a, cl, chunk, (size_t)chunk * sizeof(float), st);
 }
 
 // Score-and-select geometry: the fewest CTAs (a power of two up to
 // SELECT_FUSED_CL) whose slices hold at most SELECT_FUSED_ROWS keys each, or
 // SELECT_FUSED_CL CTAs of up to SELECT_FUSED_MAX_ROWS.
-static bool fused_geometry(const KVView& kv, int* cl, int* chunk) {
+bool score_select_geometry(const KVView& kv, int* cl, int* chunk) {
   int c = 1;
   while (c < SELECT_FUSED_CL && (kv.t_max + c - 1) / c > SELECT_FUSED_ROWS) c *= 2;
   if ((kv.t_max + c - 1) / c > SELECT_FUSED_MAX_ROWS) return false;
@@ -909,19 +779,15 @@ static bool fused_geometry(const KVView& kv, int* cl, int* chunk) {
 
 bool score_select_fits(const KVView& kv) {
   int cl, chunk;
-  return (kv.d == 64 || kv.d == 128) && fused_geometry(kv, &cl, &chunk);
+  return (kv.d == 64 || kv.d == 128) && score_select_geometry(kv, &cl, &chunk);
 }
 
 template <typename T, int DK>
 static cudaError_t score_select_dispatch_d(const SelectLaunch& a, int cl, int chunk, cudaStream_t st) {
-  void (*k)(const SelectLaunch, int);
-  const bool attn = a.out != nullptr;
-  if (attn)
-    k = cl == 1 ? score_select_kernel<T, DK, true, true> : score_select_kernel<T, DK, false, true>;
-  else
-    k = cl == 1 ? score_select_kernel<T, DK, true, false> : score_select_kernel<T, DK, false, false>;
-  // CTA 0 holds the whole row of logits, and with the attention the set too
-  return launch_clustered(k, a, cl, chunk, a.kv.t_max * (attn ? 2 : 1), st);
+  void (*k)(const SelectLaunch, int) =
+      cl == 1 ? score_select_kernel<T, DK, true> : score_select_kernel<T, DK, false>;
+  // CTA 0 holds the whole row of logits
+  return launch_select_grid(k, a, cl, chunk, (size_t)a.kv.t_max * sizeof(float), st);
 }
 
 template <typename T>
@@ -933,8 +799,8 @@ static cudaError_t score_select_dispatch(const SelectLaunch& a, int cl, int chun
 
 cudaError_t launch_score_select(const SelectLaunch& a, cudaStream_t st) {
   int cl = 1, chunk = 0;
-  if (!fused_geometry(a.kv, &cl, &chunk)) return cudaErrorNotSupported;
-  if (a.out != nullptr && (a.lse == nullptr || a.n_sink > 0 || a.window > 0)) return cudaErrorInvalidValue;
+  if (!score_select_geometry(a.kv, &cl, &chunk)) return cudaErrorNotSupported;
+  if (a.out != nullptr) return launch_retrieve(a, st);
   return a.kv.dtype == PRHS_BF16 ? score_select_dispatch<__nv_bfloat16>(a, cl, chunk, st)
                                  : score_select_dispatch<float>(a, cl, chunk, st);
 }

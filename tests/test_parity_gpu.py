@@ -387,6 +387,53 @@ def test_retrieve_long_cache(t, N, Hq, Hkv, paged):
 # --------------------------------------------------------------------------- #
 # CIS gate and dilation
 # --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("n_sink,window,n_den", [(0, 0, 0), (4, 64, 0), (4, 64, 2)])
+def test_cis_dilate_cluster(n_sink, window, n_den):
+    """Few heads with long anchor rows: the gate's dilation split over a
+    cluster of CTAs per head (4096 entries, 4 CTAs of 1024; budgeted dilation
+    keeps one CTA). A full row, a row of 1500 entries (the last two CTAs
+    empty) and a row of 3000 with runs of adjacent anchors across the CTAs'
+    boundaries and anchors inside the forced window, against the oracle's
+    (budgeted) dilation joined with the forced keys."""
+    import sparse_kv_selection_gb300 as S
+    from workloads import bf16_bits_from_f32
+    from workloads.torch_io import tensor_of
+    rng = np.random.default_rng(5)
+    B, H, t, acap, w, d = 1, 3, 40000, 4096, 3, 128
+    cap = min(t, acap * (2 * w + 1) + n_sink + window)
+    k = torch.zeros(B, H, t, d, dtype=torch.bfloat16, device="cuda")
+    kv = S.KVCache(k, k, torch.tensor([t], dtype=torch.int32, device="cuda"), H)
+    q = rng.normal(size=(B, H, d)).astype(np.float32)
+    qa = q + 0.05 * rng.normal(size=(B, H, d)).astype(np.float32)   # cosine near 0.999: reuse
+    an = np.array([[4096, 1500, 3000]], np.int32)
+    aidx = np.zeros((B, H, acap), np.int32)
+    aidx[0, 0] = np.sort(rng.choice(t, size=4096, replace=False))
+    aidx[0, 1, :1500] = np.sort(rng.choice(t, size=1500, replace=False))
+    third = set(rng.choice(t - 200, size=2900, replace=False).tolist())
+    third = sorted(third)[:2900]
+    third = np.array(third, np.int64)
+    third[1015:1035] = third[1015] + np.arange(20)           # a run across entry 1024
+    third = np.unique(np.concatenate([third, np.arange(t - 100, t)]))[:3000]
+    an[0, 2] = len(third)
+    aidx[0, 2, :len(third)] = np.sort(third)
+    idx = torch.full((B, H, cap), -4, dtype=torch.int32, device="cuda")
+    n_sel = torch.full((B, H), -4, dtype=torch.int32, device="cuda")
+    reuse = torch.full((B, H), 9, dtype=torch.uint8, device="cuda")
+    S.cis_dilate(kv, torch.from_numpy(aidx).cuda(), torch.from_numpy(an).cuda(),
+                 tensor_of(bf16_bits_from_f32(q), "bf16", "cuda"),
+                 tensor_of(bf16_bits_from_f32(qa), "bf16", "cuda"), w, 0.8, idx, n_sel, reuse,
+                 n_sink=n_sink, window=window, n_den=n_den)
+    assert S.last_error() == 0
+    gi, gn, gr = idx.cpu().numpy(), n_sel.cpu().numpy(), reuse.cpu().numpy()
+    for h in range(H):
+        assert gr[0, h] == 1, h
+        anc = aidx[0, h, :an[0, h]]
+        shared = P.dilate(anc, w, t) if n_den == 0 else P.dilate_budget(anc, w, t, len(anc) // n_den)
+        ref = np.union1d(P.forced_set(t, n_sink, window), shared)
+        assert gn[0, h] == len(ref), (h, gn[0, h], len(ref))
+        assert (gi[0, h, :gn[0, h]] == ref).all(), h
+
+
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
 def test_cis_dilate(dtype, d):
     import sparse_kv_selection_gb300 as S

@@ -533,6 +533,36 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
   if (!ONE) head_sync<ONE>(cluster);  // shared memory stays valid until every remote read is done
 }
 
+// The c-th query head not flagged in skip (c = blockIdx.x), or -1 when fewer
+// heads are left: every thread reads up to SEL_ORDER_PER flags, the block
+// counts the unflagged ones and the thread holding the c-th names it. Heads
+// with work then take the lowest block indices, which the block scheduler
+// places first, and the CTAs past them exit without holding a slot long.
+constexpr int SEL_ORDER_PER = 8;
+__device__ __forceinline__ int nth_unskipped(const uint8_t* skip, int units, int c, unsigned* warp_tot,
+                                             int* found) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j0 = tid * SEL_ORDER_PER;
+  unsigned mine = 0;  // bit k: unit j0 + k has work
+#pragma unroll
+  for (int k = 0; k < SEL_ORDER_PER; k++)
+    if (j0 + k < units && skip[j0 + k] == 0) mine |= 1u << k;
+  const unsigned cnt = __popc(mine);
+  unsigned total;
+  const unsigned before = scan_block(cnt, warp_tot, total) - cnt;
+  if (tid == 0) *found = -1;
+  __syncthreads();
+  if ((unsigned)c >= before && (unsigned)c < before + cnt) {
+    unsigned m = mine;
+    for (unsigned r = (unsigned)c - before; r > 0; r--) m &= m - 1;  // drop the lower set bits
+    *found = j0 + __ffs(m) - 1;
+  }
+  __syncthreads();
+  (void)lane;
+  (void)warp;
+  return *found;
+}
+
 template <typename T, bool ONE>
 __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const SelectLaunch a, int chunk) {
   extern __shared__ float cache[];
@@ -544,9 +574,15 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   pdl_trigger();
 
   const KVView& kv = a.kv;
-  const int qh = blockIdx.x / CL;  // the cluster's query head (b * Hq + h)
+  int qh = blockIdx.x / CL;  // the cluster's query head (b * Hq + h)
+  if (ONE && a.head_skip != nullptr && kv.B * kv.Hq <= SEL_THREADS * SEL_ORDER_PER) {
+    __shared__ int found;
+    qh = nth_unskipped(a.head_skip, kv.B * kv.Hq, qh, sh.scan, &found);
+    if (qh < 0) return;
+  } else if (a.head_skip != nullptr && a.head_skip[qh] != 0) {
+    return;  // uniform over the cluster
+  }
   const int b = qh / kv.Hq;
-  if (a.head_skip != nullptr && a.head_skip[qh] != 0) return;  // uniform over the cluster
   const int tid = threadIdx.x;
   const int t = seq_len(kv, b);
   int Nb = a.n_budget != nullptr ? a.n_budget[b] : a.N;

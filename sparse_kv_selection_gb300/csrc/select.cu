@@ -479,7 +479,9 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
         take = true;
         pos = (int)(g + q);
       }
-      const float wgt = expf(sv[e] - smax);
+      // weights for delta only (dropped / total mass): the fast exponential's
+      // few-ulp error is far inside the 1e-4 tolerance of delta
+      const float wgt = __expf(sv[e] - smax);
       if (take) {
         ssum += wgt;
         if (pos < Nb) {
@@ -565,11 +567,18 @@ __device__ __forceinline__ int nth_unskipped(const uint8_t* skip, int units, int
 
 template <typename T, bool ONE>
 __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const SelectLaunch a, int chunk) {
-  extern __shared__ float cache[];
+  extern __shared__ __align__(16) float cache[];
   __shared__ SelClusterShared sh;
+  __shared__ __align__(8) uint64_t lbar;  // the bulk copy of the logits
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = ONE ? 1 : (int)cluster.num_blocks();
   const int rank = ONE ? 0 : (int)cluster.block_rank();
+  // a row stride of whole 16-byte groups lets one bulk copy bring the slice in
+  const bool bulk = (a.kv.t_max & 3) == 0;
+  if (bulk && threadIdx.x == 0) {
+    mbar_init(&lbar, 1);
+    fence_barrier_init();
+  }
   pdl_wait();
   pdl_trigger();
 
@@ -621,8 +630,26 @@ __global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const Selec
   // ---- load this CTA's slice; its logit range ----
   const float* src = a.scores + (long long)qh * kv.t_max + lo;
   float vmin = INFINITY, vmax = -INFINITY;
+  if (bulk) {
+    __syncthreads();  // the barrier's initialisation is visible
+    const int cnt4 = (cnt + 3) & ~3;  // whole 16-byte groups, inside the row (t_max % 4 == 0)
+    if (tid == 0 && cnt4 > 0) {
+      mbar_arrive_expect_tx(&lbar, (uint32_t)(cnt4 * sizeof(float)));
+      bulk_load(cache, src, (uint32_t)(cnt4 * sizeof(float)), &lbar);
+    }
+    const bool ok = cnt4 == 0 || mbar_wait(&lbar, 0, kv.err);
+    for (int i = tid; i < cnt; i += SEL_THREADS) {
+      const float v = ok ? cache[i] : 0.f;
+      const bool forced = lo + i < ns || lo + i >= we;  // ranked below every middle key
+      cache[i] = forced ? -INFINITY : v;
+      if (!forced) {
+        vmin = fminf(vmin, v);
+        vmax = fmaxf(vmax, v);
+      }
+    }
+  }
   constexpr int PRE = 8;  // loads in flight per thread before the first is used
-  for (int i0 = 0; i0 < cnt; i0 += SEL_THREADS * PRE) {
+  for (int i0 = 0; !bulk && i0 < cnt; i0 += SEL_THREADS * PRE) {
     float v[PRE];
 #pragma unroll
     for (int k = 0; k < PRE; k++) {

@@ -43,6 +43,8 @@ struct SelClusterShared {
   unsigned fb[2][2048];       // fallback radix passes: this CTA's histograms
   unsigned cand[SEL_CANDS];   // rank 0: gathered candidate keys; every rank: a copy
   unsigned lcand[SEL_CANDS];  // this CTA's own candidate keys
+  unsigned candi[SEL_CANDS];  // one CTA: each candidate's position in the slice
+  unsigned lcandi[SEL_CANDS]; // cluster: each own candidate's position in the slice
   unsigned ncand, nlcand;
   unsigned scan[32];
   float red[SEL_WARPS], red2[SEL_WARPS];
@@ -260,9 +262,15 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
   const float w1 = (smax - smin) * (1.f / 2048.f);
   const float inv1 = flat ? 0.f : 2048.f / (smax - smin);
 
-  // ---- pass 1: value histogram over [smin, smax] ----
+  // ---- pass 1: value histogram over [smin, smax]; this thread's share of the
+  // CTA's total weight sum exp(s - max) (delta's denominator) ----
+  float zacc = 0.f;
   if (!flat) {
-    for (int i = tid; i < cnt; i += SEL_THREADS) atomicAdd(&sh.hist[vbin(cache[i], smin, inv1)], 1u);
+    for (int i = tid; i < cnt; i += SEL_THREADS) {
+      const float s = cache[i];
+      atomicAdd(&sh.hist[vbin(s, smin, inv1)], 1u);
+      zacc += __expf(s - smax);  // weights for delta only: few-ulp error, 1e-4 tolerance
+    }
     if (!ONE) {
       __syncthreads();
       for (int i = tid; i < 2048; i += SEL_THREADS)
@@ -306,31 +314,58 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
       krem = sh.krem;
     }
     if (sh.cnt_bin <= SEL_CANDS) {
-      // pass 3: gather the candidates; count the logits above them
+      // pass 3: gather the candidates; count the logits above them and mark
+      // them in a bitmap of the slice (one ballot word per warp and 32 keys, in
+      // sh.hist, free after the bin passes)
       unsigned dgt = 0;
-      for (int i = tid; i < cnt; i += SEL_THREADS) {
-        const float s = cache[i];
+      unsigned* bits = sh.hist;
+      constexpr int UC = 4;  // rows of 512 keys per iteration, read before the first is used
+      for (int r0 = 0; r0 < cnt; r0 += SEL_THREADS * UC) {
+        float sv[UC];
+#pragma unroll
+        for (int k = 0; k < UC; k++) {
+          const int i = r0 + k * SEL_THREADS + tid;
+          sv[k] = i < cnt ? cache[i] : -INFINITY;
+        }
+#pragma unroll
+        for (int k = 0; k < UC; k++) {
+        const int i0 = r0 + k * SEL_THREADS;
+        if (i0 >= cnt) break;  // uniform over the block
+        const int i = i0 + tid;
+        const float s = sv[k];
         const int c1 = vbin(s, smin, inv1);
-        bool cand = false;
-        if (c1 > b1) {
-          dgt++;
-        } else if (c1 == b1) {
-          if (b2 < 0) {
-            cand = true;
-          } else {
-            const int c2 = vbin(s, lo1, inv2);
-            if (c2 > b2) dgt++;
-            cand = c2 == b2;
+        bool cand = false, above = false;
+        if (i < cnt) {
+          if (c1 > b1) {
+            above = true;
+          } else if (c1 == b1) {
+            if (b2 < 0) {
+              cand = true;
+            } else {
+              const int c2 = vbin(s, lo1, inv2);
+              above = c2 > b2;
+              cand = c2 == b2;
+            }
           }
         }
+        dgt += above;
+        const unsigned word = __ballot_sync(FULL_MASK, above);
+        if (lane == 0) bits[(i0 >> 5) + warp] = word;
         if (cand) {
           const unsigned u = order_key(s);
           const unsigned slot = atomicAdd(&root->ncand, 1u);
-          if (slot < SEL_CANDS) root->cand[slot] = u;
+          if (slot < SEL_CANDS) {
+            root->cand[slot] = u;
+            if (ONE) root->candi[slot] = (unsigned)i;
+          }
           if (!ONE) {
             const unsigned ls = atomicAdd(&sh.nlcand, 1u);
-            if (ls < SEL_CANDS) sh.lcand[ls] = u;
+            if (ls < SEL_CANDS) {
+              sh.lcand[ls] = u;
+              sh.lcandi[ls] = (unsigned)i;
+            }
           }
+        }
         }
       }
       // a single CTA needs no count of its own: nothing follows it
@@ -432,6 +467,53 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
   constexpr int TILE = SEL_THREADS * E;
   float dsum = 0.f, ssum = 0.f;  // weights exp(s - max) of dropped / kept logits
   const unsigned below = (1u << lane) - 1u;
+  if (!flat && !fallback) {
+    // The candidate path: the bitmap holds the keys above the threshold's bin;
+    // the kept candidates join it (ties in index order, after the lower
+    // ranks' ties), then positions come from a prefix over the words' counts
+    // and only the kept keys are written and weighed (dropped weight = this
+    // CTA's total minus the kept one).
+    unsigned* bits = sh.hist;
+    const unsigned* ck = ONE ? sh.cand : sh.lcand;
+    const unsigned* cix = ONE ? sh.candi : sh.lcandi;
+    const unsigned ncl = min(ONE ? sh.ncand : sh.nlcand, (unsigned)SEL_CANDS);
+    if (tid < (int)ncl) {
+      const unsigned u = ck[tid], i = cix[tid];
+      bool keep = u > thr;
+      if (u == thr) {
+        unsigned r = carry_eq;  // equal keys before this one, in index order
+        for (unsigned jj = 0; jj < ncl; jj++) r += ck[jj] == thr && cix[jj] < i;
+        keep = r < keq;
+      }
+      if (keep && (int)i < cnt) atomicOr(&bits[i >> 5], 1u << (i & 31));
+    }
+    __syncthreads();
+    // rounds of one word per thread (kept keys cluster in index order, so
+    // contiguous ranges per thread would leave a few threads most of them)
+    const int nw = (cnt + 31) >> 5;
+    unsigned carry_pos = carry_gt + min(carry_eq, keq);
+    for (int w0 = 0; w0 < nw; w0 += SEL_THREADS) {
+      const int w = w0 + tid;
+      unsigned m = w < nw ? bits[w] : 0u;
+      const unsigned c = __popc(m);
+      unsigned tot_kept;
+      unsigned pos = carry_pos + scan_block(c, sh.scan, tot_kept) - c;
+      carry_pos += tot_kept;
+      while (m != 0u) {
+        const int i = (w << 5) + __ffs(m) - 1;
+        m &= m - 1u;
+        if (pos < (unsigned)Nb) {
+          out[pos] = lo + i;
+          if (aout) aout[pos] = lo + i;
+        } else {
+          raise_error(kv.err, PRHS_DEV_CAPACITY);
+        }
+        pos++;
+        ssum += __expf(cache[i] - smax);
+      }
+    }
+    dsum = zacc - ssum;
+  } else
   for (int base = 0; base < cnt; base += TILE) {
     const int wbase = base + warp * WSPAN;
     float sv[E];
@@ -566,7 +648,7 @@ __device__ __forceinline__ int nth_unskipped(const uint8_t* skip, int units, int
 }
 
 template <typename T, bool ONE>
-__global__ void __launch_bounds__(SEL_THREADS) select_cluster_kernel(const SelectLaunch a, int chunk) {
+__global__ void __launch_bounds__(SEL_THREADS, 2) select_cluster_kernel(const SelectLaunch a, int chunk) {
   extern __shared__ __align__(16) float cache[];
   __shared__ SelClusterShared sh;
   __shared__ __align__(8) uint64_t lbar;  // the bulk copy of the logits

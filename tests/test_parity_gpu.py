@@ -384,6 +384,56 @@ def test_retrieve_long_cache(t, N, Hq, Hkv, paged):
         assert np.abs(go[0, h] - ro).max() <= OUT_TOL and abs(gl[0, h] - rl) <= LSE_TOL, h
 
 
+@pytest.mark.parametrize("t", [4096, 12000, 50000])
+def test_retrieve_geometric_logits_radix_fallback(t):
+    """Logits in a geometric progression (2^0 ... 2^-99, many copies of each,
+    above them a hundred values in (1, 1.8]): value bins over the range leave the small
+    ones in one bin round after round, so every selection form ends in its
+    radix fallback: the one-launch retrieval (4096 keys), the one-CTA
+    selection (12000) and the cluster selection (50000). With q = e1, scale
+    1 and bf16-exact key values the logits are exact on both sides, so the
+    set (ties by lowest index) must equal the oracle's exactly."""
+    import sparse_kv_selection_gb300 as S
+    from workloads import bf16_bits_from_f32
+    from workloads.torch_io import tensor_of
+    rng = np.random.default_rng(t)
+    H, d, J = 2, 128, 100
+    copies = (t - 96) // J
+    n_big = t - J * copies
+    kf = np.zeros((1, H, t, d), np.float32)
+    vf = rng.normal(size=(1, H, t, d)).astype(np.float32)
+    for h in range(H):
+        # the large values 1 + k/128 (exact in bf16) keep the small keys' weights
+        # within a factor e^-1.8 of the largest, so delta and out test them too
+        vals = np.concatenate([np.repeat(2.0 ** -np.arange(J), copies), 1.0 + (1.0 + np.arange(n_big)) / 128])
+        kf[0, h, :, 0] = vals[rng.permutation(t)]
+    qf = np.zeros((1, H, d), np.float32)
+    qf[..., 0] = 1.0
+    kb, vb, qb = bf16_bits_from_f32(kf), bf16_bits_from_f32(vf), bf16_bits_from_f32(qf)
+    k, v, q = tensor_of(kb, "bf16", "cuda"), tensor_of(vb, "bf16", "cuda"), tensor_of(qb, "bf16", "cuda")
+    kv = S.KVCache(k, v, torch.tensor([t], dtype=torch.int32, device="cuda"), H)
+    N = n_big + copies * 50 + copies // 2   # the threshold inside the ties of 2^-50
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx = torch.full((1, H, N), -7, **i32)
+    n_sel = torch.full((1, H), -7, **i32)
+    delta = torch.zeros(1, H, device="cuda")
+    out = torch.zeros(1, H, d, device="cuda")
+    lse = torch.zeros(1, H, device="cuda")
+    ws = S.make_workspace(kv, N)
+    S.retrieve(kv, q[0], 1.0, N, idx, n_sel, delta, out, lse, ws)
+    assert S.last_error() == 0
+    gi, gn, gd, go, gl = [x.cpu().numpy() for x in (idx, n_sel, delta, out, lse)]
+    for h in range(H):
+        K, V = P.widen(kb[0, h], "bf16"), P.widen(vb[0, h], "bf16")
+        sc = P.scores(P.widen(qb[0, h], "bf16"), K, 1.0)
+        ref = P.top_n(sc, N)
+        assert gn[0, h] == N
+        assert (gi[0, h] == ref).all(), (h, np.flatnonzero(gi[0, h] != ref)[:5])
+        assert abs(gd[0, h] - P.dropped_mass(sc, ref)) <= DELTA_TOL
+        ro, rl = P.attention(P.widen(qb[0, h], "bf16"), K, V, ref, 1.0)
+        assert np.abs(go[0, h] - ro).max() <= OUT_TOL and abs(gl[0, h] - rl) <= LSE_TOL, h
+
+
 # --------------------------------------------------------------------------- #
 # CIS gate and dilation
 # --------------------------------------------------------------------------- #

@@ -422,6 +422,7 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
   a.ctas = attn_ctas(kv, sparse, cap, di->sms);
   a.min_rows = min_rows;
   a.cluster = sparse ? attn_cluster_size(kv, rows_hint > 0 ? rows_hint : cap, di->sms) : 0;
+  if (second_region && a.cluster > ATTN_SIDE_CLUSTER_MAX) a.cluster = ATTN_SIDE_CLUSTER_MAX;  // a decode step's side branch
   a.logits = sparse ? logits : nullptr;
   if (max_ctas > 0 && a.ctas > max_ctas) a.ctas = max_ctas;
   return launch_result(launch_attn(a, sparse, st), sparse ? "sparse attention" : "dense attention");

@@ -193,6 +193,11 @@ cudaError_t launch_attn(const AttnLaunch& a, bool sparse, cudaStream_t s);
 // Sparse attention with one thread-block cluster of a.cluster CTAs per query
 // head (batches with few heads; no workspace).
 constexpr int ATTN_CLUSTER_MAX = 8;
+// The decode step's reusing-heads branch runs beside the retrieval's
+// 16-CTA clusters; clusters of at most this many CTAs leave the SM room both
+// need (measured on the llama shape: 1.515 -> 1.597 M query-heads/s, though
+// the attention alone is 9.2 us with 8-CTA clusters against 11.3 with 4).
+constexpr int ATTN_SIDE_CLUSTER_MAX = 4;
 cudaError_t launch_attn_cluster(const AttnLaunch& a, cudaStream_t s);
 
 // Hooks into the C ABI layer for the library's other entry-point files:

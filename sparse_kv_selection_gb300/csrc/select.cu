@@ -122,6 +122,25 @@ __device__ __forceinline__ void find_bin(const unsigned* h, int nb, unsigned kre
   __syncthreads();
 }
 
+// The bin of the krem-th largest in a cluster: rank 0 scans the totals in its
+// own shared memory and writes the result into every rank's (remote reads of
+// 2048 counters by every rank cost several microseconds); one cluster barrier.
+template <bool ONE>
+__device__ __forceinline__ void find_bin_cluster(cg::cluster_group& cluster, SelClusterShared& sh,
+                                                 const unsigned* totals, int nb, unsigned krem,
+                                                 int CL, int rank) {
+  if (rank == 0) {
+    find_bin(totals, nb, krem, sh);
+    if (threadIdx.x < CL) {
+      SelClusterShared* rs = cluster.map_shared_rank(&sh, (int)threadIdx.x);
+      rs->digit = sh.digit;
+      rs->krem = sh.krem;
+      rs->cnt_bin = sh.cnt_bin;
+    }
+  }
+  cluster.sync();
+}
+
 __device__ __forceinline__ float float_of_key(unsigned k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
@@ -288,7 +307,8 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
     keq = (unsigned)Nb;
     cta_eq = (unsigned)cnt;
   } else {
-    find_bin(ONE ? sh.hist : root->histg[0], 2048, (unsigned)Nb, sh);
+    if (ONE) find_bin(sh.hist, 2048, (unsigned)Nb, sh);
+    else find_bin_cluster<ONE>(cluster, sh, sh.histg[0], 2048, (unsigned)Nb, CL, rank);
     const int b1 = (int)sh.digit;
     unsigned krem = sh.krem;
     const float lo1 = smin + (float)b1 * w1;
@@ -309,7 +329,8 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
         __syncthreads();
         head_sync<ONE>(cluster);
       }
-      find_bin(ONE ? sh.hist : root->histg[1], 2048, krem, sh);
+      if (ONE) find_bin(sh.hist, 2048, krem, sh);
+      else find_bin_cluster<ONE>(cluster, sh, sh.histg[1], 2048, krem, CL, rank);
       b2 = (int)sh.digit;
       krem = sh.krem;
     }

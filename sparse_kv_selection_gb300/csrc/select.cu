@@ -99,16 +99,10 @@ __device__ __forceinline__ void mirror_query(const SelectLaunch& a, int qh) {
 // Bin of a histogram (nb bins, highest first) holding the krem-th largest
 // element; `h` may live in another CTA's shared memory. Sets sh.digit, the
 // rank sh.krem inside that bin and its count sh.cnt_bin.
-__device__ __forceinline__ void find_bin(const unsigned* h, int nb, unsigned krem,
-                                         SelClusterShared& sh) {
-  const int per = nb / SEL_THREADS;  // 4 or 2
-  const int top = nb - 1 - per * threadIdx.x;
-  unsigned c[4] = {0u, 0u, 0u, 0u};
+__device__ __forceinline__ void find_bin_counts(const unsigned (&c)[4], int per, int top,
+                                                unsigned krem, SelClusterShared& sh) {
   unsigned sum = 0;
-  for (int k = 0; k < per; k++) {
-    c[k] = h[top - k];
-    sum += c[k];
-  }
+  for (int k = 0; k < per; k++) sum += c[k];
   unsigned total;
   unsigned run = scan_block(sum, sh.scan, total) - sum;
   for (int k = 0; k < per; k++) {
@@ -122,15 +116,59 @@ __device__ __forceinline__ void find_bin(const unsigned* h, int nb, unsigned kre
   __syncthreads();
 }
 
-// The bin of the krem-th largest in a cluster: rank 0 scans the totals in its
-// own shared memory and writes the result into every rank's (remote reads of
-// 2048 counters by every rank cost several microseconds); one cluster barrier.
+__device__ __forceinline__ void find_bin(const unsigned* h, int nb, unsigned krem,
+                                         SelClusterShared& sh) {
+  const int per = nb / SEL_THREADS;  // 4 or 2
+  const int top = nb - 1 - per * threadIdx.x;
+  unsigned c[4] = {0u, 0u, 0u, 0u};
+  for (int k = 0; k < per; k++) c[k] = h[top - k];
+  find_bin_counts(c, per, top, krem, sh);
+}
+
+// A cluster's histogram: every rank writes its 2048 counts, as 16-bit values
+// (a slice holds at most SELECT_SLICE_MAX keys), into its row of a table in
+// rank 0's shared memory (the cluster totals and fallback counters, unused
+// until the bins are found): 256 16-byte stores, no atomics. The caller then
+// passes a cluster barrier.
+constexpr int SEL_ROWS_MAX = 8;  // ranks a table holds: 8 rows of 2048 16-bit counts
+static_assert(SELECT_SLICE_MAX < 65536, "slice counts fit 16 bits");
+__device__ __forceinline__ void push_hist_row(cg::cluster_group& cluster, const SelClusterShared& sh,
+                                              int rank) {
+  const int t = threadIdx.x;
+  if (t < 2048 / 8) {
+    const unsigned* h = sh.hist + 8 * t;
+    const uint4 v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                               h[6] | (h[7] << 16));
+    SelClusterShared* root = cluster.map_shared_rank(const_cast<SelClusterShared*>(&sh), 0);
+    reinterpret_cast<uint4*>(&root->histg[0][0])[rank * (2048 / 8) + t] = v;
+  }
+}
+
+// The bin of the krem-th largest in a cluster's 2048-bin histogram: rank 0
+// adds the ranks' rows of its table as it scans them and writes the result
+// into every rank's shared memory (remote reads of 2048 counters by every rank
+// cost several microseconds); one cluster barrier.
 template <bool ONE>
 __device__ __forceinline__ void find_bin_cluster(cg::cluster_group& cluster, SelClusterShared& sh,
-                                                 const unsigned* totals, int nb, unsigned krem,
-                                                 int CL, int rank) {
+                                                 unsigned krem, int CL, int rank) {
   if (rank == 0) {
-    find_bin(totals, nb, krem, sh);
+    // Each thread adds its four bins (top-3 .. top, one 8-byte word of a row)
+    // over the ranks' rows.
+    static_assert(2048 / SEL_THREADS == 4, "four bins a thread");
+    const uint2* tab = reinterpret_cast<const uint2*>(&sh.histg[0][0]);
+    const int top = 2047 - 4 * (int)threadIdx.x;
+    unsigned c[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int r = 0; r < SEL_ROWS_MAX; r++) {
+      if (r < CL) {
+        const uint2 w = tab[r * (2048 / 4) + (top - 3) / 4];
+        c[3] += w.x & 0xffffu;
+        c[2] += w.x >> 16;
+        c[1] += w.y & 0xffffu;
+        c[0] += w.y >> 16;
+      }
+    }
+    find_bin_counts(c, 4, top, krem, sh);
     if (threadIdx.x < CL) {
       SelClusterShared* rs = cluster.map_shared_rank(&sh, (int)threadIdx.x);
       rs->digit = sh.digit;
@@ -239,8 +277,6 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
   const KVView& kv = a.kv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < 2048; i += SEL_THREADS) sh.hist[i] = 0;
-  if (!ONE && rank == 0)  // a single CTA finds its bins in its own histogram
-    for (int i = tid; i < 2 * 2048; i += SEL_THREADS) (&sh.histg[0][0])[i] = 0;
   if (tid == 0) {
     sh.ncand = 0;
     sh.nlcand = 0;
@@ -292,8 +328,7 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
     }
     if (!ONE) {
       __syncthreads();
-      for (int i = tid; i < 2048; i += SEL_THREADS)
-        if (sh.hist[i]) atomicAdd(&root->histg[0][i], sh.hist[i]);
+      push_hist_row(cluster, sh, rank);
     }
   }
   __syncthreads();
@@ -308,7 +343,7 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
     cta_eq = (unsigned)cnt;
   } else {
     if (ONE) find_bin(sh.hist, 2048, (unsigned)Nb, sh);
-    else find_bin_cluster<ONE>(cluster, sh, sh.histg[0], 2048, (unsigned)Nb, CL, rank);
+    else find_bin_cluster<ONE>(cluster, sh, (unsigned)Nb, CL, rank);
     const int b1 = (int)sh.digit;
     unsigned krem = sh.krem;
     const float lo1 = smin + (float)b1 * w1;
@@ -324,13 +359,12 @@ __device__ __forceinline__ void select_in_shared(const SelectLaunch& a, SelClust
       }
       __syncthreads();
       if (!ONE) {
-        for (int i = tid; i < 2048; i += SEL_THREADS)
-          if (sh.hist[i]) atomicAdd(&root->histg[1][i], sh.hist[i]);
+        push_hist_row(cluster, sh, rank);
         __syncthreads();
         head_sync<ONE>(cluster);
       }
       if (ONE) find_bin(sh.hist, 2048, krem, sh);
-      else find_bin_cluster<ONE>(cluster, sh, sh.histg[1], 2048, krem, CL, rank);
+      else find_bin_cluster<ONE>(cluster, sh, krem, CL, rank);
       b2 = (int)sh.digit;
       krem = sh.krem;
     }

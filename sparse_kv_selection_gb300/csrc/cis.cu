@@ -37,6 +37,10 @@ __device__ __forceinline__ double warp_sum_f64(double v) {
 }
 
 constexpr int CIS_PER = 4;  // anchor entries per thread per chunk
+// Dilated positions of one chunk staged in shared memory before they are
+// written (CIS_THREADS * CIS_PER anchor entries with w <= 4 always fit; a
+// chunk with more positions is written directly).
+constexpr int CIS_STAGE = CIS_THREADS * CIS_PER * 9;
 constexpr float CIS_MARGIN = 1e-4f;
 
 // Block-wide sum (all CIS_THREADS threads call it; `tot` is shared scratch
@@ -242,6 +246,7 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   __shared__ int sh_reuse;
   __shared__ int warp_tot[CIS_THREADS / 32];
   __shared__ int seg_cnt[CIS_CLUSTER_MAX];  // CLU: every rank's count of dilated positions
+  __shared__ int stage[CIS_STAGE];          // one chunk's dilated positions
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = CLU ? (int)cluster.num_blocks() : 1;
   const int rank = CLU ? (int)cluster.block_rank() : 0;
@@ -390,17 +395,32 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
     const int local = chunk_intervals(x, prev0, j0, seg_hi, t, w, ns, wlo, kv.err, start, cnt);
     int total;
     int pos = carry + block_excl_scan(local, warp_tot, &total);
+    if (total <= CIS_STAGE) {
+      // the chunk's positions are laid out in shared memory, then written
+      // by consecutive threads (each thread's runs written directly would
+      // scatter every warp store over several times the bytes it carries)
+      int lp = pos - carry;
 #pragma unroll
-    for (int k = 0; k < CIS_PER; k++) {
-      for (int e = 0; e < cnt[k]; e++) {
-        if (pos + e < a.cap) {
-          out[pos + e] = start[k] + e;
-        } else {
-          raise_error(kv.err, PRHS_DEV_CAPACITY);
-          break;
+      for (int k = 0; k < CIS_PER; k++)
+        for (int e = 0; e < cnt[k]; e++) stage[lp++] = start[k] + e;
+      __syncthreads();
+      const int room = max(0, min(total, a.cap - carry));
+      for (int i = tid; i < room; i += CIS_THREADS) out[carry + i] = stage[i];
+      if (tid == 0 && room < total) raise_error(kv.err, PRHS_DEV_CAPACITY);
+      __syncthreads();  // the stage is free for the next chunk
+    } else {
+#pragma unroll
+      for (int k = 0; k < CIS_PER; k++) {
+        for (int e = 0; e < cnt[k]; e++) {
+          if (pos + e < a.cap) {
+            out[pos + e] = start[k] + e;
+          } else {
+            raise_error(kv.err, PRHS_DEV_CAPACITY);
+            break;
+          }
         }
+        pos += cnt[k];
       }
-      pos += cnt[k];
     }
     carry += total;
   }

@@ -37,10 +37,17 @@ __device__ __forceinline__ double warp_sum_f64(double v) {
 }
 
 constexpr int CIS_PER = 4;  // anchor entries per thread per chunk
-// Dilated positions of one chunk staged in shared memory before they are
-// written (CIS_THREADS * CIS_PER anchor entries with w <= 4 always fit; a
-// chunk with more positions is written directly).
-constexpr int CIS_STAGE = CIS_THREADS * CIS_PER * 9;
+// Dilated positions of one chunk staged in dynamic shared memory before they
+// are written: room for CIS_THREADS * CIS_PER anchor entries of 2w + 1
+// positions each, at most CIS_STAGE_MAX (a chunk with more positions, w > 4,
+// is written directly). Sized by w so that short radii leave room for more
+// CTAs per SM.
+constexpr int CIS_STAGE_MAX = CIS_THREADS * CIS_PER * 9;
+__host__ __device__ __forceinline__ int cis_stage(int w, int n_den) {
+  if (n_den > 0) return 0;  // budgeted dilation writes directly
+  const long long s = (long long)CIS_THREADS * CIS_PER * (2ll * (w < 0 ? 0 : w) + 1);
+  return s < CIS_STAGE_MAX ? (int)s : CIS_STAGE_MAX;
+}
 constexpr float CIS_MARGIN = 1e-4f;
 
 // Block-wide sum (all CIS_THREADS threads call it; `tot` is shared scratch
@@ -246,7 +253,7 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
   __shared__ int sh_reuse;
   __shared__ int warp_tot[CIS_THREADS / 32];
   __shared__ int seg_cnt[CIS_CLUSTER_MAX];  // CLU: every rank's count of dilated positions
-  __shared__ int stage[CIS_STAGE];          // one chunk's dilated positions
+  extern __shared__ int stage[];            // one chunk's dilated positions (cis_stage ints)
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = CLU ? (int)cluster.num_blocks() : 1;
   const int rank = CLU ? (int)cluster.block_rank() : 0;
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(CIS_THREADS) cis_kernel(const CisLaunch a) {
     const int local = chunk_intervals(x, prev0, j0, seg_hi, t, w, ns, wlo, kv.err, start, cnt);
     int total;
     int pos = carry + block_excl_scan(local, warp_tot, &total);
-    if (total <= CIS_STAGE) {
+    if (total <= cis_stage(w, a.n_den)) {
       // the chunk's positions are laid out in shared memory, then written
       // by consecutive threads (each thread's runs written directly would
       // scatter every warp store over several times the bytes it carries)
@@ -448,11 +455,12 @@ static int cis_cluster(const CisLaunch& a, int sms) {
 template <typename T>
 static cudaError_t launch_cis_t(const CisLaunch& a, int cl, cudaStream_t st) {
   void (*k)(const CisLaunch) = cl == 1 ? cis_kernel<T, false> : cis_kernel<T, true>;
-  if (cl == 1) return launch_pdl(k, dim3(a.kv.B * a.kv.Hq), dim3(CIS_THREADS), 0, st, a.kv.pdl, a);
+  const size_t smem = (size_t)cis_stage(a.w, a.n_den) * sizeof(int);
+  if (cl == 1) return launch_pdl(k, dim3(a.kv.B * a.kv.Hq), dim3(CIS_THREADS), smem, st, a.kv.pdl, a);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.kv.B * a.kv.Hq * cl);
   cfg.blockDim = dim3(CIS_THREADS);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

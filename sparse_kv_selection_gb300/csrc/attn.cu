@@ -35,6 +35,7 @@ constexpr int ATTN_THREADS = 128;
 constexpr int ATTN_IDX_STAGE = 2048;
 constexpr int MERGE_CH = 32;  // partial records merged per shared-memory pass
 constexpr int ATTN_ALIGN_UNITS = 2048;  // most units for the unit-aligned split
+constexpr int ATTN_PB = 8;  // units whose counts a thread loads at once
 
 __device__ __forceinline__ int warp_sum_int(int v) {
 #pragma unroll
@@ -136,25 +137,38 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
   // ---- rows per unit and their prefix sums (every CTA computes the same) ----
   int nact;
   {
+    // ATTN_PB units per batch, all their loads issued before any is used (one
+    // round trip per batch instead of two dependent ones per unit)
     int loc = 0, act = 0;
-    for (int k = 0; k < per_t; k++) {
-      const int u = u0 + k;
-      if (u >= U) break;
-      int r;
-      if (SPARSE && a.unit_mask != nullptr && (a.unit_mask[u] != 0) != (a.mask_want != 0)) {
-        r = 0;  // another launch attends this unit
-      } else if (SPARSE) {
-        r = a.n_sel[u];
-        if (r < 0 || r > a.cap) {
+    for (int k0 = 0; k0 < per_t; k0 += ATTN_PB) {
+      int cnt[ATTN_PB];
+      bool skip[ATTN_PB];
+#pragma unroll
+      for (int i = 0; i < ATTN_PB; i++) {
+        const int u = u0 + k0 + i;
+        const bool in = k0 + i < per_t && u < U;
+        cnt[i] = !in ? 0 : SPARSE ? __ldg(a.n_sel + u) : __ldg(kv.seq_lens + (PER_QUERY ? u / kv.Hq : u / kv.Hkv));
+        // another launch attends the units the mask leaves out
+        skip[i] = SPARSE && in && a.unit_mask != nullptr &&
+                  (__ldg(a.unit_mask + u) != 0) != (a.mask_want != 0);
+      }
+#pragma unroll
+      for (int i = 0; i < ATTN_PB; i++) {
+        const int u = u0 + k0 + i;
+        if (k0 + i >= per_t || u >= U) break;
+        int r = cnt[i];
+        if (!SPARSE) {
+          r = checked_len(kv, r);
+        } else if (skip[i]) {
+          r = 0;
+        } else if (r < 0 || r > a.cap) {
           raise_error(kv.err, PRHS_DEV_CAPACITY);
           r = r < 0 ? 0 : a.cap;
         }
-      } else {
-        r = seq_len(kv, PER_QUERY ? u / kv.Hq : u / kv.Hkv);
+        sh_prefix[u] = r;  // temporarily the count
+        loc += r;
+        act += r > 0;
       }
-      sh_prefix[u] = r;  // temporarily the count
-      loc += r;
-      act += r > 0;
     }
     nact = block_scan(sh_prefix, loc, act);
   }

@@ -32,14 +32,20 @@ struct KVView {
   bool pdl;                    // launches overlap their stream predecessor's tail
 };
 
-// Length of sequence b, clamped to [0, t_max] (out-of-range lengths are flagged).
-__device__ __forceinline__ int seq_len(const KVView& kv, int b) {
-  int t = kv.seq_lens[b];
+// A loaded sequence length clamped to [0, t_max] (out-of-range lengths are
+// flagged). Loops that read many lengths load them all first and check them
+// after, so that the loads are not held behind a possible error write.
+__device__ __forceinline__ int checked_len(const KVView& kv, int t) {
   if (t < 0 || t > kv.t_max) {
     raise_error(kv.err, PRHS_DEV_BAD_LEN);
     t = t < 0 ? 0 : kv.t_max;
   }
   return t;
+}
+
+// Length of sequence b, clamped to [0, t_max] (out-of-range lengths are flagged).
+__device__ __forceinline__ int seq_len(const KVView& kv, int b) {
+  return checked_len(kv, kv.seq_lens[b]);
 }
 
 // Row number (in units of d elements) of key i of (b, kv head h); -1 when the

@@ -20,6 +20,8 @@ namespace prhs {
 // -------------------------------------------------------------------------- //
 // scoring
 // -------------------------------------------------------------------------- //
+constexpr int SCORE_PB = 8;  // KV heads whose lengths and skip flags a thread loads at once
+
 template <typename T, int D>
 struct ScoreShape {
   static constexpr int RB = D * (int)sizeof(T);        // bytes per key row
@@ -97,20 +99,32 @@ __global__ void __launch_bounds__(160) score_kernel(const __grid_constant__ CUte
   {
     const int per_t = (U + nthr - 1) / nthr;
     const int u0 = threadIdx.x * per_t;
+    // SCORE_PB units per batch, all their loads issued before any is used
     int loc = 0;
-    for (int k = 0; k < per_t; k++) {
-      const int u = u0 + k;
-      if (u >= U) break;
-      const int b = u / kv.Hkv, kvh = u % kv.Hkv;
-      bool need = a.head_skip == nullptr;
-      if (!need) {
-        const int qh0 = b * kv.Hq + kvh * G;
+    for (int k0 = 0; k0 < per_t; k0 += SCORE_PB) {
+      int len[SCORE_PB];
+      bool need[SCORE_PB];
 #pragma unroll
-        for (int g = 0; g < G; g++) need |= a.head_skip[qh0 + g] == 0;
+      for (int i = 0; i < SCORE_PB; i++) {
+        const int u = u0 + k0 + i;
+        const bool in = k0 + i < per_t && u < U;
+        const int b = u / kv.Hkv, kvh = u % kv.Hkv;
+        len[i] = in ? __ldg(kv.seq_lens + b) : 0;
+        need[i] = a.head_skip == nullptr;
+        if (in && !need[i]) {
+          const int qh0 = b * kv.Hq + kvh * G;
+#pragma unroll
+          for (int g = 0; g < G; g++) need[i] |= __ldg(a.head_skip + qh0 + g) == 0;
+        }
       }
-      const int tiles = need ? (seq_len(kv, b) + S::TK - 1) / S::TK : 0;
-      tprefix[u] = tiles;
-      loc += tiles;
+#pragma unroll
+      for (int i = 0; i < SCORE_PB; i++) {
+        const int u = u0 + k0 + i;
+        if (k0 + i >= per_t || u >= U) break;
+        const int tiles = need[i] ? (checked_len(kv, len[i]) + S::TK - 1) / S::TK : 0;
+        tprefix[u] = tiles;
+        loc += tiles;
+      }
     }
     int v = loc;
 #pragma unroll

@@ -37,6 +37,11 @@ constexpr int MERGE_CH = 32;  // partial records merged per shared-memory pass
 constexpr int ATTN_ALIGN_UNITS = 2048;  // most units for the unit-aligned split
 constexpr int ATTN_PB = 8;  // units whose counts a thread loads at once
 
+// Slot of unit u in the per-unit prefix arrays: one spare word after every 32,
+// so that threads owning runs of 2, 4, 8, 16 or 32 consecutive units reach 32
+// different banks.
+__host__ __device__ __forceinline__ int attn_sk(int u) { return u + (u >> 5); }
+
 __device__ __forceinline__ int warp_sum_int(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
@@ -79,7 +84,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
   // one buffer: the row numbers of a segment, or a chunk of partial records
   // while a unit is merged
   constexpr int BUF_FLOATS = (SPARSE && ATTN_IDX_STAGE > MERGE_CH * PW) ? ATTN_IDX_STAGE : MERGE_CH * PW;
-  // [units + 1] row prefix, then (aligned split) [units + 1] CTA prefix
+  // [units + 1] row prefix, then (aligned split) [units + 1] CTA prefix,
+  // both indexed through attn_sk
   extern __shared__ int sh_prefix[];
   __shared__ __align__(16) float sh_buf[BUF_FLOATS];
   int* const sh_idx = reinterpret_cast<int*>(sh_buf);
@@ -125,11 +131,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
     for (int k = 0; k < per_t; k++) {
       const int u = u0 + k;
       if (u >= U) break;
-      const int r = arr[u];
-      arr[u] = run;
+      const int r = arr[attn_sk(u)];
+      arr[attn_sk(u)] = run;
       run += r;
     }
-    if (tid == ATTN_THREADS - 1) arr[U] = run;
+    if (tid == ATTN_THREADS - 1) arr[attn_sk(U)] = run;
     __syncthreads();
     return nact;
   };
@@ -165,18 +171,18 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
           raise_error(kv.err, PRHS_DEV_CAPACITY);
           r = r < 0 ? 0 : a.cap;
         }
-        sh_prefix[u] = r;  // temporarily the count
+        sh_prefix[attn_sk(u)] = r;  // temporarily the count
         loc += r;
         act += r > 0;
       }
     }
     nact = block_scan(sh_prefix, loc, act);
   }
-  const int total = sh_prefix[U];
+  const int total = sh_prefix[attn_sk(U)];
 
   // ---- units with no rows: out = 0, lse = -inf ----
   for (int u = c; u < U; u += C) {
-    if (sh_prefix[u + 1] != sh_prefix[u]) continue;
+    if (sh_prefix[attn_sk(u + 1)] != sh_prefix[attn_sk(u)]) continue;
     if (SPARSE && a.unit_mask != nullptr && (a.unit_mask[u] != 0) != (a.mask_want != 0)) continue;
     const int qh0 = PER_QUERY ? u : (u / kv.Hkv) * kv.Hq + (u % kv.Hkv) * G;
     for (int x = tid; x < G * D; x += ATTN_THREADS) {
@@ -195,15 +201,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
   const int min_rows = max(a.min_rows, 1);
   const bool aligned = U <= ATTN_ALIGN_UNITS && 2 * nact <= C;
   int per;
-  int* const sh_cpre = sh_prefix + (U + 1);
+  int* const sh_cpre = sh_prefix + attn_sk(U) + 1;
   if (aligned) {
     per = max(min_rows, (total + (C - nact) - 1) / (C - nact));
     int loc = 0;
     for (int k = 0; k < per_t; k++) {
       const int u = u0 + k;
       if (u >= U) break;
-      const int n = (sh_prefix[u + 1] - sh_prefix[u] + per - 1) / per;
-      sh_cpre[u] = n;
+      const int n = (sh_prefix[attn_sk(u + 1)] - sh_prefix[attn_sk(u)] + per - 1) / per;
+      sh_cpre[attn_sk(u)] = n;
       loc += n;
     }
     block_scan(sh_cpre, loc, 0);
@@ -480,14 +486,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
   };
 
   if (aligned) {
-    if (c >= sh_cpre[U]) return;  // more CTAs than the split needs
+    if (c >= sh_cpre[attn_sk(U)]) return;  // more CTAs than the split needs
     int ulo = 0, uhi = U - 1;     // the unit: largest u with CP[u] <= c
     while (ulo < uhi) {
       const int mid = (ulo + uhi + 1) >> 1;
-      if (sh_cpre[mid] <= c) ulo = mid; else uhi = mid - 1;
+      if (sh_cpre[attn_sk(mid)] <= c) ulo = mid; else uhi = mid - 1;
     }
-    const int cf = sh_cpre[ulo], n = sh_cpre[ulo + 1] - cf, k = c - cf;
-    const int ru = sh_prefix[ulo + 1] - sh_prefix[ulo];
+    const int cf = sh_cpre[attn_sk(ulo)], n = sh_cpre[attn_sk(ulo + 1)] - cf, k = c - cf;
+    const int ru = sh_prefix[attn_sk(ulo + 1)] - sh_prefix[attn_sk(ulo)];
     process(ulo, (int)((long long)k * ru / n), (int)((long long)(k + 1) * ru / n), cf, cf + n - 1);
     return;
   }
@@ -497,10 +503,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
   int ulo = 0, uhi = U - 1;
   while (ulo < uhi) {
     const int mid = (ulo + uhi + 1) >> 1;
-    if (sh_prefix[mid] <= lo) ulo = mid; else uhi = mid - 1;
+    if (sh_prefix[attn_sk(mid)] <= lo) ulo = mid; else uhi = mid - 1;
   }
-  for (int u = ulo; u < U && sh_prefix[u] < hi; u++) {
-    const int P0 = sh_prefix[u], P1 = sh_prefix[u + 1];
+  for (int u = ulo; u < U && sh_prefix[attn_sk(u)] < hi; u++) {
+    const int P0 = sh_prefix[attn_sk(u)], P1 = sh_prefix[attn_sk(u + 1)];
     const int r0 = max(lo, P0) - P0, r1 = min(hi, P1) - P0;
     if (r0 < r1) process(u, r0, r1, P0 / per, (P1 - 1) / per);
   }
@@ -517,7 +523,7 @@ size_t attn_partial_floats(const KVView& kv, bool sparse, int ctas) {
 template <typename T, int D, int G, bool SPARSE, bool LG>
 static cudaError_t attn_go(const AttnLaunch& a, cudaStream_t st) {
   const size_t units = (size_t)attn_units(a.kv, SPARSE);
-  const size_t smem = (units + 1) * sizeof(int) * (units <= (size_t)ATTN_ALIGN_UNITS ? 2 : 1);
+  const size_t smem = ((size_t)attn_sk((int)units) + 1) * sizeof(int) * (units <= (size_t)ATTN_ALIGN_UNITS ? 2 : 1);
   auto k = attn_kernel<T, D, G, SPARSE, LG>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -803,16 +803,37 @@ prhs_status prhs_decode_step(const prhs_kv* kv, const void* q, const void* gate,
   SideBranch* br = nullptr;
   if ((s = side_branch(di, stream, &br)) != PRHS_OK) return s;
   std::lock_guard<std::mutex> branch_lock(br->mu);
+  // Scoring first, on its own, when what follows it on the retrieving branch
+  // is small beside the reusing heads' attention: a one-CTA selection per head
+  // with at most one head per SM, and a V-only attention without clusters.
+  // Their CTAs then run beside that attention instead of after it. Larger
+  // retrieving branches keep the order below: the attention splits its rows
+  // evenly over one wave of CTAs, so kernels that take SM room at its start
+  // hold back the CTAs they displace and the whole launch ends later.
+  const KVView vv = view_of(*kv, di->err);
+  const bool fused = !forced && score_select_fits(vv);
+  const bool score_first = !forced && !fused && vv.t_max <= SELECT_SLICE_ONE &&
+                           (long long)kv->B * kv->Hq <= di->sms &&
+                           attn_cluster_size(*kv, anchor_cap, di->sms) == 0;
+  if (score_first && (s = do_score(*kv, di, L, ws, q, scale, reuse, stream)) != PRHS_OK) return s;
   cudaError_t e = cudaEventRecord(br->fork, stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(br->side, br->fork, 0);
   if (e != cudaSuccess) return cuda_fail(e, "decode: fork");
   // The branch more likely to be the longer one is issued first, so its CTAs
   // are placed first: the one-launch retrieval on short caches, the reusing
   // heads' attention otherwise (measured both ways on 4K-, 32K- and 128K-key
-  // caches). The retrieving heads' sets hold at most anchor_cap (+ forced) rows.
-  const bool retrieve_first = !forced && score_select_fits(view_of(*kv, di->err));
+  // caches); after scoring first, the selection and V-only attention, which
+  // take few SMs. The retrieving heads' sets hold at most anchor_cap (+ forced) rows.
+  const bool retrieve_first = fused || score_first;
   for (int branch = 0; branch < 2 && s == PRHS_OK; branch++) {
-    if ((branch == 0) == retrieve_first) {
+    if ((branch == 0) == retrieve_first && score_first) {
+      s = do_select(*kv, di, L, ws, q, N, n_budget, n_sink, window, reuse, idx, n_sel, cap, delta,
+                    anchor_idx, anchor_n, anchor_cap, q_anchor, stream, gv);
+      if (s == PRHS_OK)
+        s = do_attn(*kv, di, L, ws, q, scale, idx, n_sel, cap, out, lse, true, stream, reuse, 0, false,
+                    0, ATTN_MIN_ROWS, anchor_cap,
+                    reinterpret_cast<const float*>(static_cast<const char*>(ws) + L.scores));
+    } else if ((branch == 0) == retrieve_first) {
       s = do_retrieve(*kv, di, L, ws, q, scale, N, n_budget, n_sink, window, reuse, idx, n_sel, cap,
                       delta, anchor_idx, anchor_n, anchor_cap, q_anchor, out, lse,
                       anchor_cap + n_sink + window, stream, gv);

@@ -33,6 +33,11 @@ CASES = {
     # t_max above 8192: separate scoring, selection and attention launches
     "bf16_9k_mha": dict(dtype="bf16", B=1, Hq=2, Hkv=2, d=128, t=(8500, 9500), t_max=9600,
                         n_clusters=32, steps=4, N=256, w=2),
+    # t_max above 8192 with at most one head per SM and no cluster attention
+    # (128 heads x 1300 anchors): the decode step scores before the branches
+    # fork, then selects and attends the retrieving heads beside the others
+    "gqa4_12k_score_first": dict(dtype="bf16", B=4, Hq=32, Hkv=8, d=128, t=(9000, 12000),
+                                 t_max=12000, n_clusters=40, steps=4, N=1300, w=2),
     # a cache of one key: every budget covers it (set = {0}, delta = 0)
     "t1_bf16": dict(dtype="bf16", B=2, Hq=2, Hkv=2, d=128, t=1, n_clusters=0, steps=4, N=4, w=2),
     "t1_paged_f32": dict(dtype="f32", B=2, Hq=4, Hkv=1, d=64, t=1, paged=True, block_size=16,

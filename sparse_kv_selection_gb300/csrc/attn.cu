@@ -18,7 +18,7 @@
 // Gather. Eight lanes share a row: lane j reads 16-byte chunks j, j+8, ... of
 // the K and V rows (128 contiguous bytes per 8 lanes per load), so every
 // gathered row arrives as full cache lines. A warp keeps 4 rows per step and
-// UNROLL steps in flight; the row numbers of a segment are staged in shared
+// several steps in flight; the row numbers of a segment are staged in shared
 // memory first. Softmax is online in fp32 and base 2 (logits pre-scaled by
 // log2 e). Units are query heads in both kernels; the kernel template can
 // also give one unit the G query heads of a KV head (registers per thread
@@ -27,6 +27,8 @@
 // Logit source (LG). After a fresh selection the logits of every key are
 // still in the workspace: the retrieving heads' attention then reads each
 // selected row's logit (4 bytes) and its V row only, not its K row.
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace prhs {
@@ -77,8 +79,6 @@ template <typename T, int D, int G, bool SPARSE, bool LG>
 __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch a) {
   using S = AttnShape<T, D>;
   static_assert(!LG || (SPARSE && G == 1), "logit source: sparse, one query head per unit");
-  constexpr int UNROLL = AttnUnroll<S::CPL, G>::value * (LG ? 2 : 1);
-  constexpr int STEP = 16 * UNROLL;  // rows per CTA iteration
   constexpr int PW = D + 4;          // partial record: m, l, 2 pad, o[D] (16-byte aligned)
   static_assert(D <= ATTN_THREADS && D % 64 == 0, "merge maps one thread per output element");
   // one buffer: the row numbers of a segment, or a chunk of partial records
@@ -271,18 +271,17 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
       for (int e = 0; e < S::EL; e++) o[g][e] = 0.f;
     }
 
-    for (int sb = r0; sb < r1; sb += (SPARSE ? ATTN_IDX_STAGE : (r1 - r0))) {
-      const int se = SPARSE ? min(r1, sb + ATTN_IDX_STAGE) : r1;
-      if (SPARSE && sb != r0) {
-        __syncthreads();
-        for (int x = tid; x < se - sb; x += ATTN_THREADS) sh_idx[x] = rows[sb + x];
-        __syncthreads();
-      }
-      for (int base = sb; base < se; base += STEP) {
-        long long row[UNROLL];
-        int keyv[UNROLL];
+    // Rows [sb, se) of the staged segment, weights from K (LGU false) or
+    // from the logits (LGU true); UR rows per lane group in flight. One body
+    // per weight source, so each keeps its loads together.
+    auto run_rows = [&](auto lg_tag, const int sb, const int se) {
+      constexpr bool LGU = decltype(lg_tag)::value;
+      constexpr int UR = AttnUnroll<S::CPL, G>::value * (LGU ? 2 : 1);
+      for (int base = sb; base < se; base += 16 * UR) {
+        long long row[UR];
+        int keyv[UR];
 #pragma unroll
-        for (int uu = 0; uu < UNROLL; uu++) {
+        for (int uu = 0; uu < UR; uu++) {
           const int r = base + uu * 16 + warp * 4 + sg;
           row[uu] = -1;
           keyv[uu] = 0;
@@ -297,60 +296,60 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
             }
           }
         }
-        uint4 kc[LG ? 1 : UNROLL][S::CPL], vc[UNROLL][S::CPL];
-        float lg[LG ? UNROLL : 1];
+        uint4 kc[LGU ? 1 : UR][S::CPL], vc[UR][S::CPL];
+        float lg[LGU ? UR : 1];
 #pragma unroll
-        for (int uu = 0; uu < UNROLL; uu++) {
-          if (LG) lg[uu] = row[uu] >= 0 ? __ldg(lrow + keyv[uu]) : 0.f;
+        for (int uu = 0; uu < UR; uu++) {
+          if constexpr (LGU) lg[uu] = row[uu] >= 0 ? __ldg(lrow + keyv[uu]) : 0.f;
 #pragma unroll
           for (int cc = 0; cc < S::CPL; cc++) {
             if (row[uu] >= 0) {
-              if (!LG) kc[uu][cc] = ldg_stream(kbase + row[uu] * S::RB + (cc * 8 + j) * 16);
+              if constexpr (!LGU) kc[uu][cc] = ldg_stream(kbase + row[uu] * S::RB + (cc * 8 + j) * 16);
               vc[uu][cc] = ldg_stream(vbase + row[uu] * S::RB + (cc * 8 + j) * 16);
             } else {
-              if (!LG) kc[uu][cc] = make_uint4(0, 0, 0, 0);
+              if constexpr (!LGU) kc[uu][cc] = make_uint4(0, 0, 0, 0);
               vc[uu][cc] = make_uint4(0, 0, 0, 0);
             }
           }
         }
-        float s[UNROLL][G];
+        float s[UR][G];
 #pragma unroll
-        for (int uu = 0; uu < UNROLL; uu++) {
-          if (LG) {
+        for (int uu = 0; uu < UR; uu++) {
+          if constexpr (LGU) {
             s[uu][0] = row[uu] >= 0 ? lg[uu] * LOG2E : -INFINITY;
-            continue;
-          }
-          float kf[S::EL];
+          } else {
+            float kf[S::EL];
 #pragma unroll
-          for (int cc = 0; cc < S::CPL; cc++) Elem<T>::unpack(kc[LG ? 0 : uu][cc], kf + cc * S::EPC);
+            for (int cc = 0; cc < S::CPL; cc++) Elem<T>::unpack(kc[uu][cc], kf + cc * S::EPC);
 #pragma unroll
-          for (int g = 0; g < G; g++) {
-            float acc = 0.f;
+            for (int g = 0; g < G; g++) {
+              float acc = 0.f;
 #pragma unroll
-            for (int e = 0; e < S::EL; e++) acc = fmaf(qf[g][e], kf[e], acc);
-            acc += __shfl_xor_sync(FULL_MASK, acc, 1);
-            acc += __shfl_xor_sync(FULL_MASK, acc, 2);
-            acc += __shfl_xor_sync(FULL_MASK, acc, 4);
-            s[uu][g] = row[uu] >= 0 ? acc : -INFINITY;
+              for (int e = 0; e < S::EL; e++) acc = fmaf(qf[g][e], kf[e], acc);
+              acc += __shfl_xor_sync(FULL_MASK, acc, 1);
+              acc += __shfl_xor_sync(FULL_MASK, acc, 2);
+              acc += __shfl_xor_sync(FULL_MASK, acc, 4);
+              s[uu][g] = row[uu] >= 0 ? acc : -INFINITY;
+            }
           }
         }
-        float vf[UNROLL][S::EL];
+        float vf[UR][S::EL];
 #pragma unroll
-        for (int uu = 0; uu < UNROLL; uu++)
+        for (int uu = 0; uu < UR; uu++)
 #pragma unroll
           for (int cc = 0; cc < S::CPL; cc++) Elem<T>::unpack(vc[uu][cc], vf[uu] + cc * S::EPC);
 #pragma unroll
         for (int g = 0; g < G; g++) {
           float mx = m[g];
 #pragma unroll
-          for (int uu = 0; uu < UNROLL; uu++) mx = fmaxf(mx, s[uu][g]);
+          for (int uu = 0; uu < UR; uu++) mx = fmaxf(mx, s[uu][g]);
           if (mx == -INFINITY) continue;
           const float corr = exp2f(m[g] - mx);
           l[g] *= corr;
 #pragma unroll
           for (int e = 0; e < S::EL; e++) o[g][e] *= corr;
 #pragma unroll
-          for (int uu = 0; uu < UNROLL; uu++) {
+          for (int uu = 0; uu < UR; uu++) {
             const float p = exp2f(s[uu][g] - mx);
             l[g] += p;
 #pragma unroll
@@ -359,6 +358,16 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
           m[g] = mx;
         }
       }
+    };
+
+    for (int sb = r0; sb < r1; sb += (SPARSE ? ATTN_IDX_STAGE : (r1 - r0))) {
+      const int se = SPARSE ? min(r1, sb + ATTN_IDX_STAGE) : r1;
+      if (SPARSE && sb != r0) {
+        __syncthreads();
+        for (int x = tid; x < se - sb; x += ATTN_THREADS) sh_idx[x] = rows[sb + x];
+        __syncthreads();
+      }
+      run_rows(std::integral_constant<bool, LG>{}, sb, se);
     }
 
     // ---- merge the 4 row groups of each warp, then the 4 warps ----

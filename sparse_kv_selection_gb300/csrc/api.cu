@@ -194,13 +194,14 @@ size_t elem_size(prhs_dtype dt) { return dt == PRHS_BF16 ? 2 : 4; }
 constexpr int ATTN_CTAS_PER_SM = 4;
 constexpr int SCORE_CTAS_PER_SM = 2;
 
-// CTAs of the attention kernels: enough for every SM to hold four, fewer
-// when the rows can be bounded from the host (about 32 rows per CTA).
-int attn_ctas(const prhs_kv& kv, bool sparse, int cap, int sms) {
+// CTAs of the attention kernels: enough for every SM to hold per_sm (four
+// for the K-and-V form, ATTN_LG_CTAS_PER_SM for the V-only one), fewer when
+// the rows can be bounded from the host (about 32 rows per CTA).
+int attn_ctas(const prhs_kv& kv, bool sparse, int cap, int sms, int per_sm = ATTN_CTAS_PER_SM) {
   const long long units = (long long)kv.B * kv.Hq;  // both kernels split by query head
   const long long rows = units * (sparse ? cap : t_max_of(kv));
   long long c = (rows + 31) / 32;
-  const long long most = (long long)ATTN_CTAS_PER_SM * sms;
+  const long long most = (long long)per_sm * sms;
   if (c > most) c = most;
   return c < 1 ? 1 : (int)c;
 }
@@ -230,7 +231,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 Layout layout_of(const prhs_kv& kv, int sms) {
   Layout L;
   const KVView v = view_of(kv, nullptr);
-  const int most = ATTN_CTAS_PER_SM * sms;
+  const int most = (ATTN_CTAS_PER_SM > ATTN_LG_CTAS_PER_SM ? ATTN_CTAS_PER_SM : ATTN_LG_CTAS_PER_SM) * sms;
   const size_t ps = attn_partial_floats(v, true, most);
   const size_t pd0 = dense_partial_floats(v, sms);
   const size_t pd = pd0 > ps ? pd0 : ps;
@@ -424,6 +425,7 @@ prhs_status do_attn(const prhs_kv& kv, DeviceInfo* di, const Layout& L, void* ws
   a.cluster = sparse ? attn_cluster_size(kv, rows_hint > 0 ? rows_hint : cap, di->sms) : 0;
   if (second_region && a.cluster > ATTN_SIDE_CLUSTER_MAX) a.cluster = ATTN_SIDE_CLUSTER_MAX;  // a decode step's side branch
   a.logits = sparse ? logits : nullptr;
+  if (a.logits != nullptr) a.ctas = attn_ctas(kv, sparse, cap, di->sms, ATTN_LG_CTAS_PER_SM);
   if (max_ctas > 0 && a.ctas > max_ctas) a.ctas = max_ctas;
   return launch_result(launch_attn(a, sparse, st), sparse ? "sparse attention" : "dense attention");
 }

@@ -76,7 +76,7 @@ __device__ __forceinline__ void merge_coeffs(float m1, float m2, float& M, float
 }
 
 template <typename T, int D, int G, bool SPARSE, bool LG>
-__global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch a) {
+__global__ void __launch_bounds__(ATTN_THREADS, LG ? ATTN_LG_CTAS_PER_SM : 4) attn_kernel(const AttnLaunch a) {
   using S = AttnShape<T, D>;
   static_assert(!LG || (SPARSE && G == 1), "logit source: sparse, one query head per unit");
   constexpr int PW = D + 4;          // partial record: m, l, 2 pad, o[D] (16-byte aligned)
@@ -273,10 +273,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(const AttnLaunch 
 
     // Rows [sb, se) of the staged segment, weights from K (LGU false) or
     // from the logits (LGU true); UR rows per lane group in flight. One body
-    // per weight source, so each keeps its loads together.
+    // per weight source, so each keeps its loads together. (The V-only form
+    // runs ATTN_LG_CTAS_PER_SM CTAs per SM at the same UR: more warps hide
+    // its short chains better than twice the rows per warp at four CTAs.)
     auto run_rows = [&](auto lg_tag, const int sb, const int se) {
       constexpr bool LGU = decltype(lg_tag)::value;
-      constexpr int UR = AttnUnroll<S::CPL, G>::value * (LGU ? 2 : 1);
+      constexpr int UR = AttnUnroll<S::CPL, G>::value;
       for (int base = sb; base < se; base += 16 * UR) {
         long long row[UR];
         int keyv[UR];

@@ -93,6 +93,9 @@ struct CisLaunch {
 // fixed per-CTA cost (prefix, index staging, partial record, merge) outweighs
 // the extra parallelism.
 constexpr int ATTN_MIN_ROWS = 64;
+// CTAs per SM of the V-only (logit-source) attention: its register budget
+// allows six 128-thread CTAs where the K-and-V form fits four.
+constexpr int ATTN_LG_CTAS_PER_SM = 6;
 // The same floor for the reusing heads' branch of a decode step, which runs
 // beside the retrieving heads' scoring and selection: when the reused sets
 // are small, fewer and fuller CTAs leave room on the SMs for those kernels.

@@ -326,6 +326,39 @@ def test_score_select_head_skip_and_full_budget():
             assert gn[b, h] == t and gd[b, h] == 0.0 and (gi[b, h] == np.arange(t)).all()
 
 
+@pytest.mark.parametrize("paged", [False, True])
+def test_score_select_one_head_per_kv_head_long(paged):
+    """prhs_score then prhs_select on caches above 8192 keys with one query
+    head per KV head: ragged lengths from 9000 to 40000 keys, contiguous and
+    paged (one TMA box per page), a third of the heads skipped; the sets and
+    dropped masses of the scored heads against the oracle."""
+    import sparse_kv_selection_gb300 as S
+    from workloads.torch_io import upload
+    wl = make_workload("mha_long", dtype="bf16", B=2, Hq=3, Hkv=3, d=128, t=(9000, 40000),
+                       paged=paged, block_size=16, n_clusters=40, steps=1, N=700, w=1)
+    dev = upload(wl)
+    kv = S.KVCache(dev["k"], dev["v"], dev["seq_lens"], wl.Hq, block_table=dev["block_table"])
+    N = 700
+    skip = np.zeros((wl.B, wl.Hq), np.uint8)
+    skip[0, 1] = skip[1, 0] = 1
+    idx = torch.full((wl.B, wl.Hq, N), -1, dtype=torch.int32, device="cuda")
+    n_sel = torch.zeros(wl.B, wl.Hq, dtype=torch.int32, device="cuda")
+    delta = torch.zeros(wl.B, wl.Hq, device="cuda")
+    ws = S.make_workspace(kv, N)
+    S.binding.score(kv, dev["q"][0], wl.scale, ws, head_skip=torch.from_numpy(skip).cuda())
+    S.binding.select(kv, dev["q"][0], N, idx, n_sel, delta, ws, head_skip=torch.from_numpy(skip).cuda())
+    assert S.last_error() == 0
+    gi, gn, gd = idx.cpu().numpy(), n_sel.cpu().numpy(), delta.cpu().numpy()
+    for b, h in _heads(wl):
+        if skip[b, h]:
+            continue
+        K, _ = kv_rows64(wl, b, h)
+        sc = P.scores(q64(wl, 0, b, h), K, wl.scale)
+        gset = gi[b, h, :gn[b, h]]
+        check_topn(gset, sc, N)
+        assert abs(gd[b, h] - P.dropped_mass(sc, gset)) <= DELTA_TOL, (b, h)
+
+
 @pytest.mark.parametrize("t,N", [(70001, 1500), (49153, 3), (200003, 777)])
 def test_score_select_long_cache(t, N):
     """Long caches: logits split over a cluster of CTAs, and (200003 keys,

@@ -240,7 +240,9 @@ prhs_status prhs_dense_attn(const prhs_kv* kv, const void* q, float scale, float
  *   prhs_cis_dilate(anchor -> idx, reuse);
  *   the reusing heads: prhs_sparse_attn(idx) on an internal side stream;
  *   the others: prhs_retrieve(head_skip = reuse, anchor outputs = the anchor
- *   buffers) on `stream`, which then waits for the side stream.
+ *   buffers) on `stream`, which then waits for the side stream (when the
+ *   retrieving branch is small, its scoring runs before the side stream
+ *   forks and the rest beside the side stream; results are the same).
  * Heads that reuse attend the dilated anchor set; the others retrieve a fresh
  * top-N set, attend it and make it (with the gated vector) the new anchor.
  * delta is written for retrieving heads only. Start a sequence with anchor_n

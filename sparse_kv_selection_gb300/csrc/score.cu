@@ -175,57 +175,68 @@ __global__ void __launch_bounds__(160) score_kernel(const __grid_constant__ CUte
 
   if (warp == S::NW) {
     // ------- producer warp: lane 0 paces the ring, lanes issue the TMA boxes -------
-    // The tiles of a CTA are consecutive: the next tile follows the current
-    // one in its head and a search runs only where a head ends. Its page rows
-    // are looked up (one lane per 16-row box) before the wait for the free
-    // slot, so those loads overlap the wait instead of following it.
     if (lane == 0) prefetch_tmap(&tmap);
     int issued = 0;
-    int u, tile0;
-    tile_at(0, u, tile0);
-    int len = seq_len(kv, u / kv.Hkv);
-    auto box_row = [&](int uu, int t0, int ln) -> long long {
-      const int nb = min(S::TK / PAGED_BOX_ROWS, (min(ln, t0 + S::TK) - t0 + PAGED_BOX_ROWS - 1) / PAGED_BOX_ROWS);
-      if (!a.paged || lane >= nb) return 0;
-      long long row = kv_row(kv, uu / kv.Hkv, uu % kv.Hkv, t0 + lane * PAGED_BOX_ROWS);
-      if (row < 0) {
-        raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
-        row = 0;
-      }
-      return row;
-    };
-    long long row_next = box_row(u, tile0, len);
-    for (int it = 0; it < ntiles; it++) {
-      const int s = it % S::STAGES;
-      const int cu = u, ct0 = tile0, clen = len;
-      const long long row = row_next;
-      if (it + 1 < ntiles) {
-        tile0 += S::TK;
-        if (tile0 >= len) {
-          tile_at(it + 1, u, tile0);
-          len = seq_len(kv, u / kv.Hkv);
-        }
-        row_next = box_row(u, tile0, len);
-      }
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&empty[s], ((it / S::STAGES) & 1) ^ 1, kv.err);
-      if (!__shfl_sync(FULL_MASK, ok, 0)) break;
-      uint8_t* dst = smem + s * S::STAGE_BYTES;
-      if (!a.paged) {
+    if (!a.paged) {
+      // contiguous caches: one 3-D box per tile
+      for (int it = 0; it < ntiles; it++) {
+        const int s = it % S::STAGES;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&empty[s], ((it / S::STAGES) & 1) ^ 1, kv.err);
+        if (!__shfl_sync(FULL_MASK, ok, 0)) break;
+        int u, tile0;
+        tile_at(it, u, tile0);
         if (lane == 0) {
+          uint8_t* dst = smem + s * S::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
-          tma_load_3d(dst, &tmap, 0, 0, cu * kv.t_max + ct0, &full[s]);
+          tma_load_3d(dst, &tmap, 0, 0, u * kv.t_max + tile0, &full[s]);
         }
-      } else {
-        // one 16-row box per page slice
+        __syncwarp();
+        issued = it + 1;
+      }
+    } else {
+      // paged caches: one 16-row box per page, one lane per box. The tiles of
+      // a CTA are consecutive: the next tile follows the current one in its
+      // head (a search only where a head ends), and its page rows are looked
+      // up before the wait for the free slot, so those loads overlap the wait.
+      int u, tile0;
+      tile_at(0, u, tile0);
+      int len = seq_len(kv, u / kv.Hkv);
+      auto box_row = [&](int uu, int t0, int ln) -> long long {
+        const int nb = min(S::TK / PAGED_BOX_ROWS, (min(ln, t0 + S::TK) - t0 + PAGED_BOX_ROWS - 1) / PAGED_BOX_ROWS);
+        if (lane >= nb) return 0;
+        long long row = kv_row(kv, uu / kv.Hkv, uu % kv.Hkv, t0 + lane * PAGED_BOX_ROWS);
+        if (row < 0) {
+          raise_error(kv.err, PRHS_DEV_BAD_BLOCK);
+          row = 0;
+        }
+        return row;
+      };
+      long long row_next = box_row(u, tile0, len);
+      for (int it = 0; it < ntiles; it++) {
+        const int s = it % S::STAGES;
+        const int ct0 = tile0, clen = len;
+        const long long row = row_next;
+        if (it + 1 < ntiles) {
+          tile0 += S::TK;
+          if (tile0 >= len) {
+            tile_at(it + 1, u, tile0);
+            len = seq_len(kv, u / kv.Hkv);
+          }
+          row_next = box_row(u, tile0, len);
+        }
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&empty[s], ((it / S::STAGES) & 1) ^ 1, kv.err);
+        if (!__shfl_sync(FULL_MASK, ok, 0)) break;
+        uint8_t* dst = smem + s * S::STAGE_BYTES;
         const int k1 = min(clen, ct0 + S::TK);
         const int nbox = min(S::TK / PAGED_BOX_ROWS, (k1 - ct0 + PAGED_BOX_ROWS - 1) / PAGED_BOX_ROWS);
         if (lane == 0) mbar_arrive_expect_tx(&full[s], nbox * PAGED_BOX_ROWS * S::RB);
         __syncwarp();
         if (lane < nbox) tma_load_3d(dst + lane * PAGED_BOX_ROWS * S::RB, &tmap, 0, 0, (int)row, &full[s]);
+        __syncwarp();
+        issued = it + 1;
       }
-      __syncwarp();
-      issued = it + 1;
     }
     // never leave while a copy into this CTA's shared memory is in flight
     if (lane == 0)

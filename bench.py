@@ -68,6 +68,9 @@ def parse_args():
                    help="time each kernel alone on the workload (all heads retrieving) instead")
     p.add_argument("--only", default=None,
                    help="with --kernels: time just this case (e.g. sparse_attn_dilated)")
+    p.add_argument("--batch", type=int, default=0,
+                   help="with --kernels: this many sequences of the workload instead of its own "
+                        "batch (a smaller case for profiling)")
     return p.parse_args()
 
 
@@ -793,7 +796,8 @@ def run_kernels(args):
     from workloads import preset
     from workloads.torch_io import upload
 
-    wl = preset(args.config, seed=0)
+    batch = getattr(args, "batch", 0)
+    wl = preset(args.config, seed=0, **({"B": batch} if batch > 0 else {}))
     dev = upload(wl)
     B, Hq, d = wl.B, wl.Hq, wl.d
     es = 2 if wl.dtype == "bf16" else 4
